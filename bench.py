@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Muon step.
+
+One step = one full Muon step (momentum/Nesterov, Frobenius normalisation,
+5 quintic Newton-Schulz iterations, decoupled update) over every hidden 2-D
+matrix of a Llama-3-8B-shaped weight set (32 layers; q, o 4096x4096;
+k, v 1024x4096; gate, up 14336x4096; down 4096x14336; bf16 params and
+grads, fp32 momentum), synthetic seeded inputs resident in HBM.
+
+Prints one JSON line.  `value` is the Newton-Schulz throughput in TFLOP/s
+(algorithmic flops: symmetric products on one triangle) of the whole step;
+`ms_per_step` is the step time.  With torchrun (N > 1) the matrices of N
+copies of the set are dealt to the ranks by size-sorted ping-pong ownership
+(weak scaling, no collective inside the step).
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+build) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Muon step ms & Newton-Schulz TFLOP/s (bf16, % tensor peak) on 1 GB300"
+UNIT = "TFLOP/s"
+LR, WD, MU = 0.02, 0.1, 0.95
+NS_STEPS = 5
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["llama3-8b", "gpt2-small", "moonlight-moe"], default="llama3-8b")
+    ap.add_argument("--ns-method", choices=["standard", "gram"], default="standard")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (parity runs only)")
+    ap.add_argument("--workspace-gb", type=float, default=64.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args(argv)
+
+
+def weight_set(name, layers=None):
+    from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+    if name == "llama3-8b":
+        return wl.llama3_8b(layers or 32)
+    if name == "gpt2-small":
+        return wl.gpt2_small(layers or 12)
+    return wl.moonlight_moe(layers or 27)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured (MEASURED_PEAKS.json)"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ workload
+
+def make_inputs(specs, device, seed, names_to_keep=()):
+    """Seeded synthetic tensors on the device: W ~ N(0, 0.02) bf16, G low-rank
+    (rank 64, sigma_i = 0.5**(i/8)) + 1e-3 noise bf16, M = 0 fp32."""
+    import torch
+    from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+    W, G, M = [], [], []
+    for i, s in enumerate(specs):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(wl.matrix_seed(seed, i))
+        w = torch.randn(s.shape, generator=gen, device=device).mul_(0.02).to(torch.bfloat16)
+        g = wl.lowrank_grad_device(gen, s.shape[0], s.shape[1], 64, noise=1e-3, device=device)
+        W.append(w)
+        G.append(g)
+        M.append(torch.zeros(s.shape, dtype=torch.float32, device=device))
+    return W, G, M
+
+
+def owned_specs(ws, world, rank):
+    from newton_schulz_orthogonalized_muon_gb300 import partition
+    from newton_schulz_orthogonalized_muon_gb300.workloads import ParamSpec
+    specs = [ParamSpec(f"replica{r}.{p.name}", p.shape, p.split_heads) for r in range(world) for p in ws.muon]
+    sizes = [p.shape[0] * p.shape[1] for p in specs]
+    mine = partition.owned(sizes, world, rank)
+    return [specs[i] for i in mine], mine
+
+
+# ------------------------------------------------------------ oracle arm
+
+SAMPLE_SHAPE = (1024, 4096)
+SAMPLE_TEXT = "one Muon step of one k_proj-shaped 1024x4096 matrix (fp64 numpy oracle)"
+
+
+def oracle_sample_step(_cache={}):
+    """One Muon step of one k_proj-shaped 1024x4096 matrix of the set in the
+    fp64 oracle on the host cores.  Returns (seconds, algorithmic NS flops)."""
+    import numpy as np
+    import oracle
+    from newton_schulz_orthogonalized_muon_gb300 import flops, workloads as wl
+    if "in" not in _cache:
+        _cache["in"] = (wl.weight(1, SAMPLE_SHAPE).astype(np.float64),
+                        wl.lowrank_grad(2, SAMPLE_SHAPE[0], SAMPLE_SHAPE[1], 64).astype(np.float64))
+    W, G = _cache["in"]
+    M = np.zeros(SAMPLE_SHAPE)
+    t0 = time.perf_counter()
+    oracle.muon_step(W, G, M, lr=LR, wd=WD, mu=MU, nesterov=True)
+    return time.perf_counter() - t0, flops.ns_flops_standard(SAMPLE_SHAPE[0], SAMPLE_SHAPE[1], NS_STEPS)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(min_seconds=10.0):
+    total_t, total_f, reps = 0.0, 0.0, 0
+    while total_t < min_seconds or reps == 0:
+        t, f = oracle_sample_step()
+        total_t += t
+        total_f += f
+        reps += 1
+    return {"value": total_f / total_t / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{reps} x {SAMPLE_TEXT}",
+            "seconds": round(total_t, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample_step()
+    t_sum, f_sum = 0.0, 0.0
+    for _ in range(args.steps):
+        t, f = oracle_sample_step()
+        t_sum += t
+        f_sum += f
+    value = f_sum / t_sum / 1e12
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_sum / max(args.steps, 1),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": "llama3-8b (bounded CPU sample: one k_proj-shaped 1024x4096 matrix per step)",
+                      "ns_method": "standard", "ns_steps": NS_STEPS},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                            "sample": SAMPLE_TEXT + " per step"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    ws = weight_set(args.workload, args.layers)
+    specs, _ = owned_specs(ws, world, rank)
+    W, G, M = make_inputs(specs, dev, args.seed + 7919 * rank)
+    split = [s.split_heads for s in specs]
+    h = pkg.default_handle(local)
+    h.set_workspace_limit(int(args.workspace_gb * (1 << 30)))
+    stream = torch.cuda.current_stream()
+
+    def step(grads=None):
+        pkg.muon_step(W, grads or G, M, lr=LR, wd=WD, mu=MU, nesterov=True, ns_method=args.ns_method,
+                      ns_steps=NS_STEPS, split_heads=split, handle=h)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if h.check() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    h.set_profiling(True)
+    launches0 = h.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / max(args.steps, 1)
+    launches = h.launch_count() - launches0
+    prof = h.profile()
+    h.set_profiling(False)
+    clk = clocks.stop()
+    status = h.check()
+    if status != 0:
+        raise RuntimeError(f"device error during the timed region: status {status}")
+
+    alg, dense = flops.set_flops(specs, NS_STEPS)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+        f = torch.tensor([alg, dense], device=dev, dtype=torch.float64)
+        dist.all_reduce(f, op=dist.ReduceOp.SUM)
+        alg_all, dense_all = float(f[0]), float(f[1])
+    else:
+        ms_max, alg_all, dense_all = ms, alg, dense
+    value = alg_all / (ms_max / 1e3) / 1e12
+
+    # ---- roofline of the dominant kernel class, timed live above
+    peaks, peak_src = load_peaks()
+    per_class = {"syrk": 0.0, "poly": 0.0, "update": 0.0, "final": 0.0}
+    for s in specs:
+        m, n = flops.ns_dims(s.shape[0], s.shape[1], s.split_heads)
+        kf = flops.kernel_flops_standard(m, n)
+        per_class["syrk"] += s.split_heads * NS_STEPS * kf["syrk"]
+        per_class["poly"] += s.split_heads * NS_STEPS * kf["poly"]
+        per_class["update"] += s.split_heads * (NS_STEPS - 1) * kf["update"]
+        per_class["final"] += s.split_heads * kf["update"]
+    kernel_rows = {}
+    for k, (kms, cnt) in prof.items():
+        if cnt == 0:
+            continue
+        row = {"ms_per_step": kms / args.steps, "launches_per_step": cnt / args.steps}
+        if k in per_class and kms > 0:
+            row["tflops"] = per_class[k] * args.steps / (kms / 1e3) / 1e12
+        kernel_rows[k] = row
+    gemm = {k: v for k, v in kernel_rows.items() if k in per_class}
+    dom = max(gemm, key=lambda k: gemm[k]["ms_per_step"]) if gemm else None
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if dom and os.path.exists(tpath):
+        try:
+            tr = json.load(open(tpath))
+            entry = tr.get(args.workload, {}).get(dom)
+            if entry and entry.get("kernel_source_hash") == kernel_source_hash():
+                traffic = entry.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    roofline = None
+    if dom:
+        ach = gemm[dom]["tflops"]
+        launches_dom = max(gemm[dom]["launches_per_step"], 1)
+        roofline = {"bound": "tensor", "kernel": f"ns_gemm_tc_kernel<{dom}>", "achieved": ach, "peak": peak,
+                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
+                    "flops_per_launch": per_class[dom] / launches_dom,
+                    "ms_per_launch": gemm[dom]["ms_per_step"] / launches_dom,
+                    "peak_source": f"bf16_tflops_sustained, {peak_src}"}
+    hbm = None
+    if "prepare" in kernel_rows:
+        nb = sum(flops.prepare_bytes(s.shape[0] * s.shape[1]) for s in specs)
+        gbs = nb / (kernel_rows["prepare"]["ms_per_step"] / 1e3) / 1e9
+        hbm = {"bound": "hbm", "kernel": "muon_prepare_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
+               "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": nb}
+
+    # ---- end to end through the public API: pinned host grads in, params out
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": ws.name, "ns_method": args.ns_method, "ns_steps": NS_STEPS,
+                          "muon_params_per_gpu": sum(s.shape[0] * s.shape[1] for s in specs),
+                          "matrices_per_gpu": len(specs), "l2": "inputs larger than L2 (no flush needed)",
+                          "lr": LR, "wd": WD, "mu": MU, "nesterov": True,
+                          "parallelism": f"layer-wise ownership x{world}" if world > 1 else "single GPU"},
+               "step_ms": ms_max, "ns_tflops_dense_convention": dense_all / (ms_max / 1e3) / 1e12,
+               "ns_frac_of_peak": value / peak, "roofline": roofline, "roofline_hbm": hbm,
+               "kernels": kernel_rows, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+               "cpu_baseline": cpu}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
+    """Same step through the public API with host buffers: every step copies
+    the gradients host->device from pinned memory and reads the updated
+    parameters back device->host."""
+    import torch
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    Gh = [g.cpu().pin_memory() for g in G]
+    Wh = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in W]
+    h2d = sum(g.numel() * g.element_size() for g in G)
+    d2h = sum(w.numel() * w.element_size() for w in W)
+    steps = max(1, min(args.steps, 3))
+
+    def one():
+        for gd, gh in zip(G, Gh):
+            gd.copy_(gh, non_blocking=True)
+        pkg.muon_step(W, G, M, lr=LR, wd=WD, mu=MU, nesterov=True, ns_method=args.ns_method, ns_steps=NS_STEPS,
+                      split_heads=split, handle=h)
+        for wh, wd in zip(Wh, W):
+            wh.copy_(wd, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": alg_all / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def kernel_source_hash():
+    import hashlib
+    hsh = hashlib.sha256()
+    for f in ("kernels_tc.cu", "common.cuh", "internal.h"):
+        hsh.update(open(os.path.join(ROOT, "newton_schulz_orthogonalized_muon_gb300", "csrc", f), "rb").read())
+    return hsh.hexdigest()[:16]
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,137 @@
+// Launch parameter blocks and launcher declarations shared by the kernel
+// translation units and the host scheduler (muon_api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace muon {
+
+struct SrcEntry;
+struct OutEntry;
+
+// ------------------------------------------------------------ prepare
+struct PrepParams {
+  const SrcEntry* src;     // [batch]
+  float mu;
+  int nesterov;
+  int m;                   // NS rows (after the transpose rule)
+  long long ldx;           // row stride of the NS workspace (elements)
+  float* xf;               // fp32 master [batch][m][ldx] or nullptr
+  __nv_bfloat16* xb;       // bf16 operand copy or nullptr (fp32 path)
+  float* partials;         // [batch][tiles_per_mat]
+  int tiles_per_mat;
+};
+
+struct ApplyParams {
+  const OutEntry* out;
+  const float* scale;
+  const float* xf;
+  long long ldx;
+  int m, n;
+};
+
+// --------------------------------------------------------------- AdamW
+constexpr int ADAM_CHUNK = 16384;
+
+struct AdamTensor {
+  void* p;
+  const void* g;
+  float* m;
+  float* v;
+  long long numel;
+  int pdtype, gdtype;
+};
+
+struct AdamChunk {
+  int tensor;
+  int pad;
+  long long offset;
+};
+
+struct AdamParams {
+  const AdamTensor* tensors;
+  const AdamChunk* chunks;
+  float beta1, beta2, eps;
+  float decay;       // 1 - lr*wd
+  float step_size;   // lr * sqrt(1 - beta2^t) / (1 - beta1^t)
+};
+
+// ------------------------------------------------ Newton-Schulz GEMMs
+// Modes of the NS GEMM kernels:
+//   SYRK   A = s^2 * X X^T        (symmetric, upper tiles computed, mirrored)
+//   POLY   B = b*A + c*A A        (symmetric, upper tiles computed, mirrored)
+//   UPDATE X' = s*(a*X + B X)     (fp32 master + bf16 operand copy)
+//   FINAL  out = alpha*out + beta*s*(a*X + B X)  (parameter or caller matrix)
+//
+// Gram method (iterates on R = X X^T; every matrix below is m x m, symmetric,
+// and stored as a pair of bf16 planes hi + lo, hi = bf16(v), lo = bf16(v - hi),
+// so products of two such matrices are bf16x3: hi*hi + hi*lo + lo*hi):
+//   G_R0    R = s^2 X X^T               (bf16 X operand, planes out)
+//   G_P     P = a I + b R + c R R       (planes in/out)
+//   G_PROD  C = A B                      (planes in/out; A, B commute)
+//   G_FINAL out = alpha*out + beta*s*(Q X)  (Q planes, X bf16 MN-major)
+enum NsMode : int {
+  MODE_SYRK = 0,
+  MODE_POLY = 1,
+  MODE_UPDATE = 2,
+  MODE_FINAL = 3,
+  MODE_G_R0 = 4,
+  MODE_G_P = 5,
+  MODE_G_PROD = 6,
+  MODE_G_FINAL = 7
+};
+
+struct NsGemmParams {
+  int m, n;                     // NS problem (m <= n)
+  int batch;
+  int tiles_per_mat;            // tiles of one matrix
+  int num_tiles;                // batch * tiles_per_mat
+  int mi;                       // row blocks of the output (UPDATE/FINAL)
+  const int2* tri;              // (i, j) tile table of the symmetric modes
+  const float* scale;           // per-matrix 1/||U||_F applied this iteration, or nullptr
+  float ca, cb, cc;             // quintic coefficients
+  // symmetric outputs (A or B matrix), row stride ldm
+  void* sym_out;                // bf16 (tensor-core path) or fp32 (fp32 path)
+  const void* sym_in;           // POLY: the A matrix for the b*A term (G_P: R hi plane)
+  void* sym_out_lo;             // Gram modes: lo plane of the output
+  const void* sym_in_lo;        // G_P: R lo plane
+  const void* op_b;             // fp32 path, G_PROD: the second factor
+  long long ldm;
+  // X master / operand copies, row stride ldx
+  float* xf;                    // fp32 master (read and written in place)
+  __nv_bfloat16* xb_out;        // UPDATE: bf16 copy of the new X (tensor-core path)
+  const float* xf_in;           // fp32 path: X operand (ping-pong partner of xf_out)
+  float* xf_out;                // fp32 path: new X
+  long long ldx;
+  const OutEntry* out;          // FINAL destinations [batch]
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+// tensor-core path (bf16 operands, fp32 accumulation in TMEM)
+// BN: output tile width (128 or 256).  Maps are 3-D (x = column, y = row,
+// z = matrix) bf16 maps with a 64 x 64 box and 128-byte swizzle.
+// Operands with two planes (Gram modes) pass their lo-plane maps in a1 / b1.
+cudaError_t launch_ns_gemm_tc(int mode, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                              const NsGemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
+                                     const CUtensorMap& map_b0, const CUtensorMap& map_b1, const NsGemmParams& p,
+                                     int grid, cudaStream_t s);
+size_t ns_gemm_tc_smem_bytes(int bn);
+int ns_gemm_tc_stages(int bn);
+
+// fp32 SIMT path (CUDA cores, fp32 FMA)
+cudaError_t launch_ns_gemm_simt(int mode, const NsGemmParams& p, cudaStream_t s);
+
+// elementwise
+cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s);
+cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
+                                 unsigned* err, cudaStream_t s);
+cudaError_t launch_apply(const ApplyParams& p, int batch, cudaStream_t s);
+cudaError_t launch_adamw(const AdamParams& p, int n_chunks, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t s);
+
+}  // namespace muon

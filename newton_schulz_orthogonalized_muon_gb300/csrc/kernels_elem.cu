@@ -1,0 +1,256 @@
+// HBM-bound kernels of the Muon step.
+//
+//  * muon_prepare_kernel: momentum M <- mu*M + G, Nesterov U = G + mu*M
+//    (else U = M), per-tile partial sums of U^2 for the Frobenius norm, and
+//    the NS working copy of U (fp32 master, optional bf16 MMA operand),
+//    transposed through shared memory when the block has rows > cols.
+//    ("迎接DeepSeek开源周…Muon优化器" (coreui.cn), §代码, Muon step;
+//     "Muon Optimizer and the Distributed Implementation", §Newton-Schulz
+//     Iteration, normalisation by the Frobenius norm.)
+//  * norm_finalize_kernel: per-matrix 1 / (||U||_F + eps), summed in a fixed
+//    order (deterministic), and a non-finite check.
+//  * apply_kernel: the final update when no NS step runs (O = X0).
+//  * adamw_kernel: the AdamW fallback of the same printed Muon class.
+//  * wait_selftest_kernel: a bounded wait on a barrier nothing completes,
+//    so the timeout path can be exercised without hanging a GPU.
+#include "common.cuh"
+#include "internal.h"
+
+namespace muon {
+
+constexpr int PT = 64;           // prepare tile: 64 x 64 elements
+constexpr int PREP_THREADS = 256;
+
+__global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
+  __shared__ float tile[PT][PT + 1];
+  __shared__ float red[PREP_THREADS / 32];
+
+  const int b = blockIdx.y;
+  const SrcEntry e = p.src[b];
+  const int tiles_x = (e.cols + PT - 1) / PT;
+  const int r0 = (blockIdx.x / tiles_x) * PT;
+  const int c0 = (blockIdx.x % tiles_x) * PT;
+  const int tx = threadIdx.x & 15;  // 4-column group
+  const int ty = threadIdx.x >> 4;  // row within a 16-row pass
+  const float mu = p.mu;
+  const bool vec = ((e.cols & 3) == 0) && ((e.ld & 3) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(e.g) & 15) == 0) &&
+                   (e.mom == nullptr || (reinterpret_cast<uintptr_t>(e.mom) & 15) == 0);
+  const long long xbase = static_cast<long long>(b) * p.m * p.ldx;
+  float ss = 0.f;
+
+#pragma unroll
+  for (int pass = 0; pass < PT / 16; ++pass) {
+    const int rl = ty + 16 * pass;
+    const int r = r0 + rl;
+    const int c = c0 + tx * 4;
+    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < e.rows) {
+      const long long off = static_cast<long long>(r) * e.ld + c;
+      float g[4], mo[4];
+      if (vec && c + 3 < e.cols) {
+        if (e.gdtype == DT_BF16) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.g) + off);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+          float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
+          g[0] = f0.x; g[1] = f0.y; g[2] = f1.x; g[3] = f1.y;
+        } else {
+          const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off);
+          g[0] = f.x; g[1] = f.y; g[2] = f.z; g[3] = f.w;
+        }
+        if (e.mom != nullptr) {
+          float4 m4 = *reinterpret_cast<const float4*>(e.mom + off);
+          mo[0] = fmaf(mu, m4.x, g[0]); mo[1] = fmaf(mu, m4.y, g[1]);
+          mo[2] = fmaf(mu, m4.z, g[2]); mo[3] = fmaf(mu, m4.w, g[3]);
+          *reinterpret_cast<float4*>(e.mom + off) = make_float4(mo[0], mo[1], mo[2], mo[3]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) u[k] = p.nesterov ? fmaf(mu, mo[k], g[k]) : mo[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) u[k] = g[k];
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (c + k < e.cols) {
+            const float gv = load_as_f32(e.g, off + k, e.gdtype);
+            if (e.mom != nullptr) {
+              const float mv = fmaf(mu, e.mom[off + k], gv);
+              e.mom[off + k] = mv;
+              u[k] = p.nesterov ? fmaf(mu, mv, gv) : mv;
+            } else {
+              u[k] = gv;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ss = fmaf(u[k], u[k], ss);
+
+    if (!e.transposed) {
+      // NS orientation == parameter orientation: X[r][c]
+      if (r < e.rows) {
+        const long long xo = xbase + static_cast<long long>(r) * p.ldx + c;
+        if (c + 3 < e.cols) {
+          if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+          if (p.xb != nullptr) {
+            uint2 packed = make_uint2(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]));
+            *reinterpret_cast<uint2*>(p.xb + xo) = packed;
+          }
+        } else {
+          for (int k = 0; k < 4 && c + k < e.cols; ++k) {
+            if (p.xf != nullptr) p.xf[xo + k] = u[k];
+            if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tile[rl][tx * 4 + k] = u[k];
+    }
+  }
+
+  if (e.transposed) {
+    __syncthreads();
+    // X[c][r] = U[r][c]: thread (tx, ty) writes X rows c0+ty+16*pass, 4 consecutive r.
+#pragma unroll
+    for (int pass = 0; pass < PT / 16; ++pass) {
+      const int cl = ty + 16 * pass;
+      const int c = c0 + cl;
+      const int r = r0 + tx * 4;
+      if (c < e.cols) {
+        float u[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) u[k] = tile[tx * 4 + k][cl];
+        const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
+        if (r + 3 < e.rows) {
+          if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+          if (p.xb != nullptr)
+            *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]));
+        } else {
+          for (int k = 0; k < 4 && r + k < e.rows; ++k) {
+            if (p.xf != nullptr) p.xf[xo + k] = u[k];
+            if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
+          }
+        }
+      }
+    }
+  }
+
+  // Block sum of U^2 in a fixed order.
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < PREP_THREADS / 32; ++w) t += red[w];
+    p.partials[static_cast<long long>(b) * p.tiles_per_mat + blockIdx.x] = t;
+  }
+}
+
+// One warp per matrix: scale[b] = 1 / (sqrt(sum of partials) + eps).
+__global__ void norm_finalize_kernel(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
+                                     unsigned* err) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= batch) return;
+  const float* pp = partials + static_cast<long long>(warp) * tiles_per_mat;
+  double s = 0.0;
+  for (int i = lane; i < tiles_per_mat; i += 32) s += static_cast<double>(pp[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) {
+    if (!isfinite(s)) atomicOr(err, ERRBIT_NONFINITE);
+    scale[warp] = static_cast<float>(1.0 / (sqrt(s) + static_cast<double>(eps)));
+  }
+}
+
+// Final update with no Newton-Schulz step: O = X0 = scale * U (fp32 master).
+__global__ void apply_kernel(ApplyParams p) {
+  const int b = blockIdx.y;
+  const OutEntry e = p.out[b];
+  const float s = p.scale[b];
+  const long long total = static_cast<long long>(p.m) * p.n;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / p.n), c = static_cast<int>(i % p.n);
+    const float o = s * p.xf[(static_cast<long long>(b) * p.m + r) * p.ldx + c];
+    store_out_scalar(e, r, c, o);
+  }
+}
+
+// AdamW fallback, one chunk of one tensor per block (multi-tensor launch).
+__global__ void __launch_bounds__(256) adamw_kernel(AdamParams p) {
+  const AdamChunk ch = p.chunks[blockIdx.x];
+  const AdamTensor t = p.tensors[ch.tensor];
+  const long long beg = ch.offset;
+  const long long end = min(beg + static_cast<long long>(ADAM_CHUNK), t.numel);
+  const float omb1 = 1.f - p.beta1, omb2 = 1.f - p.beta2;
+  for (long long i = beg + threadIdx.x; i < end; i += blockDim.x) {
+    const float g = load_as_f32(t.g, i, t.gdtype);
+    float m = t.m[i], v = t.v[i];
+    m = fmaf(omb1, g - m, m);
+    v = fmaf(omb2, fmaf(g, g, -v), v);
+    t.m[i] = m;
+    t.v[i] = v;
+    const float u = m / (p.eps + sqrtf(v));
+    const float w = load_as_f32(t.p, i, t.pdtype);
+    store_from_f32(t.p, i, t.pdtype, fmaf(w, p.decay, -p.step_size * u));
+  }
+}
+
+// Bounded wait on a barrier that nothing completes: must give up within
+// timeout_ns and report ERRBIT_TIMEOUT.
+__global__ void wait_selftest_kernel(unsigned long long timeout_ns, unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_bounded(&bar, 0, nullptr, timeout_ns)) atomicOr(err, ERRBIT_TIMEOUT);
+  }
+}
+
+// ------------------------------------------------------------- launchers
+cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s) {
+  if (batch == 0 || tiles_per_mat == 0) return cudaSuccess;
+  dim3 grid(tiles_per_mat, batch);
+  muon_prepare_kernel<<<grid, PREP_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
+                                 unsigned* err, cudaStream_t s) {
+  if (batch == 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = (batch * 32 + threads - 1) / threads;
+  norm_finalize_kernel<<<blocks, threads, 0, s>>>(partials, tiles_per_mat, batch, eps, scale, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const ApplyParams& p, int batch, cudaStream_t s) {
+  if (batch == 0) return cudaSuccess;
+  const long long total = static_cast<long long>(p.m) * p.n;
+  int bx = static_cast<int>((total + 255) / 256);
+  if (bx > 1024) bx = 1024;
+  if (bx < 1) bx = 1;
+  apply_kernel<<<dim3(bx, batch), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const AdamParams& p, int n_chunks, cudaStream_t s) {
+  if (n_chunks == 0) return cudaSuccess;
+  adamw_kernel<<<n_chunks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(timeout_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace muon

@@ -1,0 +1,891 @@
+// C ABI and host scheduler of the Muon step (see include/muon.h).
+//
+// The scheduler turns a parameter list into same-shape groups of NS
+// matrices: every parameter (or Muon-Split row block) becomes one m x n
+// matrix with m <= n (transposed when it has more rows than columns), and all
+// matrices of one (m, n) share one grouped launch per NS product.  A group
+// larger than the workspace limit is processed in chunks.  Per chunk the
+// launch sequence on the caller's stream is
+//   prepare (momentum, Nesterov, U, partial norms) -> norm finalize ->
+//   steps x [SYRK -> POLY -> UPDATE]  (the last UPDATE is FINAL and writes
+//   the parameter) — or, with no NS step, one apply kernel.
+// No host synchronisation happens inside a step.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "muon.h"
+
+using namespace muon;
+
+namespace {
+
+constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
+constexpr float kNormEps = 1e-7f;
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t dtype_size(int dt) { return dt == DT_BF16 ? 2 : 4; }
+
+struct Block {
+  SrcEntry src;
+  OutEntry out;
+  int m, n;
+};
+
+}  // namespace
+
+struct muon_handle_s {
+  int device = 0;
+  int num_sms = 0;
+  size_t ws_limit = size_t(16) << 30;
+  unsigned long long timeout_ns = 4000000000ull;
+  void* ws = nullptr;
+  size_t ws_cap = 0;
+  void* desc = nullptr;
+  size_t desc_cap = 0;
+  void* hstage = nullptr;
+  size_t hstage_cap = 0;
+  cudaEvent_t stage_ev = nullptr;
+  bool stage_pending = false;
+  unsigned* err = nullptr;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  std::string last;
+  // per-launch event timing (muon_handle_set_profiling)
+  struct ProfRec {
+    cudaEvent_t a, b;
+    int cls;
+  };
+  bool profiling = false;
+  std::vector<ProfRec> prof;
+  size_t prof_used = 0;
+  uint64_t launches = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+muon_status_t fail(muon_handle_t h, muon_status_t st, const std::string& msg) {
+  if (h != nullptr) h->last = msg;
+  return st;
+}
+
+muon_status_t cuda_fail(muon_handle_t h, cudaError_t e, const char* what) {
+  return fail(h, MUON_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define MUON_CUDA_TRY(expr, what)                  \
+  do {                                             \
+    cudaError_t e_ = (expr);                       \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, what); \
+  } while (0)
+
+constexpr size_t kMaxProfRecords = size_t(1) << 20;
+
+int prof_start(muon_handle_t h, int cls, cudaStream_t s) {
+  if (!h->profiling || h->prof_used >= kMaxProfRecords) return -1;
+  if (h->prof_used == h->prof.size()) {
+    muon_handle_s::ProfRec r{};
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    h->prof.push_back(r);
+  }
+  const int slot = static_cast<int>(h->prof_used++);
+  h->prof[slot].cls = cls;
+  cudaEventRecord(h->prof[slot].a, s);
+  return slot;
+}
+
+void prof_stop(muon_handle_t h, int slot, cudaStream_t s) {
+  if (slot >= 0) cudaEventRecord(h->prof[slot].b, s);
+}
+
+// Launch one kernel: optional event timing and the launch counter.
+#define MUON_LAUNCH(cls, expr, what)                       \
+  do {                                                     \
+    const int slot_ = prof_start(h, (cls), stream);        \
+    cudaError_t e_ = (expr);                               \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, what);  \
+    prof_stop(h, slot_, stream);                           \
+    ++h->launches;                                         \
+  } while (0)
+
+muon_status_t ensure_ws(muon_handle_t h, size_t bytes) {
+  if (bytes <= h->ws_cap) return MUON_OK;
+  if (h->ws != nullptr) {
+    cudaFree(h->ws);   // implicit device synchronisation: no launch still uses it
+    h->ws = nullptr;
+    h->ws_cap = 0;
+  }
+  const size_t cap = align_up(bytes, size_t(64) << 20);
+  if (cudaMalloc(&h->ws, cap) != cudaSuccess) {
+    cudaGetLastError();
+    h->ws = nullptr;
+    return fail(h, MUON_ERR_WORKSPACE, "workspace allocation of " + std::to_string(cap) + " bytes failed");
+  }
+  h->ws_cap = cap;
+  return MUON_OK;
+}
+
+// Copy a host descriptor arena to the handle's device descriptor buffer on
+// `stream` through a pinned staging buffer.
+muon_status_t upload(muon_handle_t h, const std::vector<uint8_t>& arena, cudaStream_t stream, void** dev) {
+  *dev = nullptr;
+  if (arena.empty()) return MUON_OK;
+  if (h->stage_pending) {
+    MUON_CUDA_TRY(cudaEventSynchronize(h->stage_ev), "descriptor staging wait");
+    h->stage_pending = false;
+  }
+  if (arena.size() > h->desc_cap) {
+    if (h->desc != nullptr) cudaFree(h->desc);
+    h->desc = nullptr;
+    h->desc_cap = 0;
+    const size_t cap = align_up(arena.size(), size_t(1) << 20);
+    if (cudaMalloc(&h->desc, cap) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, MUON_ERR_WORKSPACE, "descriptor buffer allocation failed");
+    }
+    h->desc_cap = cap;
+  }
+  if (arena.size() > h->hstage_cap) {
+    if (h->hstage != nullptr) cudaFreeHost(h->hstage);
+    h->hstage = nullptr;
+    h->hstage_cap = 0;
+    const size_t cap = align_up(arena.size(), size_t(1) << 20);
+    if (cudaMallocHost(&h->hstage, cap) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, MUON_ERR_WORKSPACE, "pinned staging allocation failed");
+    }
+    h->hstage_cap = cap;
+  }
+  std::memcpy(h->hstage, arena.data(), arena.size());
+  MUON_CUDA_TRY(cudaMemcpyAsync(h->desc, h->hstage, arena.size(), cudaMemcpyHostToDevice, stream),
+                "descriptor upload");
+  MUON_CUDA_TRY(cudaEventRecord(h->stage_ev, stream), "descriptor staging event");
+  h->stage_pending = true;
+  *dev = h->desc;
+  return MUON_OK;
+}
+
+template <typename T>
+size_t arena_push(std::vector<uint8_t>& arena, const T* data, size_t count) {
+  const size_t off = align_up(arena.size(), 256);
+  arena.resize(off + sizeof(T) * count);
+  if (count) std::memcpy(arena.data() + off, data, sizeof(T) * count);
+  return off;
+}
+
+bool encode_map(muon_handle_t h, CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t batch,
+                uint64_t ld) {
+  cuuint64_t dims[3] = {cols, rows, batch};
+  cuuint64_t strides[2] = {ld * 2, rows * ld * 2};
+  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tiles (i, j) of an m x m output that touch the upper triangle, for
+// 128-row by bn-column tiles.
+std::vector<int2> sym_tiles(int m, int bn) {
+  std::vector<int2> t;
+  const int mi = static_cast<int>(ceil_div(m, 128)), nj = static_cast<int>(ceil_div(m, bn));
+  for (int i = 0; i < mi; ++i)
+    for (int j = 0; j < nj; ++j)
+      if ((j + 1) * bn - 1 >= i * 128) t.push_back(make_int2(i, j));
+  return t;
+}
+
+struct GroupPlan {
+  int m = 0, n = 0;
+  long long ldx = 0, ldm = 0;
+  int prep_tiles = 0;
+  int bn_sym = 256, bn_upd = 256;
+  size_t per_mat = 0;       // workspace bytes per matrix
+  int chunk = 1;            // matrices per chunk
+  std::vector<int> members; // block indices
+  size_t tri_off = 0;
+  int tri_count = 0;
+  size_t tri128_off = 0;        // 128 x 128 symmetric tiles (Gram plane products)
+  int tri128_count = 0;
+  std::vector<std::pair<size_t, size_t>> chunk_off;   // (src offset, out offset) per chunk
+};
+
+// Workspace region offsets for one chunk capacity `cap` (bytes from ws base).
+//   standard, tensor cores: fp32 master X, two bf16 operand copies (ping-pong),
+//                           bf16 A and B
+//   standard, fp32 path:    two fp32 X buffers (ping-pong), fp32 A and B
+//   gram, tensor cores:     bf16 X0 (+ fp32 X0 when no NS step runs) and six
+//                           m x m slots (R, T, P0, P1, Q0, Q1) of two bf16 planes
+//   gram, fp32 path:        fp32 X0 and six fp32 m x m slots
+constexpr int kGramSlots = 6;
+enum { SLOT_R = 0, SLOT_T = 1, SLOT_P0 = 2, SLOT_Q0 = 4 };
+
+struct Regions {
+  size_t xf, xf2, xb0, xb1, symA, symB, partials, scale, total;
+  size_t slot[kGramSlots], slot_lo[kGramSlots];
+};
+
+Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
+  Regions r{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t xe = static_cast<size_t>(cap) * g.m * g.ldx;
+  const size_t se = static_cast<size_t>(cap) * g.m * g.ldm;
+  if (!gram) {
+    r.xf = take(xe * 4);
+    if (tc) {
+      r.xb0 = take(xe * 2);
+      r.xb1 = take(xe * 2);
+      r.symA = take(se * 2);
+      r.symB = take(se * 2);
+    } else {
+      r.xf2 = take(xe * 4);
+      r.symA = take(se * 4);
+      r.symB = take(se * 4);
+    }
+  } else {
+    if (tc) {
+      r.xb0 = take(xe * 2);
+      r.xf = (steps == 0) ? take(xe * 4) : 0;
+      for (int k = 0; k < kGramSlots; ++k) {
+        r.slot[k] = take(se * 2);
+        r.slot_lo[k] = take(se * 2);
+      }
+    } else {
+      r.xf = take(xe * 4);
+      for (int k = 0; k < kGramSlots; ++k) r.slot[k] = take(se * 4);
+    }
+  }
+  r.partials = take(static_cast<size_t>(cap) * g.prep_tiles * 4);
+  r.scale = take(static_cast<size_t>(cap) * 4);
+  r.total = off;
+  return r;
+}
+
+// Gram method for one same-shape group ("DeepSpeed 集成 Muon 优化器实战",
+// §核心算子: iterate on R = X X^T).  With P_k = aI + bR_k + cR_k^2:
+//   R_0 = X0 X0^T;  Q_1 = P_0;  Q_{k+1} = P_k Q_k;  R_{k+1} = P_k R_k P_k;
+//   O = Q X0,  X0 = s U (s = 1/||U||_F folded into the first and last products).
+// All m x m iterates are polynomials in R_0, so they commute and are
+// symmetric: every product is computed on its upper tiles and mirrored.
+muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions& R, uint8_t* ws, uint8_t* dbase,
+                             int steps, float ca, float cb, float cc, bool tc, float mu, int nesterov,
+                             cudaStream_t stream) {
+  float* xf = reinterpret_cast<float*>(ws + R.xf);
+  __nv_bfloat16* xb = tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb0) : nullptr;
+  float* partials = reinterpret_cast<float*>(ws + R.partials);
+  float* scale = reinterpret_cast<float*>(ws + R.scale);
+  void* hi[kGramSlots];
+  void* lo[kGramSlots];
+  for (int k = 0; k < kGramSlots; ++k) {
+    hi[k] = ws + R.slot[k];
+    lo[k] = tc ? static_cast<void*>(ws + R.slot_lo[k]) : nullptr;
+  }
+  CUtensorMap map_x, mhi[kGramSlots], mlo[kGramSlots];
+  if (tc) {
+    bool ok = encode_map(h, &map_x, xb, g.n, g.m, g.chunk, g.ldx);
+    for (int k = 0; k < kGramSlots && ok; ++k)
+      ok = encode_map(h, &mhi[k], hi[k], g.m, g.m, g.chunk, g.ldm) &&
+           encode_map(h, &mlo[k], lo[k], g.m, g.m, g.chunk, g.ldm);
+    if (!ok) return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  }
+  const int mi = static_cast<int>(ceil_div(g.m, 128));
+  const int nj = static_cast<int>(ceil_div(g.n, g.bn_upd));
+  for (size_t c = 0; c < g.chunk_off.size(); ++c) {
+    const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
+    const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
+    const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+    PrepParams pp{};
+    pp.src = src_d;
+    pp.mu = mu;
+    pp.nesterov = nesterov;
+    pp.m = g.m;
+    pp.ldx = g.ldx;
+    pp.xf = (tc && steps > 0) ? nullptr : xf;
+    pp.xb = xb;
+    pp.partials = partials;
+    pp.tiles_per_mat = g.prep_tiles;
+    MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");
+    MUON_LAUNCH(MUON_K_NORM, launch_norm_finalize(partials, g.prep_tiles, cnt, kNormEps, scale, h->err, stream),
+                "norm launch");
+    if (steps == 0) {
+      ApplyParams ap{out_d, scale, xf, g.ldx, g.m, g.n};
+      MUON_LAUNCH(MUON_K_APPLY, launch_apply(ap, cnt, stream), "apply launch");
+      continue;
+    }
+    NsGemmParams p{};
+    p.m = g.m;
+    p.n = g.n;
+    p.batch = cnt;
+    p.ca = ca;
+    p.cb = cb;
+    p.cc = cc;
+    p.ldm = g.ldm;
+    p.ldx = g.ldx;
+    p.out = out_d;
+    p.err = h->err;
+    p.timeout_ns = h->timeout_ns;
+    // symmetric products: tile table and grid
+    NsGemmParams q = p;
+    q.tiles_per_mat = tc ? g.tri128_count : 0;
+    q.num_tiles = cnt * q.tiles_per_mat;
+    q.tri = tc ? reinterpret_cast<const int2*>(dbase + g.tri128_off) : nullptr;
+    const int grid_sym = std::max(1, std::min(q.num_tiles, h->num_sms));
+    // R0 = s^2 X0 X0^T
+    {
+      NsGemmParams r0 = p;
+      r0.scale = scale;
+      r0.sym_out = hi[SLOT_R];
+      r0.sym_out_lo = lo[SLOT_R];
+      if (tc) {
+        r0.tiles_per_mat = g.tri_count;
+        r0.num_tiles = cnt * g.tri_count;
+        r0.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
+        const int grid = std::min(r0.num_tiles, h->num_sms);
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_G_R0, g.bn_sym, map_x, map_x, r0, grid, stream), "gram r0");
+      } else {
+        r0.xf_in = xf;
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_G_R0, r0, stream), "gram r0");
+      }
+    }
+    auto sym_product = [&](int mode, int a, int b, int out, int cls) -> muon_status_t {
+      NsGemmParams t = q;
+      t.sym_out = hi[out];
+      t.sym_out_lo = lo[out];
+      t.sym_in = hi[a];
+      t.sym_in_lo = lo[a];
+      t.op_b = hi[b];
+      if (tc) {
+        MUON_LAUNCH(cls, launch_ns_gemm_tc_planes(mode, 128, mhi[a], mlo[a], mhi[b], mlo[b], t, grid_sym, stream),
+                    "gram product");
+      } else {
+        MUON_LAUNCH(cls, launch_ns_gemm_simt(mode, t, stream), "gram product");
+      }
+      return MUON_OK;
+    };
+    int qcur = -1, qnext = SLOT_Q0;
+    for (int k = 0; k < steps; ++k) {
+      const int pk = SLOT_P0 + (k & 1);
+      muon_status_t st = sym_product(MODE_G_P, SLOT_R, SLOT_R, pk, MUON_K_POLY);     // P = aI + bR + cR^2
+      if (st != MUON_OK) return st;
+      if (k == 0) {
+        qcur = pk;
+      } else {
+        st = sym_product(MODE_G_PROD, pk, qcur, qnext, MUON_K_UPDATE);              // Q <- P Q
+        if (st != MUON_OK) return st;
+        qcur = qnext;
+        qnext = (qnext == SLOT_Q0) ? SLOT_Q0 + 1 : SLOT_Q0;
+      }
+      if (k < steps - 1) {
+        st = sym_product(MODE_G_PROD, pk, SLOT_R, SLOT_T, MUON_K_UPDATE);           // T = P R
+        if (st != MUON_OK) return st;
+        st = sym_product(MODE_G_PROD, SLOT_T, pk, SLOT_R, MUON_K_UPDATE);           // R <- T P
+        if (st != MUON_OK) return st;
+      }
+    }
+    // O = s Q X0 -> destination
+    NsGemmParams f = p;
+    f.scale = scale;
+    f.sym_in = hi[qcur];
+    if (tc) {
+      f.mi = mi;
+      f.tiles_per_mat = mi * nj;
+      f.num_tiles = cnt * mi * nj;
+      const int grid = std::min(f.num_tiles, h->num_sms);
+      MUON_LAUNCH(MUON_K_FINAL,
+                  launch_ns_gemm_tc_planes(MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur], map_x, map_x, f, grid, stream),
+                  "gram final");
+    } else {
+      f.xf_in = xf;
+      MUON_LAUNCH(MUON_K_FINAL, launch_ns_gemm_simt(MODE_G_FINAL, f, stream), "gram final");
+    }
+  }
+  return MUON_OK;
+}
+
+// Run prepare + Newton-Schulz + final write for every block.
+muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, float mu, int nesterov, int steps,
+                         const float* coeffs, int ns_method, bool tc, cudaStream_t stream) {
+  if (blocks.empty()) return MUON_OK;
+  const bool gram = (ns_method == MUON_NS_GRAM);
+  const float ca = coeffs[0], cb = coeffs[1], cc = coeffs[2];
+
+  std::map<std::pair<int, int>, GroupPlan> groups;
+  for (size_t i = 0; i < blocks.size(); ++i) {
+    GroupPlan& g = groups[{blocks[i].m, blocks[i].n}];
+    g.m = blocks[i].m;
+    g.n = blocks[i].n;
+    g.members.push_back(static_cast<int>(i));
+  }
+
+  std::vector<uint8_t> arena;
+  size_t ws_need = 0;
+  for (auto& kv : groups) {
+    GroupPlan& g = kv.second;
+    g.ldx = static_cast<long long>(align_up(g.n, 8));
+    g.ldm = static_cast<long long>(align_up(g.m, 8));
+    g.prep_tiles = static_cast<int>(ceil_div(g.m, 64) * ceil_div(g.n, 64));
+    g.bn_sym = g.m <= 128 ? 128 : 256;
+    g.bn_upd = g.n <= 128 ? 128 : 256;
+    const size_t per1 = regions(g, 1, tc, gram, steps).total;
+    const size_t per2 = regions(g, 2, tc, gram, steps).total;
+    g.per_mat = per2 > per1 ? per2 - per1 : per1;
+    const size_t fixed = per1 > g.per_mat ? per1 - g.per_mat : 0;
+    size_t fit = h->ws_limit > fixed ? (h->ws_limit - fixed) / std::max<size_t>(g.per_mat, 1) : 1;
+    fit = std::max<size_t>(fit, 1);
+    fit = std::min<size_t>(fit, g.members.size());
+    fit = std::min<size_t>(fit, 65535);
+    const int tiles_upd = static_cast<int>(ceil_div(g.m, 128) * ceil_div(g.n, g.bn_upd));
+    const int tiles_max = std::max({tiles_upd, g.prep_tiles, 1});
+    fit = std::min<size_t>(fit, static_cast<size_t>((1u << 31) - 1) / static_cast<size_t>(tiles_max));
+    g.chunk = static_cast<int>(fit);
+    ws_need = std::max(ws_need, regions(g, g.chunk, tc, gram, steps).total);
+    if (tc) {
+      std::vector<int2> tri = sym_tiles(g.m, g.bn_sym);
+      g.tri_count = static_cast<int>(tri.size());
+      g.tri_off = arena_push(arena, tri.data(), tri.size());
+      if (gram) {
+        std::vector<int2> t128 = sym_tiles(g.m, 128);
+        g.tri128_count = static_cast<int>(t128.size());
+        g.tri128_off = arena_push(arena, t128.data(), t128.size());
+      }
+    }
+    for (size_t c0 = 0; c0 < g.members.size(); c0 += g.chunk) {
+      const size_t cnt = std::min<size_t>(g.chunk, g.members.size() - c0);
+      std::vector<SrcEntry> src(cnt);
+      std::vector<OutEntry> out(cnt);
+      for (size_t k = 0; k < cnt; ++k) {
+        src[k] = blocks[g.members[c0 + k]].src;
+        out[k] = blocks[g.members[c0 + k]].out;
+      }
+      const size_t so = arena_push(arena, src.data(), cnt);
+      const size_t oo = arena_push(arena, out.data(), cnt);
+      g.chunk_off.emplace_back(so, oo);
+    }
+  }
+
+  muon_status_t st = ensure_ws(h, ws_need);
+  if (st != MUON_OK) return st;
+  void* dev = nullptr;
+  st = upload(h, arena, stream, &dev);
+  if (st != MUON_OK) return st;
+  uint8_t* dbase = static_cast<uint8_t*>(dev);
+  uint8_t* ws = static_cast<uint8_t*>(h->ws);
+
+  for (auto& kv : groups) {
+    GroupPlan& g = kv.second;
+    const Regions R = regions(g, g.chunk, tc, gram, steps);
+    if (gram) {
+      muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, ca, cb, cc, tc, mu, nesterov, stream);
+      if (gst != MUON_OK) return gst;
+      continue;
+    }
+    float* xf = reinterpret_cast<float*>(ws + R.xf);
+    float* xf2 = tc ? nullptr : reinterpret_cast<float*>(ws + R.xf2);
+    __nv_bfloat16* xb[2] = {tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb0) : nullptr,
+                            tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb1) : nullptr};
+    void* symA = ws + R.symA;
+    void* symB = ws + R.symB;
+    float* partials = reinterpret_cast<float*>(ws + R.partials);
+    float* scale = reinterpret_cast<float*>(ws + R.scale);
+
+    CUtensorMap map_x[2], map_A, map_B;
+    if (tc) {
+      if (!encode_map(h, &map_x[0], xb[0], g.n, g.m, g.chunk, g.ldx) ||
+          !encode_map(h, &map_x[1], xb[1], g.n, g.m, g.chunk, g.ldx) ||
+          !encode_map(h, &map_A, symA, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm))
+        return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    }
+    const int mi = static_cast<int>(ceil_div(g.m, 128));
+    const int nj = static_cast<int>(ceil_div(g.n, g.bn_upd));
+
+    for (size_t c = 0; c < g.chunk_off.size(); ++c) {
+      const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
+      const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
+      const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+
+      PrepParams pp{};
+      pp.src = src_d;
+      pp.mu = mu;
+      pp.nesterov = nesterov;
+      pp.m = g.m;
+      pp.ldx = g.ldx;
+      pp.xf = xf;
+      pp.xb = xb[0];
+      pp.partials = partials;
+      pp.tiles_per_mat = g.prep_tiles;
+      MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");
+      MUON_LAUNCH(MUON_K_NORM, launch_norm_finalize(partials, g.prep_tiles, cnt, kNormEps, scale, h->err, stream),
+                  "norm launch");
+
+      if (steps == 0) {
+        ApplyParams ap{out_d, scale, xf, g.ldx, g.m, g.n};
+        MUON_LAUNCH(MUON_K_APPLY, launch_apply(ap, cnt, stream), "apply launch");
+        continue;
+      }
+      for (int it = 0; it < steps; ++it) {
+        const bool last = (it == steps - 1);
+        NsGemmParams p{};
+        p.m = g.m;
+        p.n = g.n;
+        p.batch = cnt;
+        p.scale = it == 0 ? scale : nullptr;
+        p.ca = ca;
+        p.cb = cb;
+        p.cc = cc;
+        p.ldm = g.ldm;
+        p.ldx = g.ldx;
+        p.out = out_d;
+        p.err = h->err;
+        p.timeout_ns = h->timeout_ns;
+        if (tc) {
+          // SYRK: A = s^2 X X^T
+          NsGemmParams q = p;
+          q.tiles_per_mat = g.tri_count;
+          q.num_tiles = cnt * g.tri_count;
+          q.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
+          q.sym_out = symA;
+          int grid = std::min(q.num_tiles, h->num_sms);
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], q, grid, stream),
+                      "syrk launch");
+          // POLY: B = b A + c A A
+          q.scale = nullptr;
+          q.sym_in = symA;
+          q.sym_out = symB;
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, q, grid, stream), "poly launch");
+          // UPDATE / FINAL: X = s (a X + B X)
+          NsGemmParams u = p;
+          u.mi = mi;
+          u.tiles_per_mat = mi * nj;
+          u.num_tiles = cnt * mi * nj;
+          u.xf = xf;
+          u.xb_out = xb[(it + 1) & 1];
+          grid = std::min(u.num_tiles, h->num_sms);
+          MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                      launch_ns_gemm_tc(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1], u, grid, stream),
+                      "update launch");
+        } else {
+          float* xin = (it & 1) ? xf2 : xf;
+          float* xout = (it & 1) ? xf : xf2;
+          NsGemmParams q = p;
+          q.xf_in = xin;
+          q.sym_out = symA;
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_SYRK, q, stream), "syrk launch");
+          q.scale = nullptr;
+          q.sym_in = symA;
+          q.sym_out = symB;
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_simt(MODE_POLY, q, stream), "poly launch");
+          NsGemmParams u = p;
+          u.sym_in = symB;
+          u.xf_in = xin;
+          u.xf_out = xout;
+          MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE, launch_ns_gemm_simt(last ? MODE_FINAL : MODE_UPDATE, u, stream),
+                      "update launch");
+        }
+      }
+    }
+  }
+  return MUON_OK;
+}
+
+bool valid_dtype(int32_t d) { return d == MUON_F32 || d == MUON_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* muon_status_string(muon_status_t s) {
+  switch (s) {
+    case MUON_OK: return "ok";
+    case MUON_ERR_INVALID_ARG: return "invalid argument";
+    case MUON_ERR_UNSUPPORTED: return "unsupported";
+    case MUON_ERR_WORKSPACE: return "workspace allocation failed";
+    case MUON_ERR_CUDA: return "CUDA error";
+    case MUON_ERR_NONFINITE: return "non-finite gradient norm";
+    case MUON_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* muon_last_error(muon_handle_t h) { return h == nullptr ? "null handle" : h->last.c_str(); }
+
+int32_t muon_version(void) { return 10000; }
+
+muon_status_t muon_handle_create(muon_handle_t* out, int device) {
+  if (out == nullptr) return MUON_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+    cudaGetLastError();
+    return MUON_ERR_UNSUPPORTED;
+  }
+  DeviceGuard guard(device);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MUON_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return MUON_ERR_UNSUPPORTED;   // built for sm_103a only
+  muon_handle_t h = new (std::nothrow) muon_handle_s();
+  if (h == nullptr) return MUON_ERR_WORKSPACE;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    delete h;
+    return MUON_ERR_UNSUPPORTED;
+  }
+  h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  if (cudaMalloc(&h->err, sizeof(unsigned)) != cudaSuccess || cudaMemset(h->err, 0, sizeof(unsigned)) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->err) cudaFree(h->err);
+    delete h;
+    return MUON_ERR_WORKSPACE;
+  }
+  *out = h;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_destroy(muon_handle_t h) {
+  if (h == nullptr) return MUON_OK;
+  DeviceGuard guard(h->device);
+  cudaDeviceSynchronize();
+  if (h->ws) cudaFree(h->ws);
+  if (h->desc) cudaFree(h->desc);
+  if (h->hstage) cudaFreeHost(h->hstage);
+  if (h->err) cudaFree(h->err);
+  if (h->stage_ev) cudaEventDestroy(h->stage_ev);
+  for (auto& r : h->prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  delete h;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_set_workspace_limit(muon_handle_t h, size_t bytes) {
+  if (h == nullptr || bytes == 0) return MUON_ERR_INVALID_ARG;
+  h->ws_limit = bytes;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_set_timeout_ns(muon_handle_t h, uint64_t timeout_ns) {
+  if (h == nullptr || timeout_ns == 0) return MUON_ERR_INVALID_ARG;
+  h->timeout_ns = timeout_ns;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_check(muon_handle_t h, void* stream) {
+  if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MUON_CUDA_TRY(cudaStreamSynchronize(s), "stream synchronise");
+  unsigned word = 0;
+  MUON_CUDA_TRY(cudaMemcpy(&word, h->err, sizeof(unsigned), cudaMemcpyDeviceToHost), "error word read");
+  MUON_CUDA_TRY(cudaMemset(h->err, 0, sizeof(unsigned)), "error word reset");
+  if (word & ERRBIT_TIMEOUT) return fail(h, MUON_ERR_TIMEOUT, "a bounded device wait timed out");
+  if (word & ERRBIT_NONFINITE) return fail(h, MUON_ERR_NONFINITE, "a Frobenius norm was not finite");
+  return MUON_OK;
+}
+
+muon_status_t muon_orthogonalize(muon_handle_t h, void* X, int32_t dtype, int64_t batch, int64_t m, int64_t n,
+                                 int32_t steps, const float* coeffs, int32_t ns_method, void* stream) {
+  if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return fail(h, MUON_ERR_INVALID_ARG, "dtype must be MUON_F32 or MUON_BF16");
+  if (batch < 0 || m < 0 || n < 0 || m > kMaxDim || n > kMaxDim || batch > kMaxDim)
+    return fail(h, MUON_ERR_INVALID_ARG, "negative or oversized shape");
+  if (steps < 0 || steps > 100) return fail(h, MUON_ERR_INVALID_ARG, "steps must be in [0, 100]");
+  if (ns_method != MUON_NS_STANDARD && ns_method != MUON_NS_GRAM)
+    return fail(h, MUON_ERR_INVALID_ARG, "unknown ns_method");
+  if (batch == 0 || m == 0 || n == 0) return MUON_OK;
+  if (X == nullptr) return fail(h, MUON_ERR_INVALID_ARG, "X is NULL");
+  DeviceGuard guard(h->device);
+  const float* cf = coeffs ? coeffs : kDefaultCoeffs;
+  const size_t es = dtype_size(dtype);
+  std::vector<Block> blocks(static_cast<size_t>(batch));
+  for (int64_t b = 0; b < batch; ++b) {
+    uint8_t* base = static_cast<uint8_t*>(X) + static_cast<size_t>(b) * m * n * es;
+    Block& bl = blocks[b];
+    const int transposed = m > n ? 1 : 0;
+    bl.src = SrcEntry{base, nullptr, n, static_cast<int>(m), static_cast<int>(n), transposed, dtype};
+    bl.out = OutEntry{base, n, transposed, dtype, 0.f, 1.f};
+    bl.m = static_cast<int>(std::min(m, n));
+    bl.n = static_cast<int>(std::max(m, n));
+  }
+  return run_blocks(h, blocks, 0.f, 0, steps, cf, ns_method, dtype == MUON_BF16, static_cast<cudaStream_t>(stream));
+}
+
+muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_params, float lr, float wd,
+                        float mu, int32_t nesterov, int32_t ns_method, int32_t ns_steps, const float* coeffs,
+                        float update_rms, int32_t ns_dtype, void* stream) {
+  if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  if (n_params < 0) return fail(h, MUON_ERR_INVALID_ARG, "n_params < 0");
+  if (n_params > 0 && params == nullptr) return fail(h, MUON_ERR_INVALID_ARG, "params is NULL");
+  if (!valid_dtype(ns_dtype)) return fail(h, MUON_ERR_INVALID_ARG, "ns_dtype must be MUON_F32 or MUON_BF16");
+  if (ns_method != MUON_NS_STANDARD && ns_method != MUON_NS_GRAM)
+    return fail(h, MUON_ERR_INVALID_ARG, "unknown ns_method");
+  if (ns_steps < 0 || ns_steps > 100) return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 100]");
+  if (!std::isfinite(lr) || !std::isfinite(wd) || !std::isfinite(mu) || !std::isfinite(update_rms))
+    return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
+  std::vector<Block> blocks;
+  for (int32_t i = 0; i < n_params; ++i) {
+    const muon_param_t& P = params[i];
+    const std::string where = "param " + std::to_string(i) + ": ";
+    if (!valid_dtype(P.param_dtype) || !valid_dtype(P.grad_dtype))
+      return fail(h, MUON_ERR_INVALID_ARG, where + "bad dtype");
+    if (P.rows < 0 || P.cols < 0 || P.rows > kMaxDim || P.cols > kMaxDim)
+      return fail(h, MUON_ERR_INVALID_ARG, where + "negative or oversized shape");
+    if (P.split_heads < 1 || (P.rows > 0 && P.rows % P.split_heads != 0))
+      return fail(h, MUON_ERR_INVALID_ARG, where + "split_heads must be >= 1 and divide rows");
+    if (P.reserved != 0 || P.scale_dim < 0) return fail(h, MUON_ERR_INVALID_ARG, where + "bad reserved/scale_dim");
+    if (P.rows == 0 || P.cols == 0) continue;
+    if (P.param == nullptr || P.grad == nullptr || P.momentum == nullptr)
+      return fail(h, MUON_ERR_INVALID_ARG, where + "NULL pointer");
+    const int64_t rb = P.rows / P.split_heads;
+    const double sdim = static_cast<double>(P.scale_dim > 0 ? P.scale_dim : std::max(P.rows, P.cols));
+    const float beta = static_cast<float>(-static_cast<double>(lr) * update_rms * std::sqrt(sdim));
+    const float alpha = static_cast<float>(1.0 - static_cast<double>(lr) * wd);
+    const size_t ge = dtype_size(P.grad_dtype), pe = dtype_size(P.param_dtype);
+    for (int32_t hb = 0; hb < P.split_heads; ++hb) {
+      const size_t off = static_cast<size_t>(hb) * rb * P.cols;
+      Block bl;
+      const int transposed = rb > P.cols ? 1 : 0;
+      bl.src = SrcEntry{static_cast<const uint8_t*>(P.grad) + off * ge, P.momentum + off, P.cols,
+                        static_cast<int>(rb), static_cast<int>(P.cols), transposed, P.grad_dtype};
+      bl.out = OutEntry{static_cast<uint8_t*>(P.param) + off * pe, P.cols, transposed, P.param_dtype, alpha, beta};
+      bl.m = static_cast<int>(std::min<int64_t>(rb, P.cols));
+      bl.n = static_cast<int>(std::max<int64_t>(rb, P.cols));
+      blocks.push_back(bl);
+    }
+  }
+  if (blocks.empty()) return MUON_OK;
+  DeviceGuard guard(h->device);
+  const float* cf = coeffs ? coeffs : kDefaultCoeffs;
+  return run_blocks(h, blocks, mu, nesterov ? 1 : 0, ns_steps, cf, ns_method, ns_dtype == MUON_BF16,
+                    static_cast<cudaStream_t>(stream));
+}
+
+muon_status_t adamw_step(muon_handle_t h, void* const* params, const void* const* grads, float* const* exp_avg,
+                         float* const* exp_avg_sq, const int64_t* numel, const int32_t* param_dtypes,
+                         const int32_t* grad_dtypes, int32_t n, int64_t step, float lr, float beta1, float beta2,
+                         float eps, float wd, void* stream_arg) {
+  if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  if (n < 0) return fail(h, MUON_ERR_INVALID_ARG, "n < 0");
+  if (n == 0) return MUON_OK;
+  if (params == nullptr || grads == nullptr || exp_avg == nullptr || exp_avg_sq == nullptr || numel == nullptr ||
+      param_dtypes == nullptr || grad_dtypes == nullptr)
+    return fail(h, MUON_ERR_INVALID_ARG, "NULL array");
+  if (step < 1) return fail(h, MUON_ERR_INVALID_ARG, "step counts from 1");
+  if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f) || !std::isfinite(lr) || !std::isfinite(eps) ||
+      !std::isfinite(wd))
+    return fail(h, MUON_ERR_INVALID_ARG, "bad hyper-parameter");
+  std::vector<AdamTensor> tensors;
+  std::vector<AdamChunk> chunks;
+  for (int32_t i = 0; i < n; ++i) {
+    if (numel[i] < 0) return fail(h, MUON_ERR_INVALID_ARG, "negative numel");
+    if (!valid_dtype(param_dtypes[i]) || !valid_dtype(grad_dtypes[i]))
+      return fail(h, MUON_ERR_INVALID_ARG, "bad dtype");
+    if (numel[i] == 0) continue;
+    if (params[i] == nullptr || grads[i] == nullptr || exp_avg[i] == nullptr || exp_avg_sq[i] == nullptr)
+      return fail(h, MUON_ERR_INVALID_ARG, "NULL tensor pointer");
+    const int ti = static_cast<int>(tensors.size());
+    tensors.push_back(AdamTensor{params[i], grads[i], exp_avg[i], exp_avg_sq[i], numel[i], param_dtypes[i],
+                                 grad_dtypes[i]});
+    for (int64_t off = 0; off < numel[i]; off += ADAM_CHUNK) chunks.push_back(AdamChunk{ti, 0, off});
+  }
+  if (chunks.empty()) return MUON_OK;
+  DeviceGuard guard(h->device);
+  std::vector<uint8_t> arena;
+  const size_t to = arena_push(arena, tensors.data(), tensors.size());
+  const size_t co = arena_push(arena, chunks.data(), chunks.size());
+  void* dev = nullptr;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_arg);
+  muon_status_t st = upload(h, arena, stream, &dev);
+  if (st != MUON_OK) return st;
+  const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(step));
+  const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(step));
+  AdamParams p{};
+  p.tensors = reinterpret_cast<const AdamTensor*>(static_cast<uint8_t*>(dev) + to);
+  p.chunks = reinterpret_cast<const AdamChunk*>(static_cast<uint8_t*>(dev) + co);
+  p.beta1 = beta1;
+  p.beta2 = beta2;
+  p.eps = eps;
+  p.decay = static_cast<float>(1.0 - static_cast<double>(lr) * wd);
+  p.step_size = static_cast<float>(static_cast<double>(lr) * std::sqrt(bc2) / bc1);
+  MUON_LAUNCH(MUON_K_ADAMW, launch_adamw(p, static_cast<int>(chunks.size()), stream), "adamw launch");
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_set_profiling(muon_handle_t h, int32_t enable) {
+  if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  h->profiling = enable != 0;
+  h->prof_used = 0;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_profile(muon_handle_t h, double* ms, int64_t* launches, int32_t n_classes) {
+  if (h == nullptr || n_classes < 0 || n_classes > MUON_K_COUNT) return MUON_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  for (int32_t c = 0; c < n_classes; ++c) {
+    if (ms) ms[c] = 0.0;
+    if (launches) launches[c] = 0;
+  }
+  for (size_t i = 0; i < h->prof_used; ++i) {
+    const auto& r = h->prof[i];
+    MUON_CUDA_TRY(cudaEventSynchronize(r.b), "profile event wait");
+    float t = 0.f;
+    MUON_CUDA_TRY(cudaEventElapsedTime(&t, r.a, r.b), "profile elapsed time");
+    if (r.cls < n_classes) {
+      if (ms) ms[r.cls] += t;
+      if (launches) launches[r.cls] += 1;
+    }
+  }
+  h->prof_used = 0;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_launch_count(muon_handle_t h, uint64_t* count) {
+  if (h == nullptr || count == nullptr) return MUON_ERR_INVALID_ARG;
+  *count = h->launches;
+  return MUON_OK;
+}
+
+muon_status_t muon_selftest_timeout(muon_handle_t h, uint64_t timeout_ns, void* stream) {
+  if (h == nullptr || timeout_ns == 0 || timeout_ns > 10000000000ull) return MUON_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MUON_CUDA_TRY(launch_wait_selftest(timeout_ns, h->err, s), "selftest launch");
+  return MUON_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,311 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Tolerances (relative Frobenius error): fp32 path 1e-4, bf16 path 2e-2,
+momentum and the update arithmetic 1e-6.  bf16 inputs are compared against
+the oracle run on the same bf16 values widened exactly to fp64.  For bf16
+parameters the result is rounded once to bf16, so the update is compared as
+(W_new - W_old*(1 - lr*wd)) with the bf16 rounding of W_new added to the
+budget (half an ulp of |W_new| per element).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32, TOL_BF16, TOL_EXACT = 1e-4, 2e-2, 1e-6
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import newton_schulz_orthogonalized_muon_gb300 as p
+    p.load_library()
+    torch.cuda.set_device(0)
+    return p
+
+
+def to_dev(x, dtype):
+    return torch.tensor(np.asarray(x, np.float32)).to(dtype).cuda()
+
+
+def host64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def bf16_budget(w_new):
+    """Frobenius norm of the worst-case bf16 rounding of w_new (half ulp)."""
+    w = np.abs(np.asarray(w_new, np.float64))
+    ulp = np.exp2(np.floor(np.log2(np.maximum(w, 1e-30))) - 7)
+    return float(np.linalg.norm(0.5 * ulp))
+
+
+# ------------------------------------------------------------ self-test
+
+def test_bounded_wait_times_out_and_context_survives(pkg):
+    h = pkg.default_handle()
+    assert h.check() == 0
+    st = pkg.selftest_timeout(2_000_000)
+    assert st == 6                       # MUON_ERR_TIMEOUT
+    assert h.check() == 0                # word cleared, context usable
+    x = torch.ones(4, 4, device="cuda")
+    assert float(x.sum()) == 16.0
+
+
+# ------------------------------------------------------- orthogonalize
+
+ORTHO_SHAPES = [(256, 512), (100, 300), (300, 100), (1, 50), (50, 1), (64, 64), (129, 257)]
+
+
+@pytest.mark.parametrize("shape", ORTHO_SHAPES)
+def test_orthogonalize_fp32(pkg, shape):
+    X = wl.lowrank_grad(7, shape[0], shape[1], 32)
+    t = to_dev(X, torch.float32)
+    pkg.muon_orthogonalize(t)
+    ref = oracle.newton_schulz(X.astype(np.float64))
+    assert rel(host64(t), ref) < TOL_F32
+
+
+BF16_SHAPES = [(128, 512), (256, 1024), (200, 700), (700, 200), (1, 300), (300, 1), (384, 1536), (768, 768),
+               (130, 4100)]
+
+
+@pytest.mark.parametrize("shape", BF16_SHAPES)
+def test_orthogonalize_bf16(pkg, shape):
+    X = wl.lowrank_grad(8, shape[0], shape[1], 64)
+    t = to_dev(X, torch.bfloat16)
+    ref = oracle.newton_schulz(host64(t))
+    pkg.muon_orthogonalize(t)
+    assert rel(host64(t), ref) < TOL_BF16
+
+
+def test_orthogonalize_batched_bf16(pkg):
+    B, m, n = 5, 192, 320
+    X = np.stack([wl.lowrank_grad(50 + i, m, n, 32) for i in range(B)])
+    t = to_dev(X, torch.bfloat16)
+    inp = host64(t)
+    pkg.muon_orthogonalize(t)
+    out = host64(t)
+    for i in range(B):
+        assert rel(out[i], oracle.newton_schulz(inp[i])) < TOL_BF16
+
+
+@pytest.mark.parametrize("steps", [0, 1, 2])
+def test_orthogonalize_step_counts(pkg, steps):
+    X = wl.lowrank_grad(9, 96, 200, 16)
+    t32 = to_dev(X, torch.float32)
+    pkg.muon_orthogonalize(t32, steps=steps)
+    assert rel(host64(t32), oracle.newton_schulz(X.astype(np.float64), steps)) < TOL_F32
+    tb = to_dev(X, torch.bfloat16)
+    ref = oracle.newton_schulz(host64(tb), steps)
+    pkg.muon_orthogonalize(tb, steps=steps)
+    assert rel(host64(tb), ref) < TOL_BF16
+
+
+def test_orthogonalize_zero_and_empty(pkg):
+    z = torch.zeros(64, 128, device="cuda", dtype=torch.bfloat16)
+    pkg.muon_orthogonalize(z)
+    assert torch.count_nonzero(z).item() == 0
+    e = torch.zeros(0, 64, 128, device="cuda", dtype=torch.bfloat16)
+    pkg.muon_orthogonalize(e)
+
+
+# ----------------------------------------------------------- muon_step
+
+def run_step(pkg, specs, dtype, steps=1, ns_steps=5, lr=0.02, wd=0.1, mu=0.95, nesterov=True, seed=0):
+    """Run `steps` Muon steps on GPU and in the oracle from the same start;
+    return per-param (W_gpu, W_ref, W_decay_only, M_gpu, M_ref) after the
+    last step, W_decay_only = W0 * (1 - lr*wd)^steps (so W - W_decay_only is
+    the accumulated orthogonalised update)."""
+    W = [wl.weight(seed + 100 + i, s.shape) for i, s in enumerate(specs)]
+    Wd = [to_dev(w, dtype) for w in W]
+    Md = [torch.zeros(s.shape, dtype=torch.float32, device="cuda") for s in specs]
+    W_ref = [host64(w) for w in Wd]
+    W_decay = [w * (1 - lr * wd) ** steps for w in W_ref]
+    M_ref = [np.zeros(s.shape) for s in specs]
+    for k in range(steps):
+        G = [wl.lowrank_grad(seed + 1000 * k + i, s.shape[0], s.shape[1], 16, scale=1.0) for i, s in enumerate(specs)]
+        Gd = [to_dev(g, dtype) for g in G]
+        pkg.muon_step(Wd, Gd, Md, lr=lr, wd=wd, mu=mu, nesterov=nesterov, ns_steps=ns_steps,
+                      split_heads=[s.split_heads for s in specs])
+        for i, s in enumerate(specs):
+            W_ref[i], M_ref[i] = oracle.muon_step(W_ref[i], host64(Gd[i]), M_ref[i], lr=lr, wd=wd, mu=mu,
+                                                  nesterov=nesterov, steps=ns_steps, split_heads=s.split_heads)
+    torch.cuda.synchronize()
+    assert pkg.default_handle().check() == 0
+    return [(host64(Wd[i]), W_ref[i], W_decay[i], host64(Md[i]), M_ref[i]) for i in range(len(specs))]
+
+
+def delta_err(w_gpu, w_ref, base):
+    """Relative error of the accumulated update W - base."""
+    return rel(w_gpu - base, w_ref - base)
+
+
+def delta_err_bf16(w_gpu, w_ref, base, roundings):
+    """As delta_err, after subtracting the bf16 rounding budget of
+    `roundings` successive stores of the parameter."""
+    return (np.linalg.norm(w_gpu - w_ref) - roundings * bf16_budget(w_ref)) / np.linalg.norm(w_ref - base)
+
+
+def test_step_single_fp32_matrix(pkg):
+    # the single fp32 256x512 case: full-rank geometric spectrum, one step
+    ws = wl.single_matrix_256x512()
+    W0 = wl.weight(0, (256, 512))
+    G = wl.lowrank_grad(0, 256, 512, 256)
+    Wd, Gd = to_dev(W0, torch.float32), to_dev(G, torch.float32)
+    Md = torch.zeros(256, 512, dtype=torch.float32, device="cuda")
+    pkg.muon_step([Wd], [Gd], [Md], lr=0.02, wd=0.1, mu=0.95, nesterov=True)
+    W_ref, M_ref = oracle.muon_step(W0.astype(np.float64), G.astype(np.float64), np.zeros((256, 512)), lr=0.02,
+                                    wd=0.1, mu=0.95)
+    assert ws.muon[0].shape == (256, 512)
+    assert delta_err(host64(Wd), W_ref, W0.astype(np.float64) * (1 - 0.02 * 0.1)) < TOL_F32
+    assert rel(host64(Md), M_ref) < TOL_EXACT
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_step_without_ns_checks_momentum_and_update_arithmetic(pkg, dtype):
+    # ns_steps = 0: O = U/||U||_F, so W_new and M are fixed by plain arithmetic
+    specs = [wl.ParamSpec("a", (100, 300)), wl.ParamSpec("b", (300, 100)), wl.ParamSpec("c", (1, 77)),
+             wl.ParamSpec("d", (77, 1)), wl.ParamSpec("e", (64, 64))]
+    for w_gpu, w_ref, base, m_gpu, m_ref in run_step(pkg, specs, dtype, steps=2, ns_steps=0):
+        assert rel(m_gpu, m_ref) < TOL_EXACT
+        if dtype == torch.float32:
+            assert delta_err(w_gpu, w_ref, base) < TOL_EXACT
+        else:
+            assert delta_err_bf16(w_gpu, w_ref, base, 2) < TOL_EXACT
+
+
+def test_step_fp32_path_mixed_shapes(pkg):
+    specs = [wl.ParamSpec("a", (96, 160)), wl.ParamSpec("b", (160, 96)), wl.ParamSpec("c", (96, 160))]
+    for w_gpu, w_ref, base, m_gpu, m_ref in run_step(pkg, specs, torch.float32, steps=2):
+        assert delta_err(w_gpu, w_ref, base) < TOL_F32
+        assert rel(m_gpu, m_ref) < TOL_EXACT
+
+
+def test_step_bf16_gpt2_like(pkg):
+    # two layers of the GPT-2-small shapes, three consecutive steps
+    specs = wl.gpt2_small(layers=2).muon
+    for w_gpu, w_ref, base, m_gpu, m_ref in run_step(pkg, specs, torch.bfloat16, steps=3):
+        assert delta_err_bf16(w_gpu, w_ref, base, 3) < TOL_BF16
+        assert rel(m_gpu, m_ref) < TOL_EXACT
+
+
+def test_step_bf16_split_heads(pkg):
+    specs = [wl.ParamSpec("q", (512, 256), split_heads=4), wl.ParamSpec("k", (256, 512), split_heads=2)]
+    for w_gpu, w_ref, base, m_gpu, m_ref in run_step(pkg, specs, torch.bfloat16, steps=1):
+        assert delta_err_bf16(w_gpu, w_ref, base, 1) < TOL_BF16
+
+
+def test_step_is_deterministic(pkg):
+    specs = [wl.ParamSpec("a", (200, 640)), wl.ParamSpec("b", (640, 200))]
+    outs = []
+    for _ in range(2):
+        outs.append([r[0] for r in run_step(pkg, specs, torch.bfloat16, steps=2)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
+def test_step_nonfinite_gradient_is_reported(pkg):
+    W = to_dev(wl.weight(1, (64, 128)), torch.bfloat16)
+    G = to_dev(wl.gaussian(2, (64, 128)), torch.bfloat16)
+    G[3, 5] = float("nan")
+    M = torch.zeros(64, 128, device="cuda")
+    pkg.muon_step([W], [G], [M], lr=0.02, wd=0.1)
+    assert pkg.default_handle().check() == 5      # MUON_ERR_NONFINITE
+    assert pkg.default_handle().check() == 0
+
+
+def test_step_rejects_bad_arguments(pkg):
+    W = torch.zeros(64, 128, device="cuda", dtype=torch.bfloat16)
+    M = torch.zeros(64, 128, device="cuda")
+    with pytest.raises(pkg.MuonError) as e:
+        pkg.muon_step([W], [W], [M], lr=0.02, wd=0.1, split_heads=[3])
+    assert e.value.status == 1
+    with pytest.raises(ValueError):
+        pkg.muon_step([W], [W], [M.to(torch.bfloat16)], lr=0.02, wd=0.1)
+    pkg.muon_step([], [], [], lr=0.02, wd=0.1)     # no-op
+
+
+# --------------------------------------------------------------- AdamW
+
+@pytest.mark.parametrize("pdtype", [torch.float32, torch.bfloat16])
+def test_adamw_vs_oracle(pkg, pdtype):
+    sizes = [1, 17, 768, 3072, 40000]
+    P = [wl.gaussian(200 + i, (s,)) for i, s in enumerate(sizes)]
+    Pd = [to_dev(p, pdtype) for p in P]
+    Md = [torch.zeros(s, device="cuda") for s in sizes]
+    Vd = [torch.zeros(s, device="cuda") for s in sizes]
+    ref = [(host64(p), np.zeros(s), np.zeros(s)) for p, s in zip(Pd, sizes)]
+    kw = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1)
+    for t in range(1, 4):
+        G = [wl.gaussian(300 + 10 * t + i, (s,)) for i, s in enumerate(sizes)]
+        Gd = [to_dev(g, pdtype) for g in G]
+        pkg.adamw_step(Pd, Gd, Md, Vd, step=t, **kw)
+        ref = [oracle.adamw_step(p, host64(g), m, v, t, **kw) for (p, m, v), g in zip(ref, Gd)]
+    torch.cuda.synchronize()
+    for (p, m, v), pd, md, vd in zip(ref, Pd, Md, Vd):
+        assert rel(host64(md), m) < TOL_EXACT
+        assert rel(host64(vd), v) < TOL_EXACT
+        if pdtype == torch.float32:
+            assert rel(host64(pd), p) < TOL_EXACT
+        else:
+            assert np.linalg.norm(host64(pd) - p) <= 3 * bf16_budget(p) + TOL_EXACT * np.linalg.norm(p)
+
+
+# ---------------------------------------------------------------- Gram
+
+GRAM_BF16 = [(256, 4096), (128, 2048), (200, 700), (700, 200), (1, 300), (130, 1000), (256, 512)]
+
+
+@pytest.mark.parametrize("shape", GRAM_BF16)
+def test_orthogonalize_gram_bf16(pkg, shape):
+    rank = min(shape) if shape == (256, 512) else 64
+    X = wl.lowrank_grad(11, shape[0], shape[1], rank)
+    t = to_dev(X, torch.bfloat16)
+    ref = oracle.gram_newton_schulz(host64(t))
+    pkg.muon_orthogonalize(t, ns_method="gram")
+    assert rel(host64(t), ref) < TOL_BF16
+
+
+@pytest.mark.parametrize("shape", [(100, 300), (300, 100), (64, 512), (1, 40)])
+def test_orthogonalize_gram_fp32(pkg, shape):
+    X = wl.lowrank_grad(12, shape[0], shape[1], 32)
+    t = to_dev(X, torch.float32)
+    pkg.muon_orthogonalize(t, ns_method="gram")
+    assert rel(host64(t), oracle.gram_newton_schulz(X.astype(np.float64))) < TOL_F32
+
+
+@pytest.mark.parametrize("steps", [0, 1, 3])
+def test_orthogonalize_gram_step_counts(pkg, steps):
+    X = wl.lowrank_grad(13, 96, 640, 16)
+    tb = to_dev(X, torch.bfloat16)
+    ref = oracle.gram_newton_schulz(host64(tb), steps)
+    pkg.muon_orthogonalize(tb, steps=steps, ns_method="gram")
+    assert rel(host64(tb), ref) < TOL_BF16
+
+
+def test_step_gram_bf16(pkg):
+    specs = [wl.ParamSpec("a", (128, 1024)), wl.ParamSpec("b", (1024, 128)), wl.ParamSpec("c", (256, 768))]
+    W = [wl.weight(400 + i, s.shape) for i, s in enumerate(specs)]
+    Wd = [to_dev(w, torch.bfloat16) for w in W]
+    Md = [torch.zeros(s.shape, device="cuda") for s in specs]
+    W0 = [host64(w) for w in Wd]
+    G = [to_dev(wl.lowrank_grad(500 + i, s.shape[0], s.shape[1], 32), torch.bfloat16) for i, s in enumerate(specs)]
+    pkg.muon_step(Wd, G, Md, lr=0.02, wd=0.1, ns_method="gram")
+    assert pkg.default_handle().check() == 0
+    for i in range(len(specs)):
+        w_ref, m_ref = oracle.muon_step(W0[i], host64(G[i]), np.zeros(specs[i].shape), lr=0.02, wd=0.1,
+                                        method="gram")
+        base = W0[i] * (1 - 0.02 * 0.1)
+        assert delta_err_bf16(host64(Wd[i]), w_ref, base, 1) < TOL_BF16
+        assert rel(host64(Md[i]), m_ref) < TOL_EXACT
