@@ -126,20 +126,35 @@ class ClockSampler:
 
 # ------------------------------------------------------------ workload
 
-def make_inputs(specs, device, seed, names_to_keep=()):
+def make_inputs(specs, device, seed, batch=32):
     """Seeded synthetic tensors on the device: W ~ N(0, 0.02) bf16, G low-rank
-    (rank 64, sigma_i = 0.5**(i/8)) + 1e-3 noise bf16, M = 0 fp32."""
+    (rank 64, orthonormal factors, sigma_i = 0.5**(i/8)) + 1e-3 N(0,1) noise,
+    bf16, M = 0 fp32.  Same-shape matrices are drawn in batches."""
     import torch
     from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
-    W, G, M = [], [], []
+    W, G, M = [None] * len(specs), [None] * len(specs), [None] * len(specs)
+    by_shape = {}
     for i, s in enumerate(specs):
-        gen = torch.Generator(device=device)
-        gen.manual_seed(wl.matrix_seed(seed, i))
-        w = torch.randn(s.shape, generator=gen, device=device).mul_(0.02).to(torch.bfloat16)
-        g = wl.lowrank_grad_device(gen, s.shape[0], s.shape[1], 64, noise=1e-3, device=device)
-        W.append(w)
-        G.append(g)
-        M.append(torch.zeros(s.shape, dtype=torch.float32, device=device))
+        by_shape.setdefault(tuple(s.shape), []).append(i)
+    gen = torch.Generator(device=device)
+    for k, (shape, idx) in enumerate(sorted(by_shape.items())):
+        gen.manual_seed(wl.matrix_seed(seed, k))
+        rows, cols = shape
+        r = min(64, rows, cols)
+        sigma = 0.5 ** (torch.arange(r, device=device, dtype=torch.float32) / 8.0)
+        for c0 in range(0, len(idx), batch):
+            part = idx[c0:c0 + batch]
+            nb = len(part)
+            U, _ = torch.linalg.qr(torch.randn(nb, rows, r, generator=gen, device=device))
+            V, _ = torch.linalg.qr(torch.randn(nb, cols, r, generator=gen, device=device))
+            g = torch.bmm(U * sigma, V.transpose(1, 2))
+            g.add_(torch.randn(nb, rows, cols, generator=gen, device=device), alpha=1e-3)
+            w = torch.randn(nb, rows, cols, generator=gen, device=device).mul_(0.02)
+            for j, i in enumerate(part):
+                G[i] = g[j].to(torch.bfloat16)
+                W[i] = w[j].to(torch.bfloat16)
+                M[i] = torch.zeros(shape, dtype=torch.float32, device=device)
+            del U, V, g, w
     return W, G, M
 
 

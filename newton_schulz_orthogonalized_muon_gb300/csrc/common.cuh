@@ -222,4 +222,57 @@ __device__ __forceinline__ void store_out_scalar(const OutEntry& e, int r, int c
   store_from_f32(e.ptr, idx, e.dtype, v);
 }
 
+// Sixteen consecutive outputs o[0..15] of row r starting at column c0 (all
+// in range).  Non-transposed destinations whose row segment is 16-byte
+// aligned use vector loads and stores; everything else goes element by
+// element (transposed writes are coalesced across the warp, whose lanes hold
+// consecutive rows).
+__device__ __forceinline__ void store_out_16(const OutEntry& e, int r, int c0, const float* o) {
+  if (!e.transposed) {
+    const long long idx = static_cast<long long>(r) * e.ld + c0;
+    if (e.dtype == DT_BF16 && ((reinterpret_cast<uintptr_t>(reinterpret_cast<__nv_bfloat16*>(e.ptr) + idx) & 15) == 0)) {
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(e.ptr) + idx);
+      uint4 w[2];
+      if (e.alpha != 0.f) {
+        w[0] = dst[0];
+        w[1] = dst[1];
+      }
+      const __nv_bfloat162* old = reinterpret_cast<const __nv_bfloat162*>(w);
+      uint4 res[2];
+      uint32_t* rp = reinterpret_cast<uint32_t*>(res);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float v0 = e.beta * o[2 * k], v1 = e.beta * o[2 * k + 1];
+        if (e.alpha != 0.f) {
+          const float2 f = __bfloat1622float2(old[k]);
+          v0 = fmaf(e.alpha, f.x, v0);
+          v1 = fmaf(e.alpha, f.y, v1);
+        }
+        rp[k] = pack_bf16x2(v0, v1);
+      }
+      dst[0] = res[0];
+      dst[1] = res[1];
+      return;
+    }
+    if (e.dtype == DT_F32 && ((reinterpret_cast<uintptr_t>(reinterpret_cast<float*>(e.ptr) + idx) & 15) == 0)) {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.ptr) + idx);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 v = make_float4(e.beta * o[4 * q], e.beta * o[4 * q + 1], e.beta * o[4 * q + 2], e.beta * o[4 * q + 3]);
+        if (e.alpha != 0.f) {
+          const float4 w = dst[q];
+          v.x = fmaf(e.alpha, w.x, v.x);
+          v.y = fmaf(e.alpha, w.y, v.y);
+          v.z = fmaf(e.alpha, w.z, v.z);
+          v.w = fmaf(e.alpha, w.w, v.w);
+        }
+        dst[q] = v;
+      }
+      return;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) store_out_scalar(e, r, c0 + k, o[k]);
+}
+
 }  // namespace muon

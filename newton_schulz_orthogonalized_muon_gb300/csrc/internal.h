@@ -60,11 +60,13 @@ struct AdamParams {
 };
 
 // ------------------------------------------------ Newton-Schulz GEMMs
-// Modes of the NS GEMM kernels:
-//   SYRK   A = s^2 * X X^T        (symmetric, upper tiles computed, mirrored)
-//   POLY   B = b*A + c*A A        (symmetric, upper tiles computed, mirrored)
-//   UPDATE X' = s*(a*X + B X)     (fp32 master + bf16 operand copy)
-//   FINAL  out = alpha*out + beta*s*(a*X + B X)  (parameter or caller matrix)
+// Modes of the NS GEMM kernels (tensor-core path; P^ = bf16(P), X^ = bf16(X)):
+//   SYRK   A = s^2 * X^ X^^T                 (symmetric, upper tiles, mirrored)
+//   POLY   P = a*I + b*A + c*A A             (symmetric; fp32 diagonal kept aside)
+//   UPDATE X' = s*(P^ X^ + P_rr X - P^_rr X^)   (fp32 master + bf16 operand copy)
+//   FINAL  out = alpha*out + beta*X'         (parameter or caller matrix)
+// The fp32 path (CUDA cores) evaluates the same iteration as
+//   SYRK A = s^2 X X^T, POLY B = b*A + c*A A, UPDATE X' = s*(a*X + B X).
 //
 // Gram method (iterates on R = X X^T; every matrix below is m x m, symmetric,
 // and stored as a pair of bf16 planes hi + lo, hi = bf16(v), lo = bf16(v - hi),
@@ -99,6 +101,7 @@ struct NsGemmParams {
   void* sym_out_lo;             // Gram modes: lo plane of the output
   const void* sym_in_lo;        // G_P: R lo plane
   const void* op_b;             // fp32 path, G_PROD: the second factor
+  float* pdiag;                 // tensor-core path: fp32 diagonal of P [batch][m]
   long long ldm;
   // X master / operand copies, row stride ldx
   float* xf;                    // fp32 master (read and written in place)
@@ -123,8 +126,9 @@ cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0
 size_t ns_gemm_tc_smem_bytes(int bn);
 int ns_gemm_tc_stages(int bn);
 
-// fp32 SIMT path (CUDA cores, fp32 FMA)
-cudaError_t launch_ns_gemm_simt(int mode, const NsGemmParams& p, cudaStream_t s);
+// fp32 SIMT path (CUDA cores).  wide = 0: fp32 m x m matrices; wide = 1:
+// fp64 m x m matrices and accumulation (Gram modes of the fp32 path).
+cudaError_t launch_ns_gemm_simt(int mode, const NsGemmParams& p, cudaStream_t s, int wide = 0);
 
 // elementwise
 cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s);

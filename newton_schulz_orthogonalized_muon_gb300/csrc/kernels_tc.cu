@@ -1,23 +1,31 @@
 // Tensor-core Newton-Schulz GEMMs for sm_103a (tcgen05 + TMA + TMEM).
 //
-// One quintic NS iteration on X (m x n, m <= n) is, in Horner form,
-//   A = X X^T,  B = b A + c A A,  X <- a X + B X
+// One quintic NS iteration on X (m x n, m <= n) is X <- P X with
+//   A = X X^T,  P = a I + b A + c A A
 // ("Muon Optimizer and the Distributed Implementation", §Newton-Schulz
-// Iteration; "DeepSpeed 集成 Muon 优化器实战", §核心算子, coefficients
-// (3.4445, -4.7750, 2.0315)).  Each product is one launch of the persistent
-// kernel below in one of four modes:
+// Iteration: phi(X) = (a + b XX^T + c (XX^T)^2) X; "DeepSpeed 集成 Muon 优化器
+// 实战", §核心算子, coefficients (3.4445, -4.7750, 2.0315)).  Each product is
+// one launch of the persistent kernel below in one of four modes:
 //
 //   SYRK   A = s^2 X X^T    K = n, both operands K-major rows of X (bf16);
 //                           only tiles touching the upper triangle are
 //                           computed, each element c >= r is written to
 //                           (r, c) and mirrored to (c, r).
-//   POLY   B = b A + c A A  K = m, A symmetric so A A = A A^T: same operand
+//   POLY   P = a I + b A + c A A
+//                           K = m, A symmetric so A A = A A^T: same operand
 //                           form as SYRK; the b*A term is read back in the
-//                           epilogue; symmetric output as above.
-//   UPDATE X = s (a X + B X) K = m, A operand = rows of B (K-major), B
-//                           operand = X read MN-major (n contiguous); the
-//                           epilogue reads the fp32 master X and writes the
-//                           new fp32 master and its bf16 operand copy.
+//                           epilogue; symmetric bf16 output as above, and
+//                           the fp32 diagonal P_rr stored on the side.
+//   UPDATE X = s (P^ X^ + P_rr X - P^_rr X^)
+//                           K = m, A operand = rows of P^ = bf16(P)
+//                           (K-major), B operand = X^ = bf16(X) read MN-major
+//                           (n contiguous).  The diagonal of P carries the
+//                           large coefficient a = 3.4445 while a + (bA+cA^2)_rr
+//                           is O(1): rounding P's diagonal to bf16 would be
+//                           amplified by that cancellation, so the epilogue
+//                           swaps the rounded diagonal term P^_rr X^ in the
+//                           accumulator for the exact one P_rr X (fp32 master
+//                           X).  Writes the new fp32 master and its bf16 copy.
 //   FINAL  like UPDATE, but the result goes straight into its destination
 //          (the parameter: W <- (1 - lr wd) W - lr 0.2 sqrt(max(A,B)) O,
 //          transposed back where the NS ran on W^T; or the caller's matrix).
@@ -155,7 +163,10 @@ __device__ __forceinline__ void epilogue_sym(const NsGemmParams& p, int b, int g
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       v[e] = fmaf(p.cb, a[e], p.cc * v[e]);
-      if (MODE == MODE_G_P && gc0 + e == gr) v[e] += p.ca;
+      if (gc0 + e == gr) {
+        v[e] += p.ca;
+        if (MODE == MODE_POLY) p.pdiag[mat + gr] = v[e];
+      }
     }
   }
   constexpr bool kPlanes = ModeTraits<MODE>::kPlanesOut;
@@ -210,28 +221,36 @@ __device__ __forceinline__ void epilogue_update(const NsGemmParams& p, int b, in
   if (MODE == MODE_G_FINAL) {
     const OutEntry oe = p.out[b];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int gc = gc0 + e;
-      if (gc < n) store_out_scalar(oe, gr, gc, s * v[e]);
+    for (int e = 0; e < 16; ++e) v[e] *= s;
+    if (gc0 + 15 < n) {
+      store_out_16(oe, gr, gc0, v);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (gc0 + e < n) store_out_scalar(oe, gr, gc0 + e, v[e]);
     }
     return;
   }
   const size_t rowoff = (static_cast<size_t>(b) * p.m + gr) * p.ldx;
   float* xrow = p.xf + rowoff;
+  // exact diagonal term: acc + P_rr x - P^_rr x^  (x^ = bf16(x) is the operand copy)
+  const float pd = p.pdiag[static_cast<size_t>(b) * p.m + gr];
+  const float pdb = bf2f(f2bf(pd));
   if (gc0 + 15 < n) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 x = *reinterpret_cast<const float4*>(xrow + gc0 + 4 * q);
-      v[4 * q + 0] = s * fmaf(p.ca, x.x, v[4 * q + 0]);
-      v[4 * q + 1] = s * fmaf(p.ca, x.y, v[4 * q + 1]);
-      v[4 * q + 2] = s * fmaf(p.ca, x.z, v[4 * q + 2]);
-      v[4 * q + 3] = s * fmaf(p.ca, x.w, v[4 * q + 3]);
+      const float4 x4 = *reinterpret_cast<const float4*>(xrow + gc0 + 4 * q);
+      const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[4 * q + k] = s * fmaf(pd, xs[k], fmaf(-pdb, bf2f(f2bf(xs[k])), v[4 * q + k]));
     }
   } else {
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const int gc = gc0 + e;
-      v[e] = gc < n ? s * fmaf(p.ca, xrow[gc], v[e]) : 0.f;
+      const float x = gc < n ? xrow[gc] : 0.f;
+      v[e] = gc < n ? s * fmaf(pd, x, fmaf(-pdb, bf2f(f2bf(x)), v[e])) : 0.f;
     }
   }
   if (MODE == MODE_UPDATE) {
@@ -258,10 +277,12 @@ __device__ __forceinline__ void epilogue_update(const NsGemmParams& p, int b, in
     }
   } else {
     const OutEntry oe = p.out[b];
+    if (gc0 + 15 < n) {
+      store_out_16(oe, gr, gc0, v);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int gc = gc0 + e;
-      if (gc < n) store_out_scalar(oe, gr, gc, v[e]);
+      for (int e = 0; e < 16; ++e)
+        if (gc0 + e < n) store_out_scalar(oe, gr, gc0 + e, v[e]);
     }
   }
 }

@@ -236,16 +236,16 @@ struct GroupPlan {
 
 // Workspace region offsets for one chunk capacity `cap` (bytes from ws base).
 //   standard, tensor cores: fp32 master X, two bf16 operand copies (ping-pong),
-//                           bf16 A and B
+//                           bf16 A and P, fp32 diagonal of P
 //   standard, fp32 path:    two fp32 X buffers (ping-pong), fp32 A and B
 //   gram, tensor cores:     bf16 X0 (+ fp32 X0 when no NS step runs) and six
 //                           m x m slots (R, T, P0, P1, Q0, Q1) of two bf16 planes
-//   gram, fp32 path:        fp32 X0 and six fp32 m x m slots
+//   gram, fp32 path:        fp32 X0 and six fp64 m x m slots
 constexpr int kGramSlots = 6;
 enum { SLOT_R = 0, SLOT_T = 1, SLOT_P0 = 2, SLOT_Q0 = 4 };
 
 struct Regions {
-  size_t xf, xf2, xb0, xb1, symA, symB, partials, scale, total;
+  size_t xf, xf2, xb0, xb1, symA, symB, pdiag, partials, scale, total;
   size_t slot[kGramSlots], slot_lo[kGramSlots];
 };
 
@@ -266,6 +266,7 @@ Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
       r.xb1 = take(xe * 2);
       r.symA = take(se * 2);
       r.symB = take(se * 2);
+      r.pdiag = take(static_cast<size_t>(cap) * g.m * 4);
     } else {
       r.xf2 = take(xe * 4);
       r.symA = take(se * 4);
@@ -281,7 +282,7 @@ Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
       }
     } else {
       r.xf = take(xe * 4);
-      for (int k = 0; k < kGramSlots; ++k) r.slot[k] = take(se * 4);
+      for (int k = 0; k < kGramSlots; ++k) r.slot[k] = take(se * 8);
     }
   }
   r.partials = take(static_cast<size_t>(cap) * g.prep_tiles * 4);
@@ -373,7 +374,7 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
         MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_G_R0, g.bn_sym, map_x, map_x, r0, grid, stream), "gram r0");
       } else {
         r0.xf_in = xf;
-        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_G_R0, r0, stream), "gram r0");
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_G_R0, r0, stream, 1), "gram r0");
       }
     }
     auto sym_product = [&](int mode, int a, int b, int out, int cls) -> muon_status_t {
@@ -387,7 +388,7 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
         MUON_LAUNCH(cls, launch_ns_gemm_tc_planes(mode, 128, mhi[a], mlo[a], mhi[b], mlo[b], t, grid_sym, stream),
                     "gram product");
       } else {
-        MUON_LAUNCH(cls, launch_ns_gemm_simt(mode, t, stream), "gram product");
+        MUON_LAUNCH(cls, launch_ns_gemm_simt(mode, t, stream, 1), "gram product");
       }
       return MUON_OK;
     };
@@ -425,7 +426,7 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
                   "gram final");
     } else {
       f.xf_in = xf;
-      MUON_LAUNCH(MUON_K_FINAL, launch_ns_gemm_simt(MODE_G_FINAL, f, stream), "gram final");
+      MUON_LAUNCH(MUON_K_FINAL, launch_ns_gemm_simt(MODE_G_FINAL, f, stream, 1), "gram final");
     }
   }
   return MUON_OK;
@@ -514,6 +515,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                             tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb1) : nullptr};
     void* symA = ws + R.symA;
     void* symB = ws + R.symB;
+    float* pdiag = tc ? reinterpret_cast<float*>(ws + R.pdiag) : nullptr;
     float* partials = reinterpret_cast<float*>(ws + R.partials);
     float* scale = reinterpret_cast<float*>(ws + R.scale);
 
@@ -567,6 +569,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         p.out = out_d;
         p.err = h->err;
         p.timeout_ns = h->timeout_ns;
+        p.pdiag = pdiag;
         if (tc) {
           // SYRK: A = s^2 X X^T
           NsGemmParams q = p;
@@ -577,12 +580,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           int grid = std::min(q.num_tiles, h->num_sms);
           MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], q, grid, stream),
                       "syrk launch");
-          // POLY: B = b A + c A A
+          // POLY: P = a I + b A + c A A
           q.scale = nullptr;
           q.sym_in = symA;
           q.sym_out = symB;
           MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, q, grid, stream), "poly launch");
-          // UPDATE / FINAL: X = s (a X + B X)
+          // UPDATE / FINAL: X = s (P^ X^ + P_rr X - P^_rr X^)
           NsGemmParams u = p;
           u.mi = mi;
           u.tiles_per_mat = mi * nj;
