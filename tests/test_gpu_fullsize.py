@@ -64,3 +64,46 @@ def test_llama3_8b_full_set_sampled():
 
 def test_moonlight_moe_full_set_sampled():
     _run_and_check("moonlight-moe", ["layers.26.experts.63.down_proj.weight", "layers.5.attn.v_proj.weight"])
+
+
+def test_gpt2_small_three_steps_with_adamw():
+    """The whole GPT-2-small-shaped set: 48 Muon matrices (bf16, grads
+    scaled 1e-3) and 98 LayerNorm/bias vectors on AdamW, three consecutive
+    steps, every tensor checked against the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+    ws = wl.gpt2_small()
+    lr, wd, lr_adam = 0.02, 0.1, 3e-4
+    Wd = [torch.tensor(wl.weight(10 + i, s.shape)).to(torch.bfloat16).cuda() for i, s in enumerate(ws.muon)]
+    Md = [torch.zeros(s.shape, device="cuda") for s in ws.muon]
+    W_ref = [w.double().cpu().numpy() for w in Wd]
+    W0 = [w.copy() for w in W_ref]
+    M_ref = [np.zeros(s.shape) for s in ws.muon]
+    Pd = [torch.tensor(wl.weight(900 + i, s.shape)).to(torch.bfloat16).cuda() for i, s in enumerate(ws.adamw)]
+    Ad = [torch.zeros(s.shape, device="cuda") for s in ws.adamw]
+    Vd = [torch.zeros(s.shape, device="cuda") for s in ws.adamw]
+    P_ref = [(p.double().cpu().numpy(), np.zeros(s.shape), np.zeros(s.shape)) for p, s in zip(Pd, ws.adamw)]
+    for t in range(1, 4):
+        G = [torch.tensor(wl.lowrank_grad(1000 * t + i, s.shape[0], s.shape[1], 64, scale=ws.grad_scale))
+             .to(torch.bfloat16).cuda() for i, s in enumerate(ws.muon)]
+        Ga = [torch.tensor(wl.gaussian(5000 * t + i, s.shape, 1e-3)).to(torch.bfloat16).cuda()
+              for i, s in enumerate(ws.adamw)]
+        pkg.muon_step(Wd, G, Md, lr=lr, wd=wd, mu=0.95, nesterov=True)
+        pkg.adamw_step(Pd, Ga, Ad, Vd, step=t, lr=lr_adam, beta1=0.9, beta2=0.95, eps=1e-8, wd=wd)
+        for i in range(len(ws.muon)):
+            W_ref[i], M_ref[i] = oracle.muon_step(W_ref[i], G[i].double().cpu().numpy(), M_ref[i], lr=lr, wd=wd)
+        P_ref = [oracle.adamw_step(p, g.double().cpu().numpy(), m, v, t, lr=lr_adam, beta1=0.9, beta2=0.95,
+                                   eps=1e-8, wd=wd) for (p, m, v), g in zip(P_ref, Ga)]
+    assert pkg.default_handle().check() == 0
+    for i in range(len(ws.muon)):
+        base = W0[i] * (1 - lr * wd) ** 3
+        w_gpu = Wd[i].double().cpu().numpy()
+        err = (np.linalg.norm(w_gpu - W_ref[i]) - 3 * _budget(W_ref[i])) / np.linalg.norm(W_ref[i] - base)
+        assert err < TOL_BF16, (ws.muon[i].name, err)
+        assert _rel(Md[i].double().cpu().numpy(), M_ref[i]) < TOL_EXACT
+    for (p, m, v), pd, md, vd in zip(P_ref, Pd, Ad, Vd):
+        assert _rel(md.double().cpu().numpy(), m) < TOL_EXACT
+        assert _rel(vd.double().cpu().numpy(), v) < TOL_EXACT
+        assert np.linalg.norm(pd.double().cpu().numpy() - p) <= 3 * _budget(p) + TOL_EXACT * np.linalg.norm(p)
