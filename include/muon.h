@@ -150,6 +150,27 @@ muon_status_t adamw_step(muon_handle_t h, void* const* params, const void* const
  * Exercises the timeout path without hanging the GPU. */
 muon_status_t muon_selftest_timeout(muon_handle_t h, uint64_t timeout_ns, void* stream);
 
+/* Allocation-free orthogonalisation of ONE matrix, for callers that cannot
+ * allocate device memory (code inside a CUDA graph capture that forbids
+ * allocation, embedded runtimes with a fixed memory budget, processes whose
+ * device memory is owned by a custom allocator).  Same result as
+ * muon_orthogonalize(batch = 1, ns_method = standard); no handle needed.
+ * (The source pages have no counterpart: this is a deployment variant.)
+ *   X, dtype, m, n, steps, coeffs, stream: as in muon_orthogonalize.
+ * Scratch: a 24 MiB file-scope device array inside the library, held by every
+ * GPU that loads the library until the process exits.  Limits:
+ * min(m, n) <= 1024 and m*n <= 2^20 elements; larger sizes return
+ * MUON_ERR_INVALID_ARG before anything is enqueued.  Calls no cudaMalloc,
+ * cudaFree or allocating library routine.  The first call on each device
+ * (with that device current) resolves the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the one array and leaves its contents behind: calls
+ * that may overlap on the GPU (different streams without ordering) race and
+ * must be serialised by the caller.  Device-side errors (a timed-out wait)
+ * are recorded in a word inside the array, which is cleared at each call. */
+muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int64_t m, int64_t n, int32_t steps,
+                                         const float* coeffs, void* stream);
+
 /* Kernel classes reported by muon_handle_profile(). */
 enum {
   MUON_K_PREPARE = 0, /* momentum / Nesterov / norm partials / working copy */

@@ -26,7 +26,8 @@ _STATUS = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_UNSUPPORTED", 3
 EXPORTS = ("muon_handle_create", "muon_handle_destroy", "muon_handle_set_workspace_limit",
            "muon_handle_set_timeout_ns", "muon_handle_check", "muon_orthogonalize", "muon_step",
            "adamw_step", "muon_selftest_timeout", "muon_status_string", "muon_last_error", "muon_version",
-           "muon_handle_set_profiling", "muon_handle_profile", "muon_handle_launch_count")
+           "muon_handle_set_profiling", "muon_handle_profile", "muon_handle_launch_count",
+           "muon_orthogonalize_noalloc")
 KERNEL_CLASSES = ("prepare", "norm", "syrk", "poly", "update", "final", "apply", "adamw")
 
 
@@ -79,6 +80,7 @@ def load_library(path: str | None = None):
             "muon_handle_set_profiling": (i32, [vp, i32]),
             "muon_handle_profile": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64), i32]),
             "muon_handle_launch_count": (i32, [vp, ctypes.POINTER(u64)]),
+            "muon_orthogonalize_noalloc": (i32, [vp, i32, i64, i64, i32, fptr, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -203,6 +205,22 @@ def muon_orthogonalize(X: torch.Tensor, steps: int = 5, coeffs=None, ns_method="
     st = h._lib.muon_orthogonalize(h.ptr, ctypes.c_void_p(X.data_ptr()), _dtype_code(X), batch, m, n, int(steps),
                                    _coeffs(coeffs), _method(ns_method), ctypes.c_void_p(_stream_ptr(stream)))
     h._raise(st, "muon_orthogonalize")
+    return X
+
+
+def muon_orthogonalize_noalloc(X: torch.Tensor, steps: int = 5, coeffs=None, stream=None) -> torch.Tensor:
+    """In-place orthogonalisation of one 2-D matrix without any device
+    allocation (static scratch inside the library; see include/muon.h for
+    the size limits and the sharing rules)."""
+    _need_cuda(X, "X")
+    if X.dim() != 2:
+        raise ValueError("X must be 2-D")
+    lib = load_library()
+    with torch.cuda.device(X.device):
+        st = lib.muon_orthogonalize_noalloc(ctypes.c_void_p(X.data_ptr()), _dtype_code(X), X.shape[0], X.shape[1],
+                                            int(steps), _coeffs(coeffs), ctypes.c_void_p(_stream_ptr(stream)))
+    if st != 0:
+        raise MuonError(st, "muon_orthogonalize_noalloc")
     return X
 
 
