@@ -44,12 +44,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["llama3-8b", "gpt2-small", "moonlight-moe"], default="llama3-8b")
+    ap.add_argument("--workload", choices=["llama3-8b", "gpt2-small", "moonlight-moe", "wide"], default="llama3-8b",
+                    help="wide: the standard-vs-gram sweep over 64 Gaussian m x n matrices per shape")
     ap.add_argument("--ns-method", choices=["standard", "gram"], default="standard")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (parity runs only)")
     ap.add_argument("--workspace-gb", type=float, default=64.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args(argv)
 
@@ -128,8 +130,9 @@ class ClockSampler:
 
 def make_inputs(specs, device, seed, batch=32):
     """Seeded synthetic tensors on the device: W ~ N(0, 0.02) bf16, G low-rank
-    (rank 64, orthonormal factors, sigma_i = 0.5**(i/8)) + 1e-3 N(0,1) noise,
-    bf16, M = 0 fp32.  Same-shape matrices are drawn in batches."""
+    (rank 64, orthonormal factors from QR of Gaussians, sigma_i = 0.5**(i/8))
+    + 1e-3 N(0,1) noise, bf16, M = 0 fp32.  Same-shape matrices are drawn in
+    batches from one seeded torch.Generator per shape."""
     import torch
     from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
     W, G, M = [None] * len(specs), [None] * len(specs), [None] * len(specs)
@@ -289,7 +292,7 @@ def run_ours(args):
     barrier()
     ms = e0.elapsed_time(e1) / max(args.steps, 1)
     launches = h.launch_count() - launches0
-    prof = h.profile()
+    records = h.profile_records()
     h.set_profiling(False)
     clk = clocks.stop()
     status = h.check()
@@ -308,52 +311,66 @@ def run_ours(args):
         ms_max, alg_all, dense_all = ms, alg, dense
     value = alg_all / (ms_max / 1e3) / 1e12
 
-    # ---- roofline of the dominant kernel class, timed live above
+    # ---- per kernel class and per (class, same-shape group), timed live above
     peaks, peak_src = load_peaks()
-    per_class = {"syrk": 0.0, "poly": 0.0, "update": 0.0, "final": 0.0}
-    for s in specs:
-        m, n = flops.ns_dims(s.shape[0], s.shape[1], s.split_heads)
-        kf = flops.kernel_flops_standard(m, n)
-        per_class["syrk"] += s.split_heads * NS_STEPS * kf["syrk"]
-        per_class["poly"] += s.split_heads * NS_STEPS * kf["poly"]
-        per_class["update"] += s.split_heads * (NS_STEPS - 1) * kf["update"]
-        per_class["final"] += s.split_heads * kf["update"]
-    kernel_rows = {}
-    for k, (kms, cnt) in prof.items():
-        if cnt == 0:
-            continue
-        row = {"ms_per_step": kms / args.steps, "launches_per_step": cnt / args.steps}
-        if k in per_class and kms > 0:
-            row["tflops"] = per_class[k] * args.steps / (kms / 1e3) / 1e12
-        kernel_rows[k] = row
-    gemm = {k: v for k, v in kernel_rows.items() if k in per_class}
-    dom = max(gemm, key=lambda k: gemm[k]["ms_per_step"]) if gemm else None
+    groups = {}
+    for s_ in specs:
+        mn = flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads)
+        groups[mn] = groups.get(mn, 0) + s_.split_heads
+    group_list = sorted(groups.items())            # the library's group order: ascending (m, n)
+    iters = {"syrk": NS_STEPS, "poly": NS_STEPS, "update": NS_STEPS - 1, "final": 1}
+    kernel_rows, per_group = {}, {}
+    for k, tag, kms in records:
+        row = kernel_rows.setdefault(k, {"ms_per_step": 0.0, "launches_per_step": 0.0})
+        row["ms_per_step"] += kms / args.steps
+        row["launches_per_step"] += 1.0 / args.steps
+        if k in iters and 0 <= tag < len(group_list):
+            key = (k, tag)
+            e = per_group.setdefault(key, [0.0, 0])
+            e[0] += kms
+            e[1] += 1
+    class_flops = {k: 0.0 for k in iters}
+    group_rows = []
+    for (k, tag), (kms, cnt) in sorted(per_group.items(), key=lambda x: -x[1][0]):
+        (m, n), count = group_list[tag]
+        kf = flops.kernel_flops_standard(m, n)[k if k != "final" else "update"]
+        fl = count * iters[k] * args.steps * kf
+        class_flops[k] += fl
+        group_rows.append({"kernel": k, "group": f"{m}x{n}", "matrices": count, "launches": cnt,
+                           "ms_per_launch": kms / cnt, "flops_per_launch": fl / cnt,
+                           "tflops": fl / (kms / 1e3) / 1e12})
+    for k, row in kernel_rows.items():
+        if k in class_flops and row["ms_per_step"] > 0:
+            row["tflops"] = class_flops[k] / (row["ms_per_step"] * args.steps / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if dom and os.path.exists(tpath):
-        try:
-            tr = json.load(open(tpath))
-            entry = tr.get(args.workload, {}).get(dom)
-            if entry and entry.get("kernel_source_hash") == kernel_source_hash():
-                traffic = entry.get("bytes_per_launch")
-        except Exception:
-            traffic = None
     roofline = None
-    if dom:
-        ach = gemm[dom]["tflops"]
-        launches_dom = max(gemm[dom]["launches_per_step"], 1)
-        roofline = {"bound": "tensor", "kernel": f"ns_gemm_tc_kernel<{dom}>", "achieved": ach, "peak": peak,
-                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
-                    "flops_per_launch": per_class[dom] / launches_dom,
-                    "ms_per_launch": gemm[dom]["ms_per_step"] / launches_dom,
-                    "peak_source": f"bf16_tflops_sustained, {peak_src}"}
+    if group_rows:
+        top = group_rows[0]          # the (class, group) with the most time
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tpath):
+            try:
+                entry = json.load(open(tpath)).get(ws.name, {}).get(f"{top['kernel']}@{top['group']}")
+                if entry and entry.get("kernel_source_hash") == kernel_source_hash():
+                    traffic = entry.get("bytes_per_launch")
+            except Exception:
+                traffic = None
+        roofline = {"bound": "tensor", "kernel": f"ns_gemm_tc_kernel<{top['kernel']}> on the {top['group']} group "
+                                                  f"({top['matrices']} matrices)",
+                    "achieved": top["tflops"], "peak": peak, "unit": "TFLOP/s", "frac": top["tflops"] / peak,
+                    "traffic": traffic, "flops_per_launch": top["flops_per_launch"],
+                    "ms_per_launch": top["ms_per_launch"], "peak_source": f"bf16_tflops_sustained, {peak_src}"}
     hbm = None
     if "prepare" in kernel_rows:
         nb = sum(flops.prepare_bytes(s.shape[0] * s.shape[1]) for s in specs)
         gbs = nb / (kernel_rows["prepare"]["ms_per_step"] / 1e3) / 1e9
         hbm = {"bound": "hbm", "kernel": "muon_prepare_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": nb}
+
+    # ---- AdamW fallback over the set's AdamW parameters (embeddings, norms)
+    adamw = None
+    if not args.no_adamw and ws.adamw:
+        adamw = run_adamw(args, ws, dev, stream, h, peaks)
 
     # ---- end to end through the public API: pinned host grads in, params out
     e2e = None
@@ -375,12 +392,46 @@ def run_ours(args):
                           "parallelism": f"layer-wise ownership x{world}" if world > 1 else "single GPU"},
                "step_ms": ms_max, "ns_tflops_dense_convention": dense_all / (ms_max / 1e3) / 1e12,
                "ns_frac_of_peak": value / peak, "roofline": roofline, "roofline_hbm": hbm,
-               "kernels": kernel_rows, "gpu_launches": launches, "clocks": clk, "e2e": e2e,
+               "kernels": kernel_rows, "kernel_groups": group_rows, "gpu_launches": launches, "clocks": clk, "e2e": e2e, "adamw": adamw,
                "cpu_baseline": cpu}
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_adamw(args, ws, dev, stream, h, peaks):
+    """Time adamw_step over the weight set's AdamW parameters (bf16 params and
+    grads, fp32 moments), HBM-bound: 22 algorithmic bytes per element."""
+    import torch
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(12345)
+    P = [torch.randn(s.shape, generator=gen, device=dev).mul_(0.02).to(torch.bfloat16) for s in ws.adamw]
+    G = [torch.randn(s.shape, generator=gen, device=dev).mul_(1e-3).to(torch.bfloat16) for s in ws.adamw]
+    Mm = [torch.zeros(s.shape, device=dev) for s in ws.adamw]
+    V = [torch.zeros(s.shape, device=dev) for s in ws.adamw]
+    kw = dict(lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, handle=h)
+    for t in range(1, 4):
+        pkg.adamw_step(P, G, Mm, V, step=t, **kw)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(args.steps, 3)
+    e0.record(stream)
+    for t in range(4, 4 + steps):
+        pkg.adamw_step(P, G, Mm, V, step=t, **kw)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    numel = sum(p.numel() for p in P)
+    nb = flops.adamw_bytes(numel, 2, 2)
+    gbs = nb / (ms / 1e3) / 1e9
+    out = {"kernel": "adamw_kernel", "tensors": len(P), "numel": numel, "ms_per_step": ms, "bytes_per_step": nb,
+           "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}
+    del P, G, Mm, V
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
@@ -429,10 +480,61 @@ def kernel_source_hash():
     return hsh.hexdigest()[:16]
 
 
+def run_wide(args):
+    """Standard vs Gram Newton-Schulz on batches of 64 Gaussian bf16 matrices
+    per (m, n); time per batch and relative error of one sampled matrix
+    against the fp64 oracle (= the SVD closed form)."""
+    import numpy as np
+    import torch
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    from newton_schulz_orthogonalized_muon_gb300 import flops, workloads as wl
+    import oracle
+    torch.cuda.set_device(0)
+    h = pkg.default_handle(0)
+    h.set_workspace_limit(int(args.workspace_gb * (1 << 30)))
+    rows = []
+    for m, n in wl.WIDE_SWEEP:
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(wl.matrix_seed(7, m * 100000 + n))
+        X = torch.randn(wl.WIDE_BATCH, m, n, generator=gen, device="cuda").to(torch.bfloat16)
+        ref = oracle.newton_schulz(X[0].double().cpu().numpy())
+        row = {"m": m, "n": n, "batch": wl.WIDE_BATCH}
+        for method in ("standard", "gram"):
+            Y = X.clone()
+            for _ in range(max(args.warmup, 1)):
+                Y.copy_(X)
+                pkg.muon_orthogonalize(Y, ns_method=method, handle=h)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ms = 0.0
+            for _ in range(args.steps):
+                Y.copy_(X)
+                e0.record()
+                pkg.muon_orthogonalize(Y, ns_method=method, handle=h)
+                e1.record()
+                torch.cuda.synchronize()
+                ms += e0.elapsed_time(e1)
+            ms /= args.steps
+            got = Y[0].double().cpu().numpy()
+            f = flops.ns_flops_standard(m, n) if method == "standard" else flops.ns_flops_gram(m, n)
+            row[method] = {"ms": ms, "tflops_algorithmic": wl.WIDE_BATCH * f / (ms / 1e3) / 1e12,
+                           "rel_err_vs_fp64": float(np.linalg.norm(got - ref) / np.linalg.norm(ref))}
+            del Y
+        row["gram_speedup"] = row["standard"]["ms"] / row["gram"]["ms"]
+        rows.append(row)
+        del X
+        torch.cuda.empty_cache()
+    if h.check() != 0:
+        raise RuntimeError("device error during the sweep")
+    print(json.dumps({"workload": "wide-sweep", "unit": "ms per batch of 64", "rows": rows}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "wide":
+        return run_wide(args)
     return run_ours(args)
 
 

@@ -193,6 +193,14 @@ muon_status_t muon_handle_set_profiling(muon_handle_t h, int32_t enable);
  * clear the records.  Either array may be NULL. */
 muon_status_t muon_handle_profile(muon_handle_t h, double* ms, int64_t* launches, int32_t n_classes);
 
+/* Like muon_handle_profile, but one record per launch: kernel class,
+ * group tag (index of the launch's same-shape group within its call, groups
+ * in ascending (m, n) order; -1 for AdamW) and milliseconds.  Writes at most
+ * `capacity` records into the host arrays, stores the number of records in
+ * *count (which may exceed capacity) and clears the records. */
+muon_status_t muon_handle_profile_records(muon_handle_t h, int32_t* cls, int32_t* tag, float* ms, int32_t capacity,
+                                          int32_t* count);
+
 /* Number of kernels this handle has launched since it was created. */
 muon_status_t muon_handle_launch_count(muon_handle_t h, uint64_t* count);
 

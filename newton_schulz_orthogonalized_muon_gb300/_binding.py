@@ -27,7 +27,7 @@ EXPORTS = ("muon_handle_create", "muon_handle_destroy", "muon_handle_set_workspa
            "muon_handle_set_timeout_ns", "muon_handle_check", "muon_orthogonalize", "muon_step",
            "adamw_step", "muon_selftest_timeout", "muon_status_string", "muon_last_error", "muon_version",
            "muon_handle_set_profiling", "muon_handle_profile", "muon_handle_launch_count",
-           "muon_orthogonalize_noalloc")
+           "muon_orthogonalize_noalloc", "muon_handle_profile_records")
 KERNEL_CLASSES = ("prepare", "norm", "syrk", "poly", "update", "final", "apply", "adamw")
 
 
@@ -81,6 +81,8 @@ def load_library(path: str | None = None):
             "muon_handle_profile": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64), i32]),
             "muon_handle_launch_count": (i32, [vp, ctypes.POINTER(u64)]),
             "muon_orthogonalize_noalloc": (i32, [vp, i32, i64, i64, i32, fptr, vp]),
+            "muon_handle_profile_records": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), fptr, i32,
+                                                  ctypes.POINTER(i32)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -166,6 +168,16 @@ class MuonHandle:
         cnt = (ctypes.c_int64 * n)()
         self._raise(self._lib.muon_handle_profile(self._h, ms, cnt, n), "profile")
         return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+    def profile_records(self, capacity: int = 1 << 16):
+        """[(kernel class, group tag, ms)] per recorded launch, then clear."""
+        cls = (ctypes.c_int32 * capacity)()
+        tag = (ctypes.c_int32 * capacity)()
+        ms = (ctypes.c_float * capacity)()
+        n = ctypes.c_int32()
+        self._raise(self._lib.muon_handle_profile_records(self._h, cls, tag, ms, capacity, ctypes.byref(n)),
+                    "profile_records")
+        return [(KERNEL_CLASSES[cls[i]], int(tag[i]), float(ms[i])) for i in range(min(n.value, capacity))]
 
     def launch_count(self) -> int:
         c = ctypes.c_uint64()

@@ -182,23 +182,76 @@ __global__ void apply_kernel(ApplyParams p) {
 }
 
 // AdamW fallback, one chunk of one tensor per block (multi-tensor launch).
+// Eight elements per thread and step: 16-byte loads/stores of the bf16
+// parameter and gradient and two 16-byte accesses each for m and v; the
+// ragged tail (or a misaligned tensor) goes element by element.
+__device__ __forceinline__ void adamw_one(const AdamParams& p, const AdamTensor& t, long long i) {
+  const float g = load_as_f32(t.g, i, t.gdtype);
+  float m = t.m[i], v = t.v[i];
+  m = fmaf(1.f - p.beta1, g - m, m);
+  v = fmaf(1.f - p.beta2, fmaf(g, g, -v), v);
+  t.m[i] = m;
+  t.v[i] = v;
+  const float u = m / (p.eps + sqrtf(v));
+  store_from_f32(t.p, i, t.pdtype, fmaf(load_as_f32(t.p, i, t.pdtype), p.decay, -p.step_size * u));
+}
+
+__device__ __forceinline__ void load8(const void* base, long long i, int dtype, float* f) {
+  if (dtype == DT_BF16) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(base) + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(h[k]);
+      f[2 * k] = x.x;
+      f[2 * k + 1] = x.y;
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+    const float4 b = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ void store8(void* base, long long i, int dtype, const float* f) {
+  if (dtype == DT_BF16) {
+    uint4 raw;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&raw);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = pack_bf16x2(f[2 * k], f[2 * k + 1]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + i) = raw;
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
 __global__ void __launch_bounds__(256) adamw_kernel(AdamParams p) {
   const AdamChunk ch = p.chunks[blockIdx.x];
   const AdamTensor t = p.tensors[ch.tensor];
   const long long beg = ch.offset;
   const long long end = min(beg + static_cast<long long>(ADAM_CHUNK), t.numel);
+  const bool vec = ((reinterpret_cast<uintptr_t>(t.p) | reinterpret_cast<uintptr_t>(t.g) |
+                     reinterpret_cast<uintptr_t>(t.m) | reinterpret_cast<uintptr_t>(t.v)) & 15) == 0;
+  const long long vend = vec ? beg + ((end - beg) / 8) * 8 : beg;
   const float omb1 = 1.f - p.beta1, omb2 = 1.f - p.beta2;
-  for (long long i = beg + threadIdx.x; i < end; i += blockDim.x) {
-    const float g = load_as_f32(t.g, i, t.gdtype);
-    float m = t.m[i], v = t.v[i];
-    m = fmaf(omb1, g - m, m);
-    v = fmaf(omb2, fmaf(g, g, -v), v);
-    t.m[i] = m;
-    t.v[i] = v;
-    const float u = m / (p.eps + sqrtf(v));
-    const float w = load_as_f32(t.p, i, t.pdtype);
-    store_from_f32(t.p, i, t.pdtype, fmaf(w, p.decay, -p.step_size * u));
+  for (long long i = beg + 8LL * threadIdx.x; i < vend; i += 8LL * blockDim.x) {
+    float g[8], w[8], m[8], v[8];
+    load8(t.g, i, t.gdtype, g);
+    load8(t.p, i, t.pdtype, w);
+    load8(t.m, i, DT_F32, m);
+    load8(t.v, i, DT_F32, v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      m[k] = fmaf(omb1, g[k] - m[k], m[k]);
+      v[k] = fmaf(omb2, fmaf(g[k], g[k], -v[k]), v[k]);
+      w[k] = fmaf(w[k], p.decay, -p.step_size * (m[k] / (p.eps + sqrtf(v[k]))));
+    }
+    store8(t.m, i, DT_F32, m);
+    store8(t.v, i, DT_F32, v);
+    store8(t.p, i, t.pdtype, w);
   }
+  for (long long i = vend + threadIdx.x; i < end; i += blockDim.x) adamw_one(p, t, i);
 }
 
 // Bounded wait on a barrier that nothing completes: must give up within

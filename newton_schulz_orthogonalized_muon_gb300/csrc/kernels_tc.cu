@@ -59,7 +59,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;                    // bf16 elements in one 128-byte swizzle row
-constexpr int TC_THREADS = 192;
+constexpr int EPI_WARPS = 8;                           // two per TMEM lane quadrant
+constexpr int TC_THREADS = 64 + 32 * EPI_WARPS;        // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int BOX_BYTES = 64 * 64 * 2;    // one 64 x 64 bf16 TMA box
 constexpr unsigned long long DRAIN_NS = 1000000000ull;
 
@@ -70,8 +71,20 @@ struct Cfg {
   static constexpr int STAGE_BYTES = AP * A_BYTES + BP * B_BYTES;
   static constexpr int STAGES = (196608 / STAGE_BYTES) < 8 ? (196608 / STAGE_BYTES) : 8;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
+  // epilogue staging for transposed destinations: 16 columns x 128 rows fp32
+  static constexpr int XPOSE_LD = BM + 4;
+  static constexpr int XPOSE_BYTES = 2 * 16 * XPOSE_LD * 4 + 64;   // one 16 x 128 fp32 stage per column half
+  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256 + XPOSE_BYTES;
 };
+
+// Named barriers of the epilogue: id 1 + half (the 128 threads of one column
+// half), id 3 (all 256 epilogue threads).
+__device__ __forceinline__ void epi_half_sync(int half) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
+}
+__device__ __forceinline__ void epi_all_sync() {
+  asm volatile("bar.sync 3, 256;" ::: "memory");
+}
 
 template <int MODE>
 struct ModeTraits {
@@ -214,46 +227,46 @@ __device__ __forceinline__ void epilogue_sym(const NsGemmParams& p, int b, int g
   }
 }
 
-template <int MODE>
-__device__ __forceinline__ void epilogue_update(const NsGemmParams& p, int b, int gr, int gc0, float* v, float s) {
-  const int n = p.n;
-  if (gr >= p.m) return;
-  if (MODE == MODE_G_FINAL) {
-    const OutEntry oe = p.out[b];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] *= s;
-    if (gc0 + 15 < n) {
-      store_out_16(oe, gr, gc0, v);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        if (gc0 + e < n) store_out_scalar(oe, gr, gc0 + e, v[e]);
-    }
-    return;
-  }
-  const size_t rowoff = (static_cast<size_t>(b) * p.m + gr) * p.ldx;
-  float* xrow = p.xf + rowoff;
-  // exact diagonal term: acc + P_rr x - P^_rr x^  (x^ = bf16(x) is the operand copy)
-  const float pd = p.pdiag[static_cast<size_t>(b) * p.m + gr];
-  const float pdb = bf2f(f2bf(pd));
-  if (gc0 + 15 < n) {
+// Sixteen fp32-master values of row gr from column gc0 (0 beyond n).
+__device__ __forceinline__ void load_x16(const NsGemmParams& p, const float* xrow, int gc0, float* x) {
+  if (gc0 + 15 < p.n) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float4 x4 = *reinterpret_cast<const float4*>(xrow + gc0 + 4 * q);
-      const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        v[4 * q + k] = s * fmaf(pd, xs[k], fmaf(-pdb, bf2f(f2bf(xs[k])), v[4 * q + k]));
+      x[4 * q] = x4.x;
+      x[4 * q + 1] = x4.y;
+      x[4 * q + 2] = x4.z;
+      x[4 * q + 3] = x4.w;
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int gc = gc0 + e;
-      const float x = gc < n ? xrow[gc] : 0.f;
-      v[e] = gc < n ? s * fmaf(pd, x, fmaf(-pdb, bf2f(f2bf(x)), v[e])) : 0.f;
-    }
+    for (int e = 0; e < 16; ++e) x[e] = gc0 + e < p.n ? xrow[gc0 + e] : 0.f;
   }
+}
+
+// UPDATE / FINAL value (in place in v) from the accumulator and the fp32
+// master x: s * (acc + P_rr x - P^_rr x^), x^ = bf16(x) being the operand copy
+// whose diagonal term the accumulator holds.  G_FINAL: s * acc.
+template <int MODE>
+__device__ __forceinline__ void update_values(float* v, const float* x, float pd, float pdb, float s) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    if (MODE == MODE_G_FINAL)
+      v[e] *= s;
+    else
+      v[e] = s * fmaf(pd, x[e], fmaf(-pdb, bf2f(f2bf(x[e])), v[e]));
+  }
+}
+
+// Store of UPDATE (new fp32 master + bf16 operand copy) or of a FINAL /
+// G_FINAL tile whose destination is not transposed.
+template <int MODE>
+__device__ __forceinline__ void update_store(const NsGemmParams& p, int b, int gr, int gc0, const float* v) {
+  const int n = p.n;
+  if (gr >= p.m) return;
   if (MODE == MODE_UPDATE) {
+    const size_t rowoff = (static_cast<size_t>(b) * p.m + gr) * p.ldx;
+    float* xrow = p.xf + rowoff;
     __nv_bfloat16* brow = p.xb_out + rowoff;
     if (gc0 + 15 < n) {
 #pragma unroll
@@ -287,6 +300,35 @@ __device__ __forceinline__ void epilogue_update(const NsGemmParams& p, int b, in
   }
 }
 
+// FINAL / G_FINAL tile into a transposed destination (out[c][r] = O[r][c]):
+// the 128 epilogue threads of one column half stage 16 columns of the tile in shared memory
+// and write them back as 16 destination rows of 128 contiguous elements, so
+// every thread issues 16-byte vector accesses to one destination row.
+__device__ __forceinline__ void store_transposed_chunk(const NsGemmParams& p, const OutEntry& oe, int i, int gc0,
+                                                       int row_in_tile, const float* v, float* stage, int ld,
+                                                       int half) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) stage[e * ld + row_in_tile] = v[e];
+  epi_half_sync(half);
+  const int tid = row_in_tile;            // 0..127 over the four epilogue warps
+  const int wr = tid >> 3;                // destination row in this chunk (= NS column gc0 + wr)
+  const int wc = (tid & 7) * 16;          // destination column offset (= NS row within the tile)
+  const int gcol = gc0 + wr;
+  const int grow0 = i * BM + wc;
+  if (gcol < p.n && grow0 < p.m) {
+    float o[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = stage[wr * ld + wc + k];
+    const OutEntry rowwise{oe.ptr, oe.ld, 0, oe.dtype, oe.alpha, oe.beta};
+    if (grow0 + 15 < p.m) {
+      store_out_16(rowwise, gcol, grow0, o);
+    } else {
+      for (int k = 0; k < 16 && grow0 + k < p.m; ++k) store_out_scalar(rowwise, gcol, grow0 + k, o[k]);
+    }
+  }
+  epi_half_sync(half);
+}
+
 // --------------------------------------------------------------- kernel
 template <int MODE, int BN, int AP, int BP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -317,8 +359,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     mbar_init(&tfull[0], 1);
     mbar_init(&tfull[1], 1);
-    mbar_init(&tempty[0], 4);
-    mbar_init(&tempty[1], 4);
+    mbar_init(&tempty[0], EPI_WARPS);
+    mbar_init(&tempty[1], EPI_WARPS);
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -438,15 +480,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue
-    const int quad = warp & 3;                      // TMEM lane quadrant of this warp
+    // warps 2-9: TMEM lane quadrant = warp % 4 (hardware rule), column half =
+    // (warp - 2) / 4; each thread owns one output row of its half.
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
     const int ncols = kUpd ? p.n : p.m;
+    constexpr bool kFinal = (MODE == MODE_FINAL || MODE == MODE_G_FINAL);
+    constexpr bool kNeedX = (MODE == MODE_UPDATE || MODE == MODE_FINAL);
+    // after the 256-byte barrier block; the extra 1024 bytes of the
+    // allocation are the alignment slack of `smem`
+    float* xstage = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + 256) + half * 16 * C::XPOSE_LD;
+    volatile int* wait_ok =
+        reinterpret_cast<volatile int*>(smem + C::STAGES * C::STAGE_BYTES + 256 + 2 * 16 * C::XPOSE_LD * 4);
+    const int cbeg = half * (BN / 2), cend = cbeg + BN / 2;
     int acc = 0;
     uint32_t acc_ph = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int b, i, j;
       decode_tile<MODE>(p, t, b, i, j);
-      if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
+      const bool staged = kFinal && p.out[b].transposed;   // uniform over the epilogue warps
+      bool ok = mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns);
+      if (staged) {
+        // the staged store uses named barriers: all epilogue warps must agree to go on
+        if (lane == 0) wait_ok[warp - 2] = ok ? 1 : 0;
+        epi_all_sync();
+        for (int w = 0; w < EPI_WARPS; ++w) ok = ok && wait_ok[w];
+        epi_all_sync();
+      }
+      if (!ok) {
         if (lane == 0) raise_timeout(abort, p.err);
         break;
       }
@@ -459,17 +521,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (ModeTraits<MODE>::kKn) s = s * s;
       }
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      // UPDATE / FINAL: the fp32 master row and the diagonal of P for this row;
+      // the master values of the next chunk are loaded before the current
+      // chunk is processed, so their latency overlaps the current chunk.
+      const bool rowok = gr < p.m;
+      const float* xrow = kNeedX ? p.xf + (static_cast<size_t>(b) * p.m + (rowok ? gr : 0)) * p.ldx : nullptr;
+      float pd = 0.f, pdb = 0.f;
+      float xcur[16], xnext[16];
+      if (kNeedX) {
+        if (rowok) {
+          pd = p.pdiag[static_cast<size_t>(b) * p.m + gr];
+          pdb = bf2f(f2bf(pd));
+        }
+        const int g0 = j * BN + cbeg;
+        if (rowok && g0 < ncols) load_x16(p, xrow, g0, xcur);
+      }
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
+      for (int c0 = cbeg; c0 < cend; c0 += 16) {
         const int gc0 = j * BN + c0;
         if (gc0 >= ncols) break;
         if (kSym && gc0 + 15 < warp_row0) continue;  // below the diagonal
+        if (kNeedX && rowok && c0 + 16 < cend && gc0 + 16 < ncols) load_x16(p, xrow, gc0 + 16, xnext);
         float v[16];
         tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
-        if (kSym)
+        if (kSym) {
           epilogue_sym<MODE>(p, b, gr, gc0, v, s);
-        else
-          epilogue_update<MODE>(p, b, gr, gc0, v, s);
+        } else {
+          update_values<MODE>(v, xcur, pd, pdb, s);
+          if (staged)
+            store_transposed_chunk(p, p.out[b], i, gc0, row_in_tile, v, xstage, C::XPOSE_LD, half);
+          else
+            update_store<MODE>(p, b, gr, gc0, v);
+        }
+        if (kNeedX) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) xcur[e] = xnext[e];
+        }
       }
       tc_fence_before();
       __syncwarp();

@@ -64,8 +64,10 @@ struct muon_handle_s {
   struct ProfRec {
     cudaEvent_t a, b;
     int cls;
+    int tag;
   };
   bool profiling = false;
+  int prof_tag = -1;            // group index of the launches being issued
   std::vector<ProfRec> prof;
   size_t prof_used = 0;
   uint64_t launches = 0;
@@ -113,6 +115,7 @@ int prof_start(muon_handle_t h, int cls, cudaStream_t s) {
   }
   const int slot = static_cast<int>(h->prof_used++);
   h->prof[slot].cls = cls;
+  h->prof[slot].tag = h->prof_tag;
   cudaEventRecord(h->prof[slot].a, s);
   return slot;
 }
@@ -501,8 +504,10 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   uint8_t* dbase = static_cast<uint8_t*>(dev);
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
 
+  int group_index = 0;
   for (auto& kv : groups) {
     GroupPlan& g = kv.second;
+    h->prof_tag = group_index++;
     const Regions R = regions(g, g.chunk, tc, gram, steps);
     if (gram) {
       muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, ca, cb, cc, tc, mu, nesterov, stream);
@@ -833,6 +838,7 @@ muon_status_t adamw_step(muon_handle_t h, void* const* params, const void* const
   const size_t co = arena_push(arena, chunks.data(), chunks.size());
   void* dev = nullptr;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_arg);
+  h->prof_tag = -1;
   muon_status_t st = upload(h, arena, stream, &dev);
   if (st != MUON_OK) return st;
   const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(step));
@@ -871,6 +877,26 @@ muon_status_t muon_handle_profile(muon_handle_t h, double* ms, int64_t* launches
     if (r.cls < n_classes) {
       if (ms) ms[r.cls] += t;
       if (launches) launches[r.cls] += 1;
+    }
+  }
+  h->prof_used = 0;
+  return MUON_OK;
+}
+
+muon_status_t muon_handle_profile_records(muon_handle_t h, int32_t* cls, int32_t* tag, float* ms, int32_t capacity,
+                                          int32_t* count) {
+  if (h == nullptr || capacity < 0 || count == nullptr) return MUON_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  *count = static_cast<int32_t>(h->prof_used);
+  for (size_t i = 0; i < h->prof_used; ++i) {
+    const auto& r = h->prof[i];
+    MUON_CUDA_TRY(cudaEventSynchronize(r.b), "profile event wait");
+    float t = 0.f;
+    MUON_CUDA_TRY(cudaEventElapsedTime(&t, r.a, r.b), "profile elapsed time");
+    if (static_cast<int64_t>(i) < capacity) {
+      if (cls) cls[i] = r.cls;
+      if (tag) tag[i] = r.tag;
+      if (ms) ms[i] = t;
     }
   }
   h->prof_used = 0;

@@ -21,6 +21,18 @@ def ns_flops_dense(m: int, n: int, steps: int = 5) -> float:
     return float(steps) * (4.0 * m * m * n + 2.0 * m ** 3)
 
 
+def ns_flops_gram(m: int, n: int, steps: int = 5) -> float:
+    """Gram method, algorithmic: R0 = X0 X0^T (one triangle), O = Q X0, and
+    per iteration R^2 plus, from the second iteration, P Q and the two
+    products of P R P (symmetric, one triangle each).  The bf16x3 split of
+    the m x m products (three MMAs each) and the two-plane final product are
+    implementation overhead and not counted."""
+    sym = m * m * (m + 1)
+    if steps == 0:
+        return 0.0
+    return float(m * (m + 1) * n + 2.0 * m * m * n + (steps + 3 * (steps - 1)) * sym)
+
+
 def kernel_flops_standard(m: int, n: int):
     """Algorithmic flops of one matrix in each GEMM kernel class."""
     return {"syrk": float(m * (m + 1) * n), "poly": float(m * m * (m + 1)), "update": 2.0 * m * m * n}

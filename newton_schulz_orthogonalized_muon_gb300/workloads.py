@@ -76,10 +76,17 @@ def gpt2_small(layers: int = 12, d: int = 768) -> WeightSet:
     return ws
 
 
-def llama3_8b(layers: int = 32) -> WeightSet:
+def llama3_8b(layers: int = 32, vocab: int = 128256) -> WeightSet:
     """Llama-3-8B-shaped set (out x in): q, o 4096x4096; k, v 1024x4096;
-    gate, up 14336x4096; down 4096x14336, per layer."""
+    gate, up 14336x4096; down 4096x14336, per layer.  The AdamW list holds
+    what the tagging rule sends to AdamW: embed_tokens and lm_head
+    (vocab x 4096, 2-D but named embed / lm_head) and the RMSNorm vectors."""
     ws = WeightSet("llama3-8b", grad_rank=64, grad_scale=1.0)
+    ws.adamw += [ParamSpec("model.embed_tokens.weight", (vocab, 4096)), ParamSpec("lm_head.weight", (vocab, 4096)),
+                 ParamSpec("model.norm.weight", (4096,))]
+    for i in range(layers):
+        ws.adamw += [ParamSpec(f"layers.{i}.input_layernorm.weight", (4096,)),
+                     ParamSpec(f"layers.{i}.post_attention_layernorm.weight", (4096,))]
     for i in range(layers):
         p = f"layers.{i}."
         ws.muon += [ParamSpec(p + "attn.q_proj.weight", (4096, 4096)),
