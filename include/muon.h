@@ -83,7 +83,11 @@ typedef struct {
 } muon_param_t;
 
 /* Create a handle on CUDA device `device`.  Checks that the device is
- * sm_103 (GB300) and resolves the tensor-map encoder.  *out is NULL on error. */
+ * sm_103 (GB300) and resolves the tensor-map encoder.  *out is NULL on error.
+ * Groups with m a multiple of 256 (or m >= 2048) run the symmetric GEMMs of
+ * the standard bf16 path (X X^T and the polynomial) on two-SM CTA pairs;
+ * setting the environment variable MUON_TC_PAIR=0 before creating the
+ * handle selects the one-SM kernels instead. */
 muon_status_t muon_handle_create(muon_handle_t* out, int device);
 
 /* Destroy a handle: synchronises the device, frees the workspace. NULL is a no-op. */
@@ -106,7 +110,8 @@ muon_status_t muon_handle_check(muon_handle_t h, void* stream);
  * Iteration; "DeepSpeed 集成 Muon 优化器实战", §核心算子).
  *   X       device, [batch][m][n] row-major, dtype; overwritten by O
  *   dtype   MUON_BF16: bf16 tensor-core path (bf16 operands, fp32
- *           accumulation and fp32 master X); MUON_F32: fp32 CUDA-core path
+ *           accumulation, master X kept as bf16 hi + lo planes, about 16
+ *           mantissa bits); MUON_F32: fp32 CUDA-core path
  *   steps   >= 0 (0 returns the normalised input)
  *   coeffs  host pointer to (a, b, c); NULL = (3.4445, -4.7750, 2.0315)
  *   ns_method  muon_ns_method_t

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,8 +20,9 @@ struct PrepParams {
   int nesterov;
   int m;                   // NS rows (after the transpose rule)
   long long ldx;           // row stride of the NS workspace (elements)
-  float* xf;               // fp32 master [batch][m][ldx] or nullptr
-  __nv_bfloat16* xb;       // bf16 operand copy or nullptr (fp32 path)
+  float* xf;               // fp32 copy [batch][m][ldx] or nullptr
+  __nv_bfloat16* xb;       // bf16 operand copy = hi plane of the master, or nullptr (fp32 path)
+  __nv_bfloat16* xlo;      // lo plane of the master, bf16(U - bf16(U)), or nullptr
   float* partials;         // [batch][tiles_per_mat]
   int tiles_per_mat;
 };
@@ -103,9 +105,8 @@ struct NsGemmParams {
   const void* op_b;             // fp32 path, G_PROD: the second factor
   float* pdiag;                 // tensor-core path: fp32 diagonal of P [batch][m]
   long long ldm;
-  // X master / operand copies, row stride ldx
-  float* xf;                    // fp32 master (read and written in place)
-  __nv_bfloat16* xb_out;        // UPDATE: bf16 copy of the new X (tensor-core path)
+  // fp32 path: X operand / result, row stride ldx (the tensor-core path
+  // reaches its master X through tensor maps)
   const float* xf_in;           // fp32 path: X operand (ping-pong partner of xf_out)
   float* xf_out;                // fp32 path: new X
   long long ldx;
@@ -120,11 +121,41 @@ struct NsGemmParams {
 // Operands with two planes (Gram modes) pass their lo-plane maps in a1 / b1.
 cudaError_t launch_ns_gemm_tc(int mode, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
                               const NsGemmParams& p, int grid, cudaStream_t s);
+// UPDATE / FINAL: the master X is hi + lo, hi being the bf16 operand copy.
+// map_xh: hi plane of this iteration (= the B operand), map_xl: lo plane
+// (updated in place), map_xo: hi plane of the next iteration (UPDATE); all
+// bf16 with 32 x 32 boxes from encode_box32.
+cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                     const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
+                                     const NsGemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
                                      const CUtensorMap& map_b0, const CUtensorMap& map_b1, const NsGemmParams& p,
                                      int grid, cudaStream_t s);
-size_t ns_gemm_tc_smem_bytes(int bn);
-int ns_gemm_tc_stages(int bn);
+// CTA-pair variant (tcgen05 cta_group::2, 256 x 256 tiles, standard modes):
+// `pairs` clusters of two CTAs; tiles use 256-row blocks (p.tri / p.mi in
+// 256-row units).
+cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const NsGemmParams& p,
+                               int pairs, cudaStream_t s);
+cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
+                                      const CUtensorMap& b0, const CUtensorMap& b1, const NsGemmParams& p, int pairs,
+                                      cudaStream_t s);
+int ns_gemm_pair_max_pairs();
+
+// 3-D map {cols, rows, batch} (row stride ld elements, matrices rows * ld
+// apart) with a 32 x 32 box: fp32 with 128-byte swizzle (32 floats = one
+// 128-byte row) or bf16 with 64-byte swizzle: the epilogue's blocks of the
+// master X planes.
+inline bool encode_box32(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, bool f32,
+                         uint64_t cols, uint64_t rows, uint64_t batch, uint64_t ld) {
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {cols, rows, batch};
+  cuuint64_t strides[2] = {ld * es, rows * ld * es};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // fp32 SIMT path (CUDA cores).  wide = 0: fp32 m x m matrices; wide = 1:
 // fp64 m x m matrices and accumulation (Gram modes of the fp32 path).

@@ -2,7 +2,8 @@
 //
 //  * muon_prepare_kernel: momentum M <- mu*M + G, Nesterov U = G + mu*M
 //    (else U = M), per-tile partial sums of U^2 for the Frobenius norm, and
-//    the NS working copy of U (fp32 master, optional bf16 MMA operand),
+//    the NS working copy of U (fp32 for the fp32 path; for the tensor-core
+//    path the bf16 MMA operand hi = bf16(U) and the lo plane bf16(U - hi)),
 //    transposed through shared memory when the block has rows > cols.
 //    ("迎接DeepSeek开源周…Muon优化器" (coreui.cn), §代码, Muon step;
 //     "Muon Optimizer and the Distributed Implementation", §Newton-Schulz
@@ -19,6 +20,17 @@
 namespace muon {
 
 constexpr int PT = 64;           // prepare tile: 64 x 64 elements
+
+// bf16 pairs of hi = bf16(u) and lo = bf16(u - hi) for 2 * pairs values
+__device__ __forceinline__ void split_hi_lo(const float* u, uint32_t* hw, uint32_t* lw, int pairs) {
+#pragma unroll
+  for (int k = 0; k < pairs; ++k) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+    const float2 hf = __bfloat1622float2(h2);
+    hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
+    lw[k] = pack_bf16x2(u[2 * k] - hf.x, u[2 * k + 1] - hf.y);
+  }
+}
 constexpr int PREP_THREADS = 256;
 
 __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
@@ -30,48 +42,57 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
   const int tiles_x = (e.cols + PT - 1) / PT;
   const int r0 = (blockIdx.x / tiles_x) * PT;
   const int c0 = (blockIdx.x % tiles_x) * PT;
-  const int tx = threadIdx.x & 15;  // 4-column group
-  const int ty = threadIdx.x >> 4;  // row within a 16-row pass
+  const int tx = threadIdx.x & 7;   // 8-column group
+  const int ty = threadIdx.x >> 3;  // row within a 32-row pass
   const float mu = p.mu;
-  const bool vec = ((e.cols & 3) == 0) && ((e.ld & 3) == 0) &&
+  const bool vec = ((e.cols & 7) == 0) && ((e.ld & 7) == 0) &&
                    ((reinterpret_cast<uintptr_t>(e.g) & 15) == 0) &&
                    (e.mom == nullptr || (reinterpret_cast<uintptr_t>(e.mom) & 15) == 0);
   const long long xbase = static_cast<long long>(b) * p.m * p.ldx;
   float ss = 0.f;
 
 #pragma unroll
-  for (int pass = 0; pass < PT / 16; ++pass) {
-    const int rl = ty + 16 * pass;
+  for (int pass = 0; pass < PT / 32; ++pass) {
+    const int rl = ty + 32 * pass;
     const int r = r0 + rl;
-    const int c = c0 + tx * 4;
-    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    const int c = c0 + tx * 8;
+    float u[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) u[k] = 0.f;
     if (r < e.rows) {
       const long long off = static_cast<long long>(r) * e.ld + c;
-      float g[4], mo[4];
-      if (vec && c + 3 < e.cols) {
+      if (vec && c + 7 < e.cols) {
+        float g[8];
         if (e.gdtype == DT_BF16) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.g) + off);
+          const uint4 raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.g) + off);
           const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-          float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
-          g[0] = f0.x; g[1] = f0.y; g[2] = f1.x; g[3] = f1.y;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(h[k]);
+            g[2 * k] = f.x;
+            g[2 * k + 1] = f.y;
+          }
         } else {
-          const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off);
-          g[0] = f.x; g[1] = f.y; g[2] = f.z; g[3] = f.w;
+          const float4 f0 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off);
+          const float4 f1 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off + 4);
+          g[0] = f0.x; g[1] = f0.y; g[2] = f0.z; g[3] = f0.w; g[4] = f1.x; g[5] = f1.y; g[6] = f1.z; g[7] = f1.w;
         }
         if (e.mom != nullptr) {
-          float4 m4 = *reinterpret_cast<const float4*>(e.mom + off);
-          mo[0] = fmaf(mu, m4.x, g[0]); mo[1] = fmaf(mu, m4.y, g[1]);
-          mo[2] = fmaf(mu, m4.z, g[2]); mo[3] = fmaf(mu, m4.w, g[3]);
+          const float4 m0 = *reinterpret_cast<const float4*>(e.mom + off);
+          const float4 m1 = *reinterpret_cast<const float4*>(e.mom + off + 4);
+          const float mo[8] = {fmaf(mu, m0.x, g[0]), fmaf(mu, m0.y, g[1]), fmaf(mu, m0.z, g[2]), fmaf(mu, m0.w, g[3]),
+                               fmaf(mu, m1.x, g[4]), fmaf(mu, m1.y, g[5]), fmaf(mu, m1.z, g[6]), fmaf(mu, m1.w, g[7])};
           *reinterpret_cast<float4*>(e.mom + off) = make_float4(mo[0], mo[1], mo[2], mo[3]);
+          *reinterpret_cast<float4*>(e.mom + off + 4) = make_float4(mo[4], mo[5], mo[6], mo[7]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) u[k] = p.nesterov ? fmaf(mu, mo[k], g[k]) : mo[k];
+          for (int k = 0; k < 8; ++k) u[k] = p.nesterov ? fmaf(mu, mo[k], g[k]) : mo[k];
         } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) u[k] = g[k];
+          for (int k = 0; k < 8; ++k) u[k] = g[k];
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           if (c + k < e.cols) {
             const float gv = load_as_f32(e.g, off + k, e.gdtype);
             if (e.mom != nullptr) {
@@ -86,52 +107,64 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ss = fmaf(u[k], u[k], ss);
+    for (int k = 0; k < 8; ++k) ss = fmaf(u[k], u[k], ss);
 
     if (!e.transposed) {
       // NS orientation == parameter orientation: X[r][c]
       if (r < e.rows) {
         const long long xo = xbase + static_cast<long long>(r) * p.ldx + c;
-        if (c + 3 < e.cols) {
-          if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+        if (c + 7 < e.cols) {
+          if (p.xf != nullptr) {
+            *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+            *reinterpret_cast<float4*>(p.xf + xo + 4) = make_float4(u[4], u[5], u[6], u[7]);
+          }
           if (p.xb != nullptr) {
-            uint2 packed = make_uint2(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]));
-            *reinterpret_cast<uint2*>(p.xb + xo) = packed;
+            uint32_t hw[4], lw[4];
+            split_hi_lo(u, hw, lw, 4);
+            *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         } else {
-          for (int k = 0; k < 4 && c + k < e.cols; ++k) {
+          for (int k = 0; k < 8 && c + k < e.cols; ++k) {
             if (p.xf != nullptr) p.xf[xo + k] = u[k];
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
+            if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
           }
         }
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tile[rl][tx * 4 + k] = u[k];
+      for (int k = 0; k < 8; ++k) tile[rl][tx * 8 + k] = u[k];
     }
   }
 
   if (e.transposed) {
     __syncthreads();
-    // X[c][r] = U[r][c]: thread (tx, ty) writes X rows c0+ty+16*pass, 4 consecutive r.
+    // X[c][r] = U[r][c]: thread (wx, wy) writes X rows c0+wy+16*pass, 4 consecutive r.
+    const int wx = threadIdx.x & 15, wy = threadIdx.x >> 4;
 #pragma unroll
     for (int pass = 0; pass < PT / 16; ++pass) {
-      const int cl = ty + 16 * pass;
+      const int cl = wy + 16 * pass;
       const int c = c0 + cl;
-      const int r = r0 + tx * 4;
+      const int r = r0 + wx * 4;
       if (c < e.cols) {
         float u[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) u[k] = tile[tx * 4 + k][cl];
+        for (int k = 0; k < 4; ++k) u[k] = tile[wx * 4 + k][cl];
         const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
         if (r + 3 < e.rows) {
           if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
-          if (p.xb != nullptr)
-            *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]));
+          if (p.xb != nullptr) {
+            uint32_t hw[2], lw[2];
+            split_hi_lo(u, hw, lw, 2);
+            *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(hw[0], hw[1]);
+            if (p.xlo != nullptr) *reinterpret_cast<uint2*>(p.xlo + xo) = make_uint2(lw[0], lw[1]);
+          }
         } else {
           for (int k = 0; k < 4 && r + k < e.rows; ++k) {
             if (p.xf != nullptr) p.xf[xo + k] = u[k];
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
+            if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
           }
         }
       }

@@ -12,6 +12,7 @@
 // No host synchronisation happens inside a step.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <string>
@@ -71,6 +72,8 @@ struct muon_handle_s {
   std::vector<ProfRec> prof;
   size_t prof_used = 0;
   uint64_t launches = 0;
+  bool use_pair = true;         // CTA-pair GEMMs for large groups (MUON_TC_PAIR=0 disables)
+  int max_pairs = 0;
 };
 
 namespace {
@@ -212,15 +215,18 @@ bool encode_map(muon_handle_t h, CUtensorMap* map, void* base, uint64_t cols, ui
 }
 
 // Tiles (i, j) of an m x m output that touch the upper triangle, for
-// 128-row by bn-column tiles.
-std::vector<int2> sym_tiles(int m, int bn) {
+// bm-row by bn-column tiles.
+std::vector<int2> sym_tiles(int m, int bn, int bm = 128) {
   std::vector<int2> t;
-  const int mi = static_cast<int>(ceil_div(m, 128)), nj = static_cast<int>(ceil_div(m, bn));
+  const int mi = static_cast<int>(ceil_div(m, bm)), nj = static_cast<int>(ceil_div(m, bn));
   for (int i = 0; i < mi; ++i)
     for (int j = 0; j < nj; ++j)
-      if ((j + 1) * bn - 1 >= i * 128) t.push_back(make_int2(i, j));
+      if ((j + 1) * bn - 1 >= i * bm) t.push_back(make_int2(i, j));
   return t;
 }
+
+// Groups whose m fills 256-row pair tiles well run on the CTA-pair kernels.
+bool pair_group(int m) { return m >= 256 && (m % 256 == 0 || m >= 2048); }
 
 struct GroupPlan {
   int m = 0, n = 0;
@@ -234,6 +240,9 @@ struct GroupPlan {
   int tri_count = 0;
   size_t tri128_off = 0;        // 128 x 128 symmetric tiles (Gram plane products)
   int tri128_count = 0;
+  size_t tri256_off = 0;        // 256 x 256 symmetric tiles (CTA-pair kernels)
+  int tri256_count = 0;
+  bool pair = false;
   std::vector<std::pair<size_t, size_t>> chunk_off;   // (src offset, out offset) per chunk
 };
 
@@ -248,7 +257,7 @@ constexpr int kGramSlots = 6;
 enum { SLOT_R = 0, SLOT_T = 1, SLOT_P0 = 2, SLOT_Q0 = 4 };
 
 struct Regions {
-  size_t xf, xf2, xb0, xb1, symA, symB, pdiag, partials, scale, total;
+  size_t xf, xf2, xlo, xb0, xb1, symA, symB, pdiag, partials, scale, total;
   size_t slot[kGramSlots], slot_lo[kGramSlots];
 };
 
@@ -263,14 +272,18 @@ Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
   const size_t xe = static_cast<size_t>(cap) * g.m * g.ldx;
   const size_t se = static_cast<size_t>(cap) * g.m * g.ldm;
   if (!gram) {
-    r.xf = take(xe * 4);
     if (tc) {
+      // master X = hi + lo: hi is the operand copy (xb0 / xb1 ping-pong), lo
+      // in place; the fp32 copy only when no NS step runs
+      r.xf = (steps == 0) ? take(xe * 4) : 0;
+      r.xlo = (steps == 0) ? 0 : take(xe * 2);
       r.xb0 = take(xe * 2);
       r.xb1 = take(xe * 2);
       r.symA = take(se * 2);
       r.symB = take(se * 2);
       r.pdiag = take(static_cast<size_t>(cap) * g.m * 4);
     } else {
+      r.xf = take(xe * 4);
       r.xf2 = take(xe * 4);
       r.symA = take(se * 4);
       r.symB = take(se * 4);
@@ -369,7 +382,13 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
       r0.scale = scale;
       r0.sym_out = hi[SLOT_R];
       r0.sym_out_lo = lo[SLOT_R];
-      if (tc) {
+      if (tc && g.pair) {
+        r0.tiles_per_mat = g.tri256_count;
+        r0.num_tiles = cnt * g.tri256_count;
+        r0.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
+        const int pairs = std::min(r0.num_tiles, h->max_pairs);
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_G_R0, map_x, map_x, r0, pairs, stream), "gram r0");
+      } else if (tc) {
         r0.tiles_per_mat = g.tri_count;
         r0.num_tiles = cnt * g.tri_count;
         r0.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
@@ -387,7 +406,14 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
       t.sym_in = hi[a];
       t.sym_in_lo = lo[a];
       t.op_b = hi[b];
-      if (tc) {
+      if (tc && g.pair) {
+        t.tiles_per_mat = g.tri256_count;
+        t.num_tiles = cnt * g.tri256_count;
+        t.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
+        const int pairs = std::min(t.num_tiles, h->max_pairs);
+        MUON_LAUNCH(cls, launch_ns_gemm_pair_planes(mode, mhi[a], mlo[a], mhi[b], mlo[b], t, pairs, stream),
+                    "gram product");
+      } else if (tc) {
         MUON_LAUNCH(cls, launch_ns_gemm_tc_planes(mode, 128, mhi[a], mlo[a], mhi[b], mlo[b], t, grid_sym, stream),
                     "gram product");
       } else {
@@ -481,6 +507,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         g.tri128_count = static_cast<int>(t128.size());
         g.tri128_off = arena_push(arena, t128.data(), t128.size());
       }
+      if (h->use_pair && h->max_pairs > 0 && pair_group(g.m)) {
+        std::vector<int2> t256 = sym_tiles(g.m, 256, 256);
+        g.tri256_count = static_cast<int>(t256.size());
+        g.tri256_off = arena_push(arena, t256.data(), t256.size());
+        g.pair = true;
+      }
     }
     for (size_t c0 = 0; c0 < g.members.size(); c0 += g.chunk) {
       const size_t cnt = std::min<size_t>(g.chunk, g.members.size() - c0);
@@ -524,12 +556,16 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     float* partials = reinterpret_cast<float*>(ws + R.partials);
     float* scale = reinterpret_cast<float*>(ws + R.scale);
 
-    CUtensorMap map_x[2], map_A, map_B;
-    if (tc) {
+    __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(ws + R.xlo) : nullptr;
+    CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl;
+    if (tc && steps > 0) {
       if (!encode_map(h, &map_x[0], xb[0], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &map_x[1], xb[1], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &map_A, symA, g.m, g.m, g.chunk, g.ldm) ||
-          !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm))
+          !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_box32(h->encode, &map_xh[0], xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_box32(h->encode, &map_xh[1], xb[1], false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_box32(h->encode, &map_xl, xlo, false, g.n, g.m, g.chunk, g.ldx))
         return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
     const int mi = static_cast<int>(ceil_div(g.m, 128));
@@ -546,8 +582,9 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
       pp.nesterov = nesterov;
       pp.m = g.m;
       pp.ldx = g.ldx;
-      pp.xf = xf;
+      pp.xf = (tc && steps > 0) ? nullptr : xf;
       pp.xb = xb[0];
+      pp.xlo = xlo;
       pp.partials = partials;
       pp.tiles_per_mat = g.prep_tiles;
       MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");
@@ -575,7 +612,31 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         p.err = h->err;
         p.timeout_ns = h->timeout_ns;
         p.pdiag = pdiag;
-        if (tc) {
+        if (tc && g.pair) {
+          // SYRK and POLY on CTA pairs (256 x 256 tiles); UPDATE / FINAL on
+          // one-CTA kernels, whose heavier epilogue gains nothing from pairing
+          NsGemmParams q = p;
+          q.tiles_per_mat = g.tri256_count;
+          q.num_tiles = cnt * g.tri256_count;
+          q.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
+          q.sym_out = symA;
+          const int pairs = std::min(q.num_tiles, h->max_pairs);
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], q, pairs, stream),
+                      "syrk launch");
+          q.scale = nullptr;
+          q.sym_in = symA;
+          q.sym_out = symB;
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, q, pairs, stream), "poly launch");
+          NsGemmParams u = p;
+          u.mi = mi;
+          u.tiles_per_mat = mi * nj;
+          u.num_tiles = cnt * mi * nj;
+          const int grid = std::min(u.num_tiles, h->num_sms);
+          MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                      launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1],
+                                               map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
+                      "update launch");
+        } else if (tc) {
           // SYRK: A = s^2 X X^T
           NsGemmParams q = p;
           q.tiles_per_mat = g.tri_count;
@@ -595,11 +656,10 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           u.mi = mi;
           u.tiles_per_mat = mi * nj;
           u.num_tiles = cnt * mi * nj;
-          u.xf = xf;
-          u.xb_out = xb[(it + 1) & 1];
           grid = std::min(u.num_tiles, h->num_sms);
           MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                      launch_ns_gemm_tc(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1], u, grid, stream),
+                      launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1],
+                                               map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
                       "update launch");
         } else {
           float* xin = (it & 1) ? xf2 : xf;
@@ -673,6 +733,9 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
     return MUON_ERR_UNSUPPORTED;
   }
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  const char* pair_env = std::getenv("MUON_TC_PAIR");
+  h->use_pair = !(pair_env != nullptr && pair_env[0] == '0');
+  h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
   if (cudaMalloc(&h->err, sizeof(unsigned)) != cudaSuccess || cudaMemset(h->err, 0, sizeof(unsigned)) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) {
     cudaGetLastError();

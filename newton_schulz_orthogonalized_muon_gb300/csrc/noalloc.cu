@@ -137,7 +137,10 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
   OutEntry* out_d = reinterpret_cast<OutEntry*>(take(sizeof(OutEntry)));
   int2* tri_d = reinterpret_cast<int2*>(take(sizeof(int2) * kMaxTri));
   const size_t xe = static_cast<size_t>(M) * ldx, se = static_cast<size_t>(M) * ldm;
+  // fp32 copy of X0 (fp32 path, or no NS step); the tensor-core path's lo
+  // plane of the master X = hi + lo shares its space
   float* xf = reinterpret_cast<float*>(take(xe * 4));
+  __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(xf) : nullptr;
   float* xf2 = tc ? nullptr : reinterpret_cast<float*>(take(xe * 4));
   __nv_bfloat16* xb0 = tc ? reinterpret_cast<__nv_bfloat16*>(take(xe * 2)) : nullptr;
   __nv_bfloat16* xb1 = tc ? reinterpret_cast<__nv_bfloat16*>(take(xe * 2)) : nullptr;
@@ -164,8 +167,9 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
   pp.src = src_d;
   pp.m = M;
   pp.ldx = ldx;
-  pp.xf = xf;
+  pp.xf = (tc && steps > 0) ? nullptr : xf;
   pp.xb = xb0;
+  pp.xlo = xlo;
   pp.partials = partials;
   pp.tiles_per_mat = prep_tiles;
   if (launch_prepare(pp, 1, prep_tiles, stream) != cudaSuccess) return MUON_ERR_CUDA;
@@ -174,9 +178,12 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
     ApplyParams ap{out_d, scale, xf, ldx, M, N};
     return launch_apply(ap, 1, stream) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
   }
-  CUtensorMap map_x[2], map_A, map_B;
+  CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl;
   if (tc && !(encode_map(S->encode, &map_x[0], xb0, N, M, ldx) && encode_map(S->encode, &map_x[1], xb1, N, M, ldx) &&
-              encode_map(S->encode, &map_A, symA, M, M, ldm) && encode_map(S->encode, &map_B, symB, M, M, ldm)))
+              encode_map(S->encode, &map_A, symA, M, M, ldm) && encode_map(S->encode, &map_B, symB, M, M, ldm) &&
+              encode_box32(S->encode, &map_xh[0], xb0, false, N, M, 1, ldx) &&
+              encode_box32(S->encode, &map_xh[1], xb1, false, N, M, 1, ldx) &&
+              encode_box32(S->encode, &map_xl, xlo, false, N, M, 1, ldx)))
     return MUON_ERR_CUDA;
   const int mi = (M + 127) / 128, nj = (N + bn_upd - 1) / bn_upd;
   for (int it = 0; it < steps; ++it) {
@@ -214,10 +221,9 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
       u.mi = mi;
       u.tiles_per_mat = mi * nj;
       u.num_tiles = mi * nj;
-      u.xf = xf;
-      u.xb_out = (it & 1) ? xb0 : xb1;
       const int gu = u.num_tiles < S->num_sms ? u.num_tiles : S->num_sms;
-      e = launch_ns_gemm_tc(last ? MODE_FINAL : MODE_UPDATE, bn_upd, map_B, map_x[it & 1], u, gu, stream);
+      e = launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, bn_upd, map_B, map_x[it & 1], map_xh[it & 1],
+                                   map_xl, map_xh[(it + 1) & 1], u, gu, stream);
     } else {
       float* xin = (it & 1) ? xf2 : xf;
       float* xout = (it & 1) ? xf : xf2;

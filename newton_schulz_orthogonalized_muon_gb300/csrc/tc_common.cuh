@@ -1,0 +1,473 @@
+// Device code shared by the one-CTA (kernels_tc.cu) and CTA-pair
+// (kernels_tc2.cu) tensor-core Newton-Schulz GEMMs: tile constants, bounded
+// warp-wide waits, tile decoding and the epilogues of every mode.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace muon {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                    // bf16 elements in one 128-byte swizzle row
+constexpr int EPI_WARPS = 8;                           // two per TMEM lane quadrant
+constexpr int TC_THREADS = 64 + 32 * EPI_WARPS;        // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int BOX_BYTES = 64 * 64 * 2;    // one 64 x 64 bf16 TMA box
+constexpr int MAX_DYN_SMEM = 232448;      // 227 KB opt-in dynamic shared memory per CTA
+constexpr unsigned long long DRAIN_NS = 1000000000ull;
+
+
+template <int MODE>
+struct ModeTraits {
+  static constexpr bool kSym = (MODE == MODE_SYRK || MODE == MODE_POLY || MODE == MODE_G_R0 ||
+                                MODE == MODE_G_P || MODE == MODE_G_PROD);
+  static constexpr bool kMN = (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_G_FINAL);
+  static constexpr bool kKn = (MODE == MODE_SYRK || MODE == MODE_G_R0);   // K = n (else K = m)
+  static constexpr bool kPlanesOut = (MODE == MODE_G_R0 || MODE == MODE_G_P || MODE == MODE_G_PROD);
+};
+
+// Warp-collective bounded wait: every lane polls, the warp leaves together.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t timeout_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    const bool ok = mbar_try_wait(a, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((it & 31u) == 31u) {
+      const bool give_up = (*abort != 0) || (globaltimer_ns() - t0 > timeout_ns);
+      if (__any_sync(0xffffffffu, give_up)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void raise_timeout(volatile int* abort, unsigned* err) {
+  *abort = 1;
+  atomicOr(err, ERRBIT_TIMEOUT);
+}
+
+template <int MODE>
+__device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b, int& i, int& j) {
+  b = t / p.tiles_per_mat;
+  const int l = t - b * p.tiles_per_mat;
+  if (ModeTraits<MODE>::kSym) {
+    const int2 ij = p.tri[l];
+    i = ij.x;
+    j = ij.y;
+  } else {
+    j = l / p.mi;          // column-block major: neighbouring tiles share X's column block
+    i = l - j * p.mi;
+  }
+}
+
+// ------------------------------------------------------------ epilogues
+// v[16]: accumulator values of row gr, columns gc0 .. gc0+15.
+template <int MODE>
+__device__ __forceinline__ void epilogue_sym(const NsGemmParams& p, int b, int gr, int gc0, float* v, float s) {
+  const int m = p.m;
+  if (gr >= m) return;
+  const size_t mat = static_cast<size_t>(b) * m;
+  if (MODE == MODE_SYRK || MODE == MODE_G_R0) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] *= s;
+  } else if (MODE == MODE_POLY || MODE == MODE_G_P) {
+    // v = b * A + c * acc (G_P: A = R = hi + lo planes, plus a on the diagonal)
+    const __nv_bfloat16* ain = reinterpret_cast<const __nv_bfloat16*>(p.sym_in) + (mat + gr) * p.ldm;
+    const __nv_bfloat16* alo =
+        MODE == MODE_G_P ? reinterpret_cast<const __nv_bfloat16*>(p.sym_in_lo) + (mat + gr) * p.ldm : nullptr;
+    float a[16];
+    if (gc0 + 15 < m) {
+      uint4 raw[2];
+      raw[0] = *reinterpret_cast<const uint4*>(ain + gc0);
+      raw[1] = *reinterpret_cast<const uint4*>(ain + gc0 + 8);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(raw);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        a[2 * e] = f.x;
+        a[2 * e + 1] = f.y;
+      }
+      if (MODE == MODE_G_P) {
+        raw[0] = *reinterpret_cast<const uint4*>(alo + gc0);
+        raw[1] = *reinterpret_cast<const uint4*>(alo + gc0 + 8);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 f = __bfloat1622float2(h[e]);
+          a[2 * e] += f.x;
+          a[2 * e + 1] += f.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int gc = gc0 + e;
+        a[e] = gc < m ? bf2f(ain[gc]) + (MODE == MODE_G_P ? bf2f(alo[gc]) : 0.f) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      v[e] = fmaf(p.cb, a[e], p.cc * v[e]);
+      if (gc0 + e == gr) {
+        v[e] += p.ca;
+        if (MODE == MODE_POLY) p.pdiag[mat + gr] = v[e];
+      }
+    }
+  }
+  constexpr bool kPlanes = ModeTraits<MODE>::kPlanesOut;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.sym_out);
+  __nv_bfloat16* outlo = kPlanes ? reinterpret_cast<__nv_bfloat16*>(p.sym_out_lo) : nullptr;
+  float lo[16];
+  if (kPlanes) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) lo[e] = v[e] - bf2f(f2bf(v[e]));
+  }
+  __nv_bfloat16* row = out + (mat + gr) * p.ldm;
+  __nv_bfloat16* rowlo = kPlanes ? outlo + (mat + gr) * p.ldm : nullptr;
+  if (gc0 >= gr && gc0 + 15 < m) {
+    uint4 pk[2];
+    uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    *reinterpret_cast<uint4*>(row + gc0) = pk[0];
+    *reinterpret_cast<uint4*>(row + gc0 + 8) = pk[1];
+    if (kPlanes) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(lo[2 * e], lo[2 * e + 1]);
+      *reinterpret_cast<uint4*>(rowlo + gc0) = pk[0];
+      *reinterpret_cast<uint4*>(rowlo + gc0 + 8) = pk[1];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int gc = gc0 + e;
+      if (gc >= gr && gc < m) {
+        row[gc] = f2bf(v[e]);
+        if (kPlanes) rowlo[gc] = f2bf(lo[e]);
+      }
+    }
+  }
+  // mirror below the diagonal: lanes hold consecutive rows, so each store
+  // of the warp covers 32 consecutive elements of row gc.
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int gc = gc0 + e;
+    if (gc > gr && gc < m) {
+      out[(mat + gc) * p.ldm + gr] = f2bf(v[e]);
+      if (kPlanes) outlo[(mat + gc) * p.ldm + gr] = f2bf(lo[e]);
+    }
+  }
+}
+
+// ------------------------------------------- UPDATE / FINAL / G_FINAL epilogue
+// The master X of the tensor-core path is held as two bf16 planes, X = hi +
+// lo: hi = bf16(X) is the MMA operand copy itself, lo = bf16(X - hi) keeps
+// about 16 mantissa bits in all.  Each epilogue warp owns 32 rows (its TMEM
+// lane quadrant) and half of the tile's columns, which it walks in 32 x 32
+// blocks.  Per warp, in shared memory, SLOTS slots of 4 KB:
+//   UPDATE / FINAL: [hi 32 x 32 bf16 | lo 32 x 32 bf16], 64-byte rows with
+//   64-byte swizzle, loaded by TMA up to two blocks ahead (across tile
+//   boundaries) so the loads overlap the main loop.  UPDATE writes the new
+//   hi and lo back in place and stores both with TMA (hi to the other
+//   operand buffer, lo in place).
+//   FINAL / G_FINAL: after the block's inputs are in registers the slot is
+//   reused as 32 x 32 fp32 (128-byte rows, 128-byte swizzle) holding the
+//   result in destination orientation (transposed when the destination is
+//   out[c][r]), then written out as 16-byte row segments, eight lanes per
+//   destination row.
+// With the swizzles, one lane per row accessing 16-byte chunks of its row,
+// and eight lanes covering one row, are free of bank conflicts.
+template <int MODE>
+struct EpiLayout {
+  static constexpr bool kMN = ModeTraits<MODE>::kMN;
+  static constexpr bool kLoadX = (MODE == MODE_UPDATE || MODE == MODE_FINAL);
+  static constexpr int SLOTS = kLoadX ? 2 : 1;
+  static constexpr int SLOT_BYTES = 4096;
+  static constexpr int LO_OFF = 2048;                 // lo plane within a slot
+  static constexpr int WARP_BYTES = SLOTS * SLOT_BYTES;   // a multiple of 1024
+  static constexpr int BYTES = kMN ? EPI_WARPS * WARP_BYTES : 0;
+};
+
+// byte offset of 16-byte chunk q of row r: 128-byte rows, 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128_off(int r, int q) {
+  return static_cast<uint32_t>(r * 128 + ((q ^ (r & 7)) << 4));
+}
+// byte offset of 16-byte chunk q of row r: 64-byte rows, 64-byte swizzle
+__device__ __forceinline__ uint32_t sw64_off(int r, int q) {
+  return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& raw, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __bfloat1622float2(h[k]);
+    f[2 * k] = t.x;
+    f[2 * k + 1] = t.y;
+  }
+}
+
+// out[r][c0 .. c0+3] = alpha * out + beta * o (not transposed, r < m, c0 < n)
+__device__ __forceinline__ void store_out_4(const OutEntry& e, int r, int c0, int n, float4 o, float4 old) {
+  const long long idx = static_cast<long long>(r) * e.ld + c0;
+  const float ov[4] = {o.x, o.y, o.z, o.w};
+  const float wv[4] = {old.x, old.y, old.z, old.w};
+  float v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = fmaf(e.alpha, wv[k], e.beta * ov[k]);
+  if (c0 + 3 < n) {
+    if (e.dtype == DT_BF16) {
+      __nv_bfloat16* q = reinterpret_cast<__nv_bfloat16*>(e.ptr) + idx;
+      if ((reinterpret_cast<uintptr_t>(q) & 7) == 0) {
+        *reinterpret_cast<uint2*>(q) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        return;
+      }
+    } else {
+      float* q = reinterpret_cast<float*>(e.ptr) + idx;
+      if ((reinterpret_cast<uintptr_t>(q) & 15) == 0) {
+        *reinterpret_cast<float4*>(q) = make_float4(v[0], v[1], v[2], v[3]);
+        return;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (c0 + k < n) store_from_f32(e.ptr, idx + k, e.dtype, v[k]);
+}
+
+// the old destination values matching store_out_4 (zeros when alpha == 0)
+__device__ __forceinline__ float4 load_out_4(const OutEntry& e, int r, int c0, int n) {
+  float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (e.alpha == 0.f) return w;
+  const long long idx = static_cast<long long>(r) * e.ld + c0;
+  if (c0 + 3 < n) {
+    if (e.dtype == DT_BF16) {
+      const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(e.ptr) + idx;
+      if ((reinterpret_cast<uintptr_t>(q) & 7) == 0) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(q);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+      }
+    } else {
+      const float* q = reinterpret_cast<const float*>(e.ptr) + idx;
+      if ((reinterpret_cast<uintptr_t>(q) & 15) == 0) return *reinterpret_cast<const float4*>(q);
+    }
+  }
+  float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    if (c0 + k < n) t[k] = load_as_f32(e.ptr, idx + k, e.dtype);
+  return make_float4(t[0], t[1], t[2], t[3]);
+}
+
+// The whole tile loop of one epilogue warp for the UPDATE / FINAL / G_FINAL
+// modes (tiles blockIdx.x, blockIdx.x + gridDim.x, ... of the one-CTA
+// kernel).  wbuf: this warp's WARP_BYTES of shared memory (1024-aligned);
+// xfull: this warp's SLOTS barriers.  Maps (3-D, 32 x 32 bf16 boxes, 64-byte
+// swizzle): map_xh = hi plane read this iteration (the B operand), map_xl =
+// lo plane (read and written in place), map_xo = hi plane written for the
+// next iteration.  On return (also after a timeout, already recorded) the
+// warp's loads have landed and its stores have completed.
+template <int MODE, int BN>
+__device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtensorMap* map_xh,
+                                            const CUtensorMap* map_xl, const CUtensorMap* map_xo, uint8_t* wbuf,
+                                            uint64_t* xfull, uint64_t* tfull, uint64_t* tempty, volatile int* abort,
+                                            uint32_t tmem_base, int warp, int lane) {
+  using L = EpiLayout<MODE>;
+  constexpr int NB = BN / 64;                          // 32-column blocks per warp per tile
+  const int quad = warp & 3;
+  const int cbeg = ((warp - 2) >> 2) * (BN / 2);
+  const uint32_t wsm = smem_u32(wbuf);
+
+  // ---- input prefetch, in this warp's block order, at most SLOTS blocks ahead
+  int pf_t = blockIdx.x, pf_blk = 0;
+  uint32_t issued = 0, done = 0;
+  auto issue_next = [&]() {
+    while (pf_t < p.num_tiles) {
+      int b, i, j;
+      decode_tile<MODE>(p, pf_t, b, i, j);
+      const int g0 = j * BN + cbeg;
+      const int nb = g0 >= p.n ? 0 : min(NB, (p.n - g0 + 31) >> 5);
+      if (pf_blk < nb) {
+        if (lane == 0) {
+          const int slot = static_cast<int>(issued & 1u);
+          const uint32_t dst = wsm + slot * L::SLOT_BYTES;
+          const int x = g0 + 32 * pf_blk, y = i * BM + quad * 32;
+          mbar_arrive_expect_tx(&xfull[slot], L::SLOT_BYTES);
+          tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
+          tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
+        }
+        ++issued;
+        ++pf_blk;
+        return;
+      }
+      pf_t += gridDim.x;
+      pf_blk = 0;
+    }
+  };
+  if (L::kLoadX) {
+    issue_next();
+    issue_next();
+  }
+
+  bool ok = true;
+  int acc = 0;
+  uint32_t acc_ph = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    int b, i, j;
+    decode_tile<MODE>(p, t, b, i, j);
+    if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
+      if (lane == 0) raise_timeout(abort, p.err);
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const int row0 = i * BM + quad * 32;
+    const int gr = row0 + lane;
+    const float s = p.scale != nullptr ? p.scale[b] : 1.f;
+    // exact diagonal term: acc + P_rr x - P^_rr hi, hi being the operand copy
+    // whose product with the rounded diagonal P^_rr the accumulator holds
+    float pd = 0.f, pdb = 0.f;
+    if (L::kLoadX && gr < p.m) {
+      pd = p.pdiag[static_cast<size_t>(b) * p.m + gr];
+      pdb = bf2f(f2bf(pd));
+    }
+    OutEntry oe{};
+    if (MODE != MODE_UPDATE) oe = p.out[b];
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + cbeg);
+    const int g0 = j * BN + cbeg;
+    const int nb = g0 >= p.n ? 0 : min(NB, (p.n - g0 + 31) >> 5);
+#pragma unroll 1
+    for (int k = 0; k < nb; ++k) {
+      const int gcb = g0 + 32 * k;
+      const int slot = L::kLoadX ? static_cast<int>(done & 1u) : 0;
+      uint8_t* sbuf = wbuf + slot * L::SLOT_BYTES;
+      if (L::kLoadX && !mbar_wait_warp(&xfull[slot], (done >> 1) & 1u, abort, p.timeout_ns)) {
+        if (lane == 0) raise_timeout(abort, p.err);
+        ok = false;
+        break;
+      }
+      if constexpr (MODE == MODE_UPDATE) {
+#pragma unroll
+        for (int h = 0; h < 32; h += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(32 * k + h), v);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint4* ph = reinterpret_cast<uint4*>(sbuf + sw64_off(lane, (h >> 3) + q));
+            uint4* pl = reinterpret_cast<uint4*>(sbuf + L::LO_OFF + sw64_off(lane, (h >> 3) + q));
+            float hi[8], lo[8], o[8];
+            unpack8(*ph, hi);
+            unpack8(*pl, lo);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o[e] = s * fmaf(pd, hi[e] + lo[e], fmaf(-pdb, hi[e], v[8 * q + e]));
+            uint4 nh, nl;
+            uint32_t* wh = reinterpret_cast<uint32_t*>(&nh);
+            uint32_t* wl = reinterpret_cast<uint32_t*>(&nl);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+              const float2 hf = __bfloat1622float2(h2);
+              wh[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              wl[e] = pack_bf16x2(o[2 * e] - hf.x, o[2 * e + 1] - hf.y);
+            }
+            *ph = nh;
+            *pl = nl;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.m) {   // rows past m: nothing to store
+          const uint32_t src = wsm + slot * L::SLOT_BYTES;
+          tma_store_3d(map_xo, src, gcb, row0, b);
+          tma_store_3d(map_xl, src + L::LO_OFF, gcb, row0, b);
+          bulk_commit_group();
+          bulk_wait_read_all();          // the slot may be refilled
+        }
+        __syncwarp();
+      } else {
+        // FINAL / G_FINAL: the block's correction terms into registers, then
+        // the slot holds the fp32 result in destination orientation
+        float corr[32];
+        if (MODE == MODE_FINAL) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float hi[8], lo[8];
+            unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)), hi);
+            unpack8(*reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)), lo);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd - pdb, hi[e], pd * lo[e]);
+          }
+          __syncwarp();                  // every lane holds its row: the slot may be overwritten
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) corr[e] = 0.f;
+        }
+        const bool tr = oe.transposed != 0;
+#pragma unroll
+        for (int h = 0; h < 32; h += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(32 * k + h), v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = s * (v[e] + corr[h + e]);
+          if (tr) {
+            // slot row = block column c, position = block row (this lane)
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              *reinterpret_cast<float*>(sbuf + sw128_off(h + e, lane >> 2) + 4 * (lane & 3)) = v[e];
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<float4*>(sbuf + sw128_off(lane, (h >> 2) + q)) =
+                  make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
+        }
+        __syncwarp();                    // the block's results are in the slot
+        // destination rows of this block: drow0 + (0..31), limit dlim; columns
+        // dcol0 + (0..31), limit dcols
+        const int drow0 = tr ? gcb : row0, dlim = tr ? p.n : p.m;
+        const int dcol0 = tr ? row0 : gcb, dcols = tr ? p.m : p.n;
+        const OutEntry rowwise{oe.ptr, oe.ld, 0, oe.dtype, oe.alpha, oe.beta};
+        const int rq = lane >> 3, q = lane & 7;
+        const bool colok = dcol0 + 4 * q < dcols;
+        float4 w[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = 4 * it + rq;
+          w[it] = (drow0 + r < dlim && colok) ? load_out_4(rowwise, drow0 + r, dcol0 + 4 * q, dcols)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = 4 * it + rq;
+          if (drow0 + r < dlim && colok)
+            store_out_4(rowwise, drow0 + r, dcol0 + 4 * q, dcols,
+                        *reinterpret_cast<const float4*>(sbuf + sw128_off(r, q)), w[it]);
+        }
+        fence_proxy_async_smem();        // generic accesses of the slot before its next TMA fill
+        __syncwarp();
+      }
+      ++done;
+      if (L::kLoadX) issue_next();
+    }
+    if (!ok) break;
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[acc]);
+    acc ^= 1;
+    if (acc == 0) acc_ph ^= 1u;
+  }
+  // loads still in flight land before the CTA's shared memory goes away;
+  // stores complete
+  if (lane == 0) {
+    for (uint32_t u = done; u < issued; ++u)
+      mbar_wait_bounded(&xfull[u & 1u], (u >> 1) & 1u, nullptr, DRAIN_NS);
+    if (MODE == MODE_UPDATE) bulk_wait_all();
+  }
+  __syncwarp();
+}
+
+}  // namespace tc
+}  // namespace muon

@@ -49,9 +49,10 @@ def set_flops(specs, steps: int = 5):
 
 
 def prepare_bytes(numel: int, grad_bytes: int = 2) -> float:
-    """HBM bytes of the momentum/Nesterov/norm/cast pass: read G, read and
-    write M (fp32), write the bf16 operand copy and the fp32 master copy."""
-    return float(numel) * (grad_bytes + 4 + 4 + 2 + 4)
+    """HBM bytes of the momentum/Nesterov/norm/cast pass of the tensor-core
+    path: read G, read and write M (fp32), write the two bf16 planes of the
+    master X (hi = the MMA operand copy, lo = the residual)."""
+    return float(numel) * (grad_bytes + 4 + 4 + 2 + 2)
 
 
 def adamw_bytes(numel: int, param_bytes: int = 2, grad_bytes: int = 2) -> float:
