@@ -355,7 +355,9 @@ def run_ours(args):
                     traffic = entry.get("bytes_per_launch")
             except Exception:
                 traffic = None
-        roofline = {"bound": "tensor", "kernel": f"ns_gemm_tc_kernel<{top['kernel']}> on the {top['group']} group "
+        m_top = int(top["group"].split("x")[0])
+        kname = "ns_gemm_pair_kernel" if uses_pairs(m_top) else "ns_gemm_tc_kernel"
+        roofline = {"bound": "tensor", "kernel": f"{kname}<{top['kernel'].upper()}> on the {top['group']} group "
                                                   f"({top['matrices']} matrices)",
                     "achieved": top["tflops"], "peak": peak, "unit": "TFLOP/s", "frac": top["tflops"] / peak,
                     "traffic": traffic, "flops_per_launch": top["flops_per_launch"],
@@ -531,6 +533,20 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     return {"value": alg_all / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "mode": "pipelined (copies overlapped with compute)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12}
+
+
+def uses_pairs(m):
+    """The library's rule for which groups run on the CTA-pair kernels (m a
+    multiple of 256, or m >= MUON_TC_PAIR_MIN_M, 2048 by default; none with
+    MUON_TC_PAIR=0); standard method."""
+    env = os.environ.get("MUON_TC_PAIR")
+    if env == "0":
+        return False
+    try:
+        min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "2048"))
+    except ValueError:
+        min_m = 2048
+    return m >= 256 and (m % 256 == 0 or m >= min_m)
 
 
 def kernel_source_hash():

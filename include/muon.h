@@ -84,10 +84,12 @@ typedef struct {
 
 /* Create a handle on CUDA device `device`.  Checks that the device is
  * sm_103 (GB300) and resolves the tensor-map encoder.  *out is NULL on error.
- * Groups with m a multiple of 256 (or m >= 2048) run the symmetric GEMMs of
- * the standard bf16 path (X X^T and the polynomial) on two-SM CTA pairs;
- * setting the environment variable MUON_TC_PAIR=0 before creating the
- * handle selects the one-SM kernels instead. */
+ * Groups with m a multiple of 256 (or m >= 2048) run the GEMMs of the bf16
+ * path on two-SM CTA pairs (256 x 256 tiles); the environment variable
+ * MUON_TC_PAIR, read when the handle is created, selects the one-SM kernels
+ * instead ("0") or pairs for the symmetric products only ("sym");
+ * MUON_TC_PAIR_MIN_M (default 2048) is the m from which groups whose m is
+ * not a multiple of 256 run on pairs too. */
 muon_status_t muon_handle_create(muon_handle_t* out, int device);
 
 /* Destroy a handle: synchronises the device, frees the workspace. NULL is a no-op. */
@@ -134,6 +136,44 @@ muon_status_t muon_orthogonalize(muon_handle_t h, void* X, int32_t dtype, int64_
 muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_params, float lr, float wd,
                         float mu, int32_t nesterov, int32_t ns_method, int32_t ns_steps, const float* coeffs,
                         float update_rms, int32_t ns_dtype, void* stream);
+
+/* Update scale of muon_step_ex:
+ *   MUON_SCALE_RMS  update_rms * sqrt(scale_dim), scale_dim = max(A, B) by
+ *                   default: matches the update RMS to AdamW's
+ *                   ("迎接DeepSeek开源周…Muon优化器", §2 参数更新尺度调整, 0.2);
+ *                   DeepSeek-V4's sqrt(max(n, m)) * gamma is this mode with
+ *                   update_rms = gamma ("Muon Optimizer and the Distributed
+ *                   Implementation", §Variation).
+ *   MUON_SCALE_MUP  sqrt(d_out / d_in) = sqrt(rows / cols) of the parameter
+ *                   as stored (out x in): the dual of the gradient under the
+ *                   RMS -> RMS operator norm has spectral norm
+ *                   sqrt(d_out / d_in) (same page and section, the muP form).
+ * In both modes the update is further multiplied by extra_scale (MindSpeed's
+ * "--muon-extra-scale-factor", "Muon 优化器" feature doc, parameter table). */
+typedef enum { MUON_SCALE_RMS = 0, MUON_SCALE_MUP = 1 } muon_scale_mode_t;
+
+typedef struct {
+  float lr;                /* learning rate */
+  float wd;                /* decoupled weight decay: W <- W * (1 - lr * wd) first */
+  float mu;                /* momentum */
+  int32_t nesterov;        /* 1: U = G + mu * M_new; 0: U = M_new */
+  int32_t ns_method;       /* muon_ns_method_t */
+  int32_t ns_steps;        /* 0 .. 100 */
+  const float* coeffs;     /* host (a, b, c) or NULL for (3.4445, -4.7750, 2.0315) */
+  int32_t ns_dtype;        /* MUON_BF16: tensor-core path; MUON_F32: fp32 path */
+  int32_t scale_mode;      /* muon_scale_mode_t */
+  float update_rms;        /* MUON_SCALE_RMS factor (0.2); ignored by MUON_SCALE_MUP */
+  float extra_scale;       /* multiplies the update in every mode (1.0) */
+} muon_step_options_t;
+
+/* muon_step with the update scale chosen by opts (host struct, read during
+ * the call only):
+ *   W <- W*(1 - lr*wd) - lr * extra_scale * scale(mode) * O
+ * Everything else as muon_step, which equals muon_step_ex with
+ * MUON_SCALE_RMS and extra_scale = 1.  Invalid mode or non-finite factors:
+ * MUON_ERR_INVALID_ARG before anything is enqueued. */
+muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t n_params,
+                           const muon_step_options_t* opts, void* stream);
 
 /* AdamW fallback for non-Muon parameters (the AdamW backup of the printed
  * Muon class, "迎接DeepSeek开源周…Muon优化器", §代码):

@@ -18,6 +18,7 @@ from ._build import LIB_PATH
 
 MUON_F32, MUON_BF16 = 0, 1
 MUON_NS_STANDARD, MUON_NS_GRAM = 0, 1
+MUON_SCALE_RMS, MUON_SCALE_MUP = 0, 1
 QUINTIC = (3.4445, -4.7750, 2.0315)
 
 _STATUS = {0: "MUON_OK", 1: "MUON_ERR_INVALID_ARG", 2: "MUON_ERR_UNSUPPORTED", 3: "MUON_ERR_WORKSPACE",
@@ -27,7 +28,7 @@ EXPORTS = ("muon_handle_create", "muon_handle_destroy", "muon_handle_set_workspa
            "muon_handle_set_timeout_ns", "muon_handle_check", "muon_orthogonalize", "muon_step",
            "adamw_step", "muon_selftest_timeout", "muon_status_string", "muon_last_error", "muon_version",
            "muon_handle_set_profiling", "muon_handle_profile", "muon_handle_launch_count",
-           "muon_orthogonalize_noalloc", "muon_handle_profile_records")
+           "muon_orthogonalize_noalloc", "muon_handle_profile_records", "muon_step_ex")
 KERNEL_CLASSES = ("prepare", "norm", "syrk", "poly", "update", "final", "apply", "adamw")
 
 
@@ -43,6 +44,13 @@ class MuonParamC(ctypes.Structure):
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("param_dtype", ctypes.c_int32),
                 ("grad_dtype", ctypes.c_int32), ("split_heads", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("scale_dim", ctypes.c_int64)]
+
+
+class MuonStepOptionsC(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float), ("nesterov", ctypes.c_int32),
+                ("ns_method", ctypes.c_int32), ("ns_steps", ctypes.c_int32),
+                ("coeffs", ctypes.POINTER(ctypes.c_float)), ("ns_dtype", ctypes.c_int32),
+                ("scale_mode", ctypes.c_int32), ("update_rms", ctypes.c_float), ("extra_scale", ctypes.c_float)]
 
 
 _lib = None
@@ -83,6 +91,7 @@ def load_library(path: str | None = None):
             "muon_orthogonalize_noalloc": (i32, [vp, i32, i64, i64, i32, fptr, vp]),
             "muon_handle_profile_records": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), fptr, i32,
                                                   ctypes.POINTER(i32)]),
+            "muon_step_ex": (i32, [vp, ctypes.POINTER(MuonParamC), i32, ctypes.POINTER(MuonStepOptionsC), vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -238,9 +247,12 @@ def muon_orthogonalize_noalloc(X: torch.Tensor, steps: int = 5, coeffs=None, str
 
 def muon_step(params, grads, momenta, *, lr: float, wd: float, mu: float = 0.95, nesterov: bool = True,
               ns_method="standard", ns_steps: int = 5, coeffs=None, update_rms: float = 0.2, ns_dtype=None,
-              split_heads=None, scale_dims=None, handle: MuonHandle | None = None, stream=None):
+              split_heads=None, scale_dims=None, scale_mode="rms", extra_scale: float = 1.0,
+              handle: MuonHandle | None = None, stream=None):
     """One Muon step over lists of 2-D params (updated in place), grads and
-    fp32 momentum buffers (updated in place)."""
+    fp32 momentum buffers (updated in place).  scale_mode "rms":
+    update_rms * sqrt(max(A, B)); "mup": sqrt(rows / cols); either times
+    extra_scale (muon_step_ex)."""
     n = len(params)
     if len(grads) != n or len(momenta) != n:
         raise ValueError("params, grads and momenta must have the same length")
@@ -261,12 +273,16 @@ def muon_step(params, grads, momenta, *, lr: float, wd: float, mu: float = 0.95,
         ns_dtype = MUON_BF16 if all(p.dtype == torch.bfloat16 for p in params) else MUON_F32
     elif isinstance(ns_dtype, torch.dtype):
         ns_dtype = MUON_BF16 if ns_dtype == torch.bfloat16 else MUON_F32
+    modes = {"rms": MUON_SCALE_RMS, "mup": MUON_SCALE_MUP}
+    if scale_mode not in modes:
+        raise ValueError(f"scale_mode must be one of {tuple(modes)}")
+    cf = _coeffs(coeffs)
+    opts = MuonStepOptionsC(float(lr), float(wd), float(mu), 1 if nesterov else 0, _method(ns_method), int(ns_steps),
+                            cf, int(ns_dtype), modes[scale_mode], float(update_rms), float(extra_scale))
     dev = params[0].device.index if n else None
     h = handle or default_handle(dev)
-    st = h._lib.muon_step(h.ptr, arr, n, float(lr), float(wd), float(mu), 1 if nesterov else 0, _method(ns_method),
-                          int(ns_steps), _coeffs(coeffs), float(update_rms), int(ns_dtype),
-                          ctypes.c_void_p(_stream_ptr(stream)))
-    h._raise(st, "muon_step")
+    st = h._lib.muon_step_ex(h.ptr, arr, n, ctypes.byref(opts), ctypes.c_void_p(_stream_ptr(stream)))
+    h._raise(st, "muon_step_ex")
 
 
 def adamw_step(params, grads, exp_avgs, exp_avg_sqs, *, step: int, lr: float, beta1: float, beta2: float,

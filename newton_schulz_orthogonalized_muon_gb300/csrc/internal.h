@@ -131,11 +131,14 @@ cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& map_a,
 cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
                                      const CUtensorMap& map_b0, const CUtensorMap& map_b1, const NsGemmParams& p,
                                      int grid, cudaStream_t s);
-// CTA-pair variant (tcgen05 cta_group::2, 256 x 256 tiles, standard modes):
-// `pairs` clusters of two CTAs; tiles use 256-row blocks (p.tri / p.mi in
-// 256-row units).
+// CTA-pair variant (tcgen05 cta_group::2, 256 x 256 tiles): `pairs`
+// clusters of two CTAs; tiles use 256-row blocks (p.tri / p.mi in 256-row
+// units) and, for UPDATE / FINAL, 256-column blocks.
 cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b, const NsGemmParams& p,
                                int pairs, cudaStream_t s);
+cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                                      const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
+                                      const NsGemmParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
                                       const CUtensorMap& b0, const CUtensorMap& b1, const NsGemmParams& p, int pairs,
                                       cudaStream_t s);

@@ -283,8 +283,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue
-    mn_epilogue<MODE, BN>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES, xfull + 2 * (warp - 2),
-                          tfull, tempty, abort, tmem_base, warp, lane);
+    EpiTiles et{};
+    et.t0 = blockIdx.x;
+    et.tstep = gridDim.x;
+    et.row_off = 0;
+    et.remote = false;
+    et.tempty = tempty;
+    mn_epilogue<MODE, BN, BM>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES, xfull + 2 * (warp - 2),
+                              tfull, et, abort, tmem_base, warp, lane);
   }
 
   tc_fence_before();

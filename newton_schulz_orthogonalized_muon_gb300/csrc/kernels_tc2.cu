@@ -1,12 +1,13 @@
 // CTA-pair tensor-core Newton-Schulz GEMMs (tcgen05.mma.cta_group::2).
 //
-// The symmetric products of kernels_tc.cu (SYRK and POLY of the standard
+// The products of kernels_tc.cu (SYRK, POLY, UPDATE, FINAL of the standard
 // method; G_R0, G_P, G_PROD of the Gram method) with the same epilogues, on
 // 256 x 256 output tiles computed by a cluster of two CTAs on two SMs:
 //   * each CTA loads its own 128 rows of the A operand and its half (128 of
-//     256) of the B operand per K step, 32 KB per stage instead of the 48 KB
-//     a single CTA needs for a 128 x 256 tile, so six stages fit in shared
-//     memory and each SM pulls a third less data through L2;
+//     256 columns) of the B operand per K step, 32 KB per stage instead of
+//     the 48 KB a single CTA needs for a 128 x 256 tile, so six stages (five
+//     beside the UPDATE / FINAL epilogue buffers) fit in shared memory and
+//     each SM pulls a third less data through L2;
 //   * the leader CTA (cluster rank 0) issues tcgen05.mma.cta_group::2
 //     (M = 256 across the pair, N = 256, K = 16); the hardware reads the
 //     peer's operand halves from the peer's shared memory and writes each
@@ -29,33 +30,43 @@ using namespace tc;
 constexpr int PBM = 256;       // rows of the pair's tile (128 per CTA)
 constexpr int PBN = 256;       // columns of the tile = N of the pair MMA (128 loaded per CTA)
 
-template <int AP, int BP>
+template <int MODE, int AP, int BP>
 struct PairCfg {
   static constexpr int A_BYTES = 128 * BK * 2;           // one plane of this CTA's 128 rows of A
   static constexpr int B_BYTES = 128 * BK * 2;           // one plane of this CTA's half of B
   static constexpr int STAGE_BYTES = AP * A_BYTES + BP * B_BYTES;   // 32 KB with one plane each
-  static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - 256) / STAGE_BYTES;
+  static constexpr int EPI_BYTES = EpiLayout<MODE>::BYTES;
+  static constexpr int BAR_BYTES = 512;
+  // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
+  static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
   static constexpr int TMEM_COLS = 2 * PBN;              // double-buffered 256-column accumulator
-  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + 256;
+  static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
+  static_assert(STAGES >= 2 && SMEM <= MAX_DYN_SMEM, "shared memory");
 };
 
 template <int MODE, int AP, int BP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                         const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
-                        const NsGemmParams p) {
-  using C = PairCfg<AP, BP>;
-  static_assert(ModeTraits<MODE>::kSym, "CTA pairs run the symmetric products only");
+                        const __grid_constant__ CUtensorMap map_xh, const __grid_constant__ CUtensorMap map_xl,
+                        const __grid_constant__ CUtensorMap map_xo, const NsGemmParams p) {
+  using C = PairCfg<MODE, AP, BP>;
+  using L = EpiLayout<MODE>;
+  constexpr bool kUpd = ModeTraits<MODE>::kMN;
+  static_assert(MODE != MODE_G_FINAL, "G_FINAL runs on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;                 // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::EPI_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xfull = drain + 1;                                        // [EPI_WARPS][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull + 2 * EPI_WARPS);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  static_assert(8 * (2 * 8 + 5 + 2 * EPI_WARPS) + 8 <= C::BAR_BYTES, "barrier block");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -74,6 +85,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     mbar_init(&tempty[0], 2 * EPI_WARPS);   // leader: every epilogue warp of both CTAs
     mbar_init(&tempty[1], 2 * EPI_WARPS);
     mbar_init(drain, 1);
+    for (int w = 0; w < 2 * EPI_WARPS; ++w) mbar_init(&xfull[w], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -83,6 +95,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     tma_prefetch_map(&map_b0);
     if (AP == 2) tma_prefetch_map(&map_a1);
     if (BP == 2) tma_prefetch_map(&map_b1);
+    if (L::kLoadX) {
+      tma_prefetch_map(&map_xh);
+      tma_prefetch_map(&map_xl);
+    }
+    if (MODE == MODE_UPDATE) tma_prefetch_map(&map_xo);
   }
   tc_fence_before();
   cluster_sync_all();      // the peer's barriers are initialised and TMEM is allocated in both CTAs
@@ -121,8 +138,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           for (int pb = 0; pb < BP; ++pb) {
             const CUtensorMap* mb = pb == 0 ? &map_b0 : &map_b1;
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-              tma_load_3d_pair(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, fb, kb * BK, bcol + q * 64, b);
+            for (int q = 0; q < 2; ++q) {
+              if (kUpd)      // X^ read MN-major: 64 columns x 64 K rows per box
+                tma_load_3d_pair(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, fb, bcol + q * 64, kb * BK, b);
+              else
+                tma_load_3d_pair(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, fb, kb * BK, bcol + q * 64, b);
+            }
           }
           ++issued;
           if (++s == C::STAGES) {
@@ -143,7 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ----------------------------------------------- MMA issuer (leader)
-      const uint32_t idesc = idesc_bf16_f32(PBM, PBN, 0);
+      const uint32_t idesc = idesc_bf16_f32(PBM, PBN, kUpd ? 1 : 0);
       int s = 0, acc = 0;
       uint32_t ph = 0, acc_ph = 0;
       bool ok = true;
@@ -166,7 +187,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t a0 = sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t b0 = sdesc_sw128(sb + kk * 32, 16, 1024);
+            // K-major B: 32 bytes per K = 16 step; MN-major B: 2 KB per step,
+            // 8 KB between the two 64-column boxes
+            const uint64_t b0 = kUpd ? sdesc_sw128(sb + kk * 2048, BOX_BYTES, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma_bf16_pair(d, a0, b0, idesc, (kb | kk) != 0 ? 1u : 0u);
             if (BP == 2)     // hi(A) * lo(B)
               umma_bf16_pair(d, a0, sdesc_sw128(sb + C::B_BYTES + kk * 32, 16, 1024), idesc, 1u);
@@ -188,7 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       umma_commit_pair_mc(drain, 0x1);
       mbar_wait_bounded(drain, 0, nullptr, DRAIN_NS);
     }
-  } else {
+  } else if constexpr (ModeTraits<MODE>::kSym) {
     // --------------------------------------------------------- epilogue
     // warps 2-9: TMEM lane quadrant = warp % 4 (hardware rule), column half =
     // (warp - 2) / 4; each thread owns one output row of its half.
@@ -231,6 +254,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_ph ^= 1u;
     }
+  } else {
+    // --------------------------------------------------------- epilogue
+    // UPDATE / FINAL: each CTA drains its own 128 accumulator rows of the
+    // 256 x 256 tile through the TMA epilogue; the accumulator is handed
+    // back to the leader's "tmem empty" barrier.
+    EpiTiles et{};
+    et.t0 = pair;
+    et.tstep = npairs;
+    et.row_off = static_cast<int>(rank) * 128;
+    et.remote = true;
+    et.tempty = nullptr;
+    et.tempty_remote[0] = mapa_shared(smem_u32(&tempty[0]), 0);
+    et.tempty_remote[1] = mapa_shared(smem_u32(&tempty[1]), 0);
+    mn_epilogue<MODE, PBN, PBM>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES,
+                                xfull + 2 * (warp - 2), tfull, et, abort, tmem_base, warp, lane);
   }
 
   tc_fence_before();
@@ -245,27 +283,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
 template <int MODE, int AP, int BP>
 cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const NsGemmParams& p, int pairs, cudaStream_t s) {
+                        const CUtensorMap& xh, const CUtensorMap& xl, const CUtensorMap& xo, const NsGemmParams& p,
+                        int pairs, cudaStream_t s) {
   auto kern = ns_gemm_pair_kernel<MODE, AP, BP>;
-  using C = PairCfg<AP, BP>;
+  using C = PairCfg<MODE, AP, BP>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<2 * pairs, TC_THREADS, C::SMEM, s>>>(a0, a1, b0, b1, p);
+  kern<<<2 * pairs, TC_THREADS, C::SMEM, s>>>(a0, a1, b0, b1, xh, xl, xo, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// Number of CTA pairs of this kernel that fit on the device at once.
+// Number of CTA pairs of this kernel that fit on the device at once (the
+// UPDATE instantiation has the largest shared-memory footprint).
 int ns_gemm_pair_max_pairs() {
   static int cached = -1;
   if (cached < 0) {
-    auto kern = ns_gemm_pair_kernel<MODE_SYRK, 1, 1>;
-    using C = PairCfg<1, 1>;
+    auto kern = ns_gemm_pair_kernel<MODE_UPDATE, 1, 1>;
+    using C = PairCfg<MODE_UPDATE, 1, 1>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM)) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -296,9 +336,20 @@ cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& a, const CUtensorMa
                                int pairs, cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   switch (mode) {
-    case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b, p, pairs, s);
-    case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b, p, pairs, s);
-    case MODE_G_R0: return launch_pair<MODE_G_R0, 1, 1>(a, a, b, b, p, pairs, s);
+    case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
+    case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
+    case MODE_G_R0: return launch_pair<MODE_G_R0, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& xh,
+                                      const CUtensorMap& xl, const CUtensorMap& xo, const NsGemmParams& p, int pairs,
+                                      cudaStream_t s) {
+  if (p.num_tiles == 0) return cudaSuccess;
+  switch (mode) {
+    case MODE_UPDATE: return launch_pair<MODE_UPDATE, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
+    case MODE_FINAL: return launch_pair<MODE_FINAL, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -308,8 +359,8 @@ cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CU
                                       cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   switch (mode) {
-    case MODE_G_P: return launch_pair<MODE_G_P, 2, 2>(a0, a1, b0, b1, p, pairs, s);
-    case MODE_G_PROD: return launch_pair<MODE_G_PROD, 2, 2>(a0, a1, b0, b1, p, pairs, s);
+    case MODE_G_P: return launch_pair<MODE_G_P, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, pairs, s);
+    case MODE_G_PROD: return launch_pair<MODE_G_PROD, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, pairs, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -73,6 +73,8 @@ struct muon_handle_s {
   size_t prof_used = 0;
   uint64_t launches = 0;
   bool use_pair = true;         // CTA-pair GEMMs for large groups (MUON_TC_PAIR=0 disables)
+  bool pair_update = true;      // UPDATE / FINAL on pairs too (MUON_TC_PAIR=sym: symmetric products only)
+  int pair_min_m = 2048;        // ragged m from here on runs on pairs too (MUON_TC_PAIR_MIN_M)
   int max_pairs = 0;
 };
 
@@ -225,8 +227,9 @@ std::vector<int2> sym_tiles(int m, int bn, int bm = 128) {
   return t;
 }
 
-// Groups whose m fills 256-row pair tiles well run on the CTA-pair kernels.
-bool pair_group(int m) { return m >= 256 && (m % 256 == 0 || m >= 2048); }
+// Groups whose m fills 256-row pair tiles well run on the CTA-pair kernels:
+// m a multiple of 256, or m >= pair_min_m (ragged last tile).
+bool pair_group(int m, int pair_min_m) { return m >= 256 && (m % 256 == 0 || m >= pair_min_m); }
 
 struct GroupPlan {
   int m = 0, n = 0;
@@ -507,7 +510,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         g.tri128_count = static_cast<int>(t128.size());
         g.tri128_off = arena_push(arena, t128.data(), t128.size());
       }
-      if (h->use_pair && h->max_pairs > 0 && pair_group(g.m)) {
+      if (h->use_pair && h->max_pairs > 0 && pair_group(g.m, h->pair_min_m)) {
         std::vector<int2> t256 = sym_tiles(g.m, 256, 256);
         g.tri256_count = static_cast<int>(t256.size());
         g.tri256_off = arena_push(arena, t256.data(), t256.size());
@@ -613,8 +616,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         p.timeout_ns = h->timeout_ns;
         p.pdiag = pdiag;
         if (tc && g.pair) {
-          // SYRK and POLY on CTA pairs (256 x 256 tiles); UPDATE / FINAL on
-          // one-CTA kernels, whose heavier epilogue gains nothing from pairing
+          // SYRK, POLY and (unless MUON_TC_PAIR=sym) UPDATE / FINAL on CTA
+          // pairs, 256 x 256 tiles
           NsGemmParams q = p;
           q.tiles_per_mat = g.tri256_count;
           q.num_tiles = cnt * g.tri256_count;
@@ -628,14 +631,26 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.sym_out = symB;
           MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, q, pairs, stream), "poly launch");
           NsGemmParams u = p;
-          u.mi = mi;
-          u.tiles_per_mat = mi * nj;
-          u.num_tiles = cnt * mi * nj;
-          const int grid = std::min(u.num_tiles, h->num_sms);
-          MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                      launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1],
-                                               map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
-                      "update launch");
+          if (h->pair_update) {
+            const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
+            u.mi = mi2;
+            u.tiles_per_mat = mi2 * nj2;
+            u.num_tiles = cnt * mi2 * nj2;
+            const int upairs = std::min(u.num_tiles, h->max_pairs);
+            MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                        launch_ns_gemm_pair_update(last ? MODE_FINAL : MODE_UPDATE, map_B, map_x[it & 1],
+                                                   map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream),
+                        "update launch");
+          } else {
+            u.mi = mi;
+            u.tiles_per_mat = mi * nj;
+            u.num_tiles = cnt * mi * nj;
+            const int grid = std::min(u.num_tiles, h->num_sms);
+            MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                        launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1],
+                                                 map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
+                        "update launch");
+          }
         } else if (tc) {
           // SYRK: A = s^2 X X^T
           NsGemmParams q = p;
@@ -735,6 +750,11 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   const char* pair_env = std::getenv("MUON_TC_PAIR");
   h->use_pair = !(pair_env != nullptr && pair_env[0] == '0');
+  h->pair_update = h->use_pair && !(pair_env != nullptr && std::strcmp(pair_env, "sym") == 0);
+  if (const char* mm = std::getenv("MUON_TC_PAIR_MIN_M")) {
+    const long v = std::strtol(mm, nullptr, 10);
+    if (v >= 256 && v <= (1L << 30)) h->pair_min_m = static_cast<int>(v);
+  }
   h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
   if (cudaMalloc(&h->err, sizeof(unsigned)) != cudaSuccess || cudaMemset(h->err, 0, sizeof(unsigned)) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) {
@@ -816,17 +836,21 @@ muon_status_t muon_orthogonalize(muon_handle_t h, void* X, int32_t dtype, int64_
   return run_blocks(h, blocks, 0.f, 0, steps, cf, ns_method, dtype == MUON_BF16, static_cast<cudaStream_t>(stream));
 }
 
-muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_params, float lr, float wd,
-                        float mu, int32_t nesterov, int32_t ns_method, int32_t ns_steps, const float* coeffs,
-                        float update_rms, int32_t ns_dtype, void* stream) {
+muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t n_params,
+                           const muon_step_options_t* opts, void* stream) {
   if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  if (opts == nullptr) return fail(h, MUON_ERR_INVALID_ARG, "opts is NULL");
+  const muon_step_options_t o = *opts;
   if (n_params < 0) return fail(h, MUON_ERR_INVALID_ARG, "n_params < 0");
   if (n_params > 0 && params == nullptr) return fail(h, MUON_ERR_INVALID_ARG, "params is NULL");
-  if (!valid_dtype(ns_dtype)) return fail(h, MUON_ERR_INVALID_ARG, "ns_dtype must be MUON_F32 or MUON_BF16");
-  if (ns_method != MUON_NS_STANDARD && ns_method != MUON_NS_GRAM)
+  if (!valid_dtype(o.ns_dtype)) return fail(h, MUON_ERR_INVALID_ARG, "ns_dtype must be MUON_F32 or MUON_BF16");
+  if (o.ns_method != MUON_NS_STANDARD && o.ns_method != MUON_NS_GRAM)
     return fail(h, MUON_ERR_INVALID_ARG, "unknown ns_method");
-  if (ns_steps < 0 || ns_steps > 100) return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 100]");
-  if (!std::isfinite(lr) || !std::isfinite(wd) || !std::isfinite(mu) || !std::isfinite(update_rms))
+  if (o.ns_steps < 0 || o.ns_steps > 100) return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 100]");
+  if (o.scale_mode != MUON_SCALE_RMS && o.scale_mode != MUON_SCALE_MUP)
+    return fail(h, MUON_ERR_INVALID_ARG, "unknown scale_mode");
+  if (!std::isfinite(o.lr) || !std::isfinite(o.wd) || !std::isfinite(o.mu) || !std::isfinite(o.update_rms) ||
+      !std::isfinite(o.extra_scale))
     return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
   std::vector<Block> blocks;
   for (int32_t i = 0; i < n_params; ++i) {
@@ -843,9 +867,17 @@ muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_p
     if (P.param == nullptr || P.grad == nullptr || P.momentum == nullptr)
       return fail(h, MUON_ERR_INVALID_ARG, where + "NULL pointer");
     const int64_t rb = P.rows / P.split_heads;
-    const double sdim = static_cast<double>(P.scale_dim > 0 ? P.scale_dim : std::max(P.rows, P.cols));
-    const float beta = static_cast<float>(-static_cast<double>(lr) * update_rms * std::sqrt(sdim));
-    const float alpha = static_cast<float>(1.0 - static_cast<double>(lr) * wd);
+    // update scale: RMS matching update_rms * sqrt(max(A, B)) (or scale_dim),
+    // or muP sqrt(d_out / d_in) of the stored (out x in) parameter
+    double scale;
+    if (o.scale_mode == MUON_SCALE_MUP) {
+      scale = std::sqrt(static_cast<double>(P.rows) / static_cast<double>(P.cols));
+    } else {
+      const double sdim = static_cast<double>(P.scale_dim > 0 ? P.scale_dim : std::max(P.rows, P.cols));
+      scale = static_cast<double>(o.update_rms) * std::sqrt(sdim);
+    }
+    const float beta = static_cast<float>(-static_cast<double>(o.lr) * o.extra_scale * scale);
+    const float alpha = static_cast<float>(1.0 - static_cast<double>(o.lr) * o.wd);
     const size_t ge = dtype_size(P.grad_dtype), pe = dtype_size(P.param_dtype);
     for (int32_t hb = 0; hb < P.split_heads; ++hb) {
       const size_t off = static_cast<size_t>(hb) * rb * P.cols;
@@ -861,9 +893,27 @@ muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_p
   }
   if (blocks.empty()) return MUON_OK;
   DeviceGuard guard(h->device);
-  const float* cf = coeffs ? coeffs : kDefaultCoeffs;
-  return run_blocks(h, blocks, mu, nesterov ? 1 : 0, ns_steps, cf, ns_method, ns_dtype == MUON_BF16,
+  const float* cf = o.coeffs ? o.coeffs : kDefaultCoeffs;
+  return run_blocks(h, blocks, o.mu, o.nesterov ? 1 : 0, o.ns_steps, cf, o.ns_method, o.ns_dtype == MUON_BF16,
                     static_cast<cudaStream_t>(stream));
+}
+
+muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_params, float lr, float wd,
+                        float mu, int32_t nesterov, int32_t ns_method, int32_t ns_steps, const float* coeffs,
+                        float update_rms, int32_t ns_dtype, void* stream) {
+  muon_step_options_t o{};
+  o.lr = lr;
+  o.wd = wd;
+  o.mu = mu;
+  o.nesterov = nesterov;
+  o.ns_method = ns_method;
+  o.ns_steps = ns_steps;
+  o.coeffs = coeffs;
+  o.ns_dtype = ns_dtype;
+  o.scale_mode = MUON_SCALE_RMS;
+  o.update_rms = update_rms;
+  o.extra_scale = 1.0f;
+  return muon_step_ex(h, params, n_params, &o, stream);
 }
 
 muon_status_t adamw_step(muon_handle_t h, void* const* params, const void* const* grads, float* const* exp_avg,

@@ -235,44 +235,100 @@ __device__ __forceinline__ void store_out_4(const OutEntry& e, int r, int c0, in
     if (c0 + k < n) store_from_f32(e.ptr, idx + k, e.dtype, v[k]);
 }
 
-// the old destination values matching store_out_4 (zeros when alpha == 0)
-__device__ __forceinline__ float4 load_out_4(const OutEntry& e, int r, int c0, int n) {
-  float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+// The old destination values matching store_out_4, as raw bits so that the
+// load can be issued well before its use: a 16-byte-aligned fp32 segment or
+// an 8-byte-aligned bf16 segment is loaded whole (decode_out_4 converts it);
+// anything else (ragged, misaligned) element by element, already as floats.
+// Zeros when alpha == 0.
+__device__ __forceinline__ bool out4_vec(const OutEntry& e, long long idx, int c0, int n) {
+  if (c0 + 3 >= n) return false;
+  const uintptr_t a = e.dtype == DT_BF16 ? reinterpret_cast<uintptr_t>(reinterpret_cast<const __nv_bfloat16*>(e.ptr) + idx)
+                                         : reinterpret_cast<uintptr_t>(reinterpret_cast<const float*>(e.ptr) + idx);
+  return (a & (e.dtype == DT_BF16 ? 7u : 15u)) == 0;
+}
+
+__device__ __forceinline__ uint4 load_out_4_raw(const OutEntry& e, int r, int c0, int n) {
+  uint4 w = make_uint4(0u, 0u, 0u, 0u);
   if (e.alpha == 0.f) return w;
   const long long idx = static_cast<long long>(r) * e.ld + c0;
-  if (c0 + 3 < n) {
+  if (out4_vec(e, idx, c0, n)) {
     if (e.dtype == DT_BF16) {
-      const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(e.ptr) + idx;
-      if ((reinterpret_cast<uintptr_t>(q) & 7) == 0) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(q);
-        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        return make_float4(a.x, a.y, b.x, b.y);
-      }
+      const uint2 raw = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(e.ptr) + idx);
+      w.x = raw.x;
+      w.y = raw.y;
     } else {
-      const float* q = reinterpret_cast<const float*>(e.ptr) + idx;
-      if ((reinterpret_cast<uintptr_t>(q) & 15) == 0) return *reinterpret_cast<const float4*>(q);
+      w = *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(e.ptr) + idx);
     }
+    return w;
   }
   float t[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < 4; ++k)
     if (c0 + k < n) t[k] = load_as_f32(e.ptr, idx + k, e.dtype);
-  return make_float4(t[0], t[1], t[2], t[3]);
+  return make_uint4(__float_as_uint(t[0]), __float_as_uint(t[1]), __float_as_uint(t[2]), __float_as_uint(t[3]));
 }
 
+__device__ __forceinline__ float4 decode_out_4(const OutEntry& e, int r, int c0, int n, uint4 w) {
+  if (e.alpha != 0.f && e.dtype == DT_BF16 && out4_vec(e, static_cast<long long>(r) * e.ld + c0, c0, n)) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w));
+}
+
+// One 32 x 32 destination block of a FINAL / G_FINAL warp: destination rows
+// drow0 .. drow0+31 (< dlim), columns dcol0 .. dcol0+31 (< dcols); lane
+// (rq = lane / 8, q = lane % 8) covers row 4 it + rq, columns 4q .. 4q+3.
+struct OutBlock {
+  OutEntry e;          // row-wise view of the destination (transposition folded into drow0 / dcol0)
+  int drow0, dlim, dcol0, dcols;
+};
+
+__device__ __forceinline__ OutBlock out_block(const OutEntry& oe, int row0, int gcb, int m, int n) {
+  const bool tr = oe.transposed != 0;
+  OutBlock o;
+  o.e = OutEntry{oe.ptr, oe.ld, 0, oe.dtype, oe.alpha, oe.beta};
+  o.drow0 = tr ? gcb : row0;
+  o.dlim = tr ? n : m;
+  o.dcol0 = tr ? row0 : gcb;
+  o.dcols = tr ? m : n;
+  return o;
+}
+
+__device__ __forceinline__ void prefetch_out_block(const OutBlock& o, int lane, uint4* w) {
+  const int rq = lane >> 3, q = lane & 7;
+  const bool colok = o.dcol0 + 4 * q < o.dcols;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = 4 * it + rq;
+    w[it] = (o.drow0 + r < o.dlim && colok) ? load_out_4_raw(o.e, o.drow0 + r, o.dcol0 + 4 * q, o.dcols)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Where an epilogue warp's tiles are and whom it tells that the accumulator
+// is free again: tiles t0, t0 + tstep, ...; tile row block i covers rows
+// i * TROWS + row_off .. + 127 of this CTA; one-CTA kernel: the local
+// "tmem empty" barrier; CTA pair: the leader's, at cluster addresses.
+struct EpiTiles {
+  int t0, tstep, row_off;
+  bool remote;
+  uint64_t* tempty;                 // local barriers (remote == false)
+  uint32_t tempty_remote[2];        // leader's barriers (remote == true)
+};
+
 // The whole tile loop of one epilogue warp for the UPDATE / FINAL / G_FINAL
-// modes (tiles blockIdx.x, blockIdx.x + gridDim.x, ... of the one-CTA
-// kernel).  wbuf: this warp's WARP_BYTES of shared memory (1024-aligned);
+// modes.  wbuf: this warp's WARP_BYTES of shared memory (1024-aligned);
 // xfull: this warp's SLOTS barriers.  Maps (3-D, 32 x 32 bf16 boxes, 64-byte
 // swizzle): map_xh = hi plane read this iteration (the B operand), map_xl =
 // lo plane (read and written in place), map_xo = hi plane written for the
 // next iteration.  On return (also after a timeout, already recorded) the
 // warp's loads have landed and its stores have completed.
-template <int MODE, int BN>
+template <int MODE, int BN, int TROWS>
 __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtensorMap* map_xh,
                                             const CUtensorMap* map_xl, const CUtensorMap* map_xo, uint8_t* wbuf,
-                                            uint64_t* xfull, uint64_t* tfull, uint64_t* tempty, volatile int* abort,
+                                            uint64_t* xfull, uint64_t* tfull, const EpiTiles& et, volatile int* abort,
                                             uint32_t tmem_base, int warp, int lane) {
   using L = EpiLayout<MODE>;
   constexpr int NB = BN / 64;                          // 32-column blocks per warp per tile
@@ -281,7 +337,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   const uint32_t wsm = smem_u32(wbuf);
 
   // ---- input prefetch, in this warp's block order, at most SLOTS blocks ahead
-  int pf_t = blockIdx.x, pf_blk = 0;
+  int pf_t = et.t0, pf_blk = 0;
   uint32_t issued = 0, done = 0;
   auto issue_next = [&]() {
     while (pf_t < p.num_tiles) {
@@ -293,7 +349,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         if (lane == 0) {
           const int slot = static_cast<int>(issued & 1u);
           const uint32_t dst = wsm + slot * L::SLOT_BYTES;
-          const int x = g0 + 32 * pf_blk, y = i * BM + quad * 32;
+          const int x = g0 + 32 * pf_blk, y = i * TROWS + et.row_off + quad * 32;
           mbar_arrive_expect_tx(&xfull[slot], L::SLOT_BYTES);
           tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
           tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
@@ -302,7 +358,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         ++pf_blk;
         return;
       }
-      pf_t += gridDim.x;
+      pf_t += et.tstep;
       pf_blk = 0;
     }
   };
@@ -314,16 +370,22 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   bool ok = true;
   int acc = 0;
   uint32_t acc_ph = 0;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+  uint4 wpre[8];                        // FINAL / G_FINAL: old destination values of the next block
+  for (int t = et.t0; t < p.num_tiles; t += et.tstep) {
     int b, i, j;
     decode_tile<MODE>(p, t, b, i, j);
+    if (MODE != MODE_UPDATE) {
+      // the tile's first block of old destination values, under the main loop
+      const int g0p = j * BN + cbeg;
+      if (g0p < p.n) prefetch_out_block(out_block(p.out[b], i * TROWS + et.row_off + quad * 32, g0p, p.m, p.n), lane, wpre);
+    }
     if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
       if (lane == 0) raise_timeout(abort, p.err);
       ok = false;
       break;
     }
     tc_fence_after();
-    const int row0 = i * BM + quad * 32;
+    const int row0 = i * TROWS + et.row_off + quad * 32;
     const int gr = row0 + lane;
     const float s = p.scale != nullptr ? p.scale[b] : 1.f;
     // exact diagonal term: acc + P_rr x - P^_rr hi, hi being the operand copy
@@ -425,27 +487,20 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
           }
         }
         __syncwarp();                    // the block's results are in the slot
-        // destination rows of this block: drow0 + (0..31), limit dlim; columns
-        // dcol0 + (0..31), limit dcols
-        const int drow0 = tr ? gcb : row0, dlim = tr ? p.n : p.m;
-        const int dcol0 = tr ? row0 : gcb, dcols = tr ? p.m : p.n;
-        const OutEntry rowwise{oe.ptr, oe.ld, 0, oe.dtype, oe.alpha, oe.beta};
+        const OutBlock ob = out_block(oe, row0, gcb, p.m, p.n);
         const int rq = lane >> 3, q = lane & 7;
-        const bool colok = dcol0 + 4 * q < dcols;
-        float4 w[8];
+        const bool colok = ob.dcol0 + 4 * q < ob.dcols;
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
           const int r = 4 * it + rq;
-          w[it] = (drow0 + r < dlim && colok) ? load_out_4(rowwise, drow0 + r, dcol0 + 4 * q, dcols)
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ob.drow0 + r < ob.dlim && colok) {
+            const float4 old = decode_out_4(ob.e, ob.drow0 + r, ob.dcol0 + 4 * q, ob.dcols, wpre[it]);
+            store_out_4(ob.e, ob.drow0 + r, ob.dcol0 + 4 * q, ob.dcols,
+                        *reinterpret_cast<const float4*>(sbuf + sw128_off(r, q)), old);
+          }
         }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int r = 4 * it + rq;
-          if (drow0 + r < dlim && colok)
-            store_out_4(rowwise, drow0 + r, dcol0 + 4 * q, dcols,
-                        *reinterpret_cast<const float4*>(sbuf + sw128_off(r, q)), w[it]);
-        }
+        // the next block's old destination values, one block ahead
+        if (k + 1 < nb) prefetch_out_block(out_block(oe, row0, gcb + 32, p.m, p.n), lane, wpre);
         fence_proxy_async_smem();        // generic accesses of the slot before its next TMA fill
         __syncwarp();
       }
@@ -455,7 +510,12 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
     if (!ok) break;
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&tempty[acc]);
+    if (lane == 0) {
+      if (et.remote)
+        mbar_arrive_cluster(et.tempty_remote[acc]);
+      else
+        mbar_arrive(&et.tempty[acc]);
+    }
     acc ^= 1;
     if (acc == 0) acc_ph ^= 1u;
   }

@@ -151,21 +151,38 @@ def orthogonalize(X, steps: int = NS_STEPS, coeffs=QUINTIC, method: str = "stand
     raise ValueError(f"unknown Newton-Schulz method {method!r}")
 
 
-def update_scale(shape, update_rms: float = UPDATE_RMS) -> float:
-    """0.2 * sqrt(max(A, B)) with A, B the first two dimensions of the
-    parameter's shape: scales the orthogonalised update to the RMS of an
-    AdamW update ([Moonlight] §2 参数更新尺度调整 and adjust_lr_for_muon
-    under §代码)."""
+def update_scale(shape, update_rms: float = UPDATE_RMS, mode: str = "rms", extra: float = 1.0) -> float:
+    """The factor the orthogonalised update is multiplied by, times
+    ``extra`` (MindSpeed's extra scale factor, [MindSpeed] parameter table,
+    --muon-extra-scale-factor).  A, B are the parameter's first two
+    dimensions.
+
+    * "rms": update_rms * sqrt(max(A, B)), 0.2 by default: scales the update
+      to the RMS of an AdamW update ([Moonlight] §2 参数更新尺度调整 and
+      adjust_lr_for_muon under §代码).  DeepSeek-V4's rescaling
+      sqrt(max(n, m)) * gamma is this form with update_rms = gamma ([Chensy]
+      §Variation of Muon Optimizer).
+    * "mup": sqrt(d_out / d_in) with the weight stored as (d_out, d_in) =
+      (A, B): the dual of the gradient under the RMS -> RMS operator norm
+      is sqrt(d_out / d_in) msign(G) ([Chensy] §Variation of Muon
+      Optimizer, the muP form)."""
     A, B = int(shape[0]), int(shape[1])
-    return update_rms * math.sqrt(max(A, B))
+    if mode == "rms":
+        base = update_rms * math.sqrt(max(A, B))
+    elif mode == "mup":
+        base = math.sqrt(A / B)
+    else:
+        raise ValueError(f"unknown scale mode {mode!r}")
+    return extra * base
 
 
-def apply_update(W, O, lr: float, wd: float, shape, update_rms: float = UPDATE_RMS):
+def apply_update(W, O, lr: float, wd: float, shape, update_rms: float = UPDATE_RMS, mode: str = "rms",
+                 extra: float = 1.0):
     """Decoupled weight decay then the scaled step:
-    W <- W * (1 - lr*wd) - lr * 0.2*sqrt(max(A,B)) * O; the decay uses the
-    unadjusted lr ([Moonlight] §1 权重衰减机制, §2 更新公式, and the Muon step
-    under §代码)."""
-    return _f64(W) * (1.0 - lr * wd) - lr * update_scale(shape, update_rms) * _f64(O)
+    W <- W * (1 - lr*wd) - lr * scale * O (scale from update_scale, by
+    default 0.2*sqrt(max(A,B))); the decay uses the unadjusted lr
+    ([Moonlight] §1 权重衰减机制, §2 更新公式, and the Muon step under §代码)."""
+    return _f64(W) * (1.0 - lr * wd) - lr * update_scale(shape, update_rms, mode, extra) * _f64(O)
 
 
 def orthogonalize_split(U, split_heads: int = 1, steps: int = NS_STEPS, coeffs=QUINTIC,
@@ -186,7 +203,8 @@ def orthogonalize_split(U, split_heads: int = 1, steps: int = NS_STEPS, coeffs=Q
 
 def muon_step(W, G, M, *, lr: float, wd: float, mu: float = 0.95, nesterov: bool = True,
               steps: int = NS_STEPS, coeffs=QUINTIC, method: str = "standard",
-              split_heads: int = 1, update_rms: float = UPDATE_RMS, eps: float = NORM_EPS):
+              split_heads: int = 1, update_rms: float = UPDATE_RMS, eps: float = NORM_EPS,
+              scale_mode: str = "rms", extra_scale: float = 1.0):
     """One Muon step for one parameter ([Moonlight] §代码, Muon step):
     momentum (and Nesterov), Newton-Schulz on the (flattened) update, then
     decay and the scaled update.  A gradient with more than two dimensions is
@@ -198,7 +216,7 @@ def muon_step(W, G, M, *, lr: float, wd: float, mu: float = 0.95, nesterov: bool
     M2 = _f64(M).reshape(G2.shape)
     M_new, U = momentum_update(M2, G2, mu, nesterov)
     O = orthogonalize_split(U, split_heads, steps, coeffs, method, eps)
-    W_new = apply_update(W.reshape(O.shape), O, lr, wd, W.shape, update_rms)
+    W_new = apply_update(W.reshape(O.shape), O, lr, wd, W.shape, update_rms, scale_mode, extra_scale)
     return W_new.reshape(W.shape), M_new.reshape(np.shape(M))
 
 

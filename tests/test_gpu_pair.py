@@ -3,7 +3,8 @@
 Groups whose m is a multiple of 256 (or >= 2048) run on the pair kernels;
 a handle created with MUON_TC_PAIR=0 runs the one-CTA kernels.  Both are
 compared with the fp64 oracle, and with each other, on the same inputs,
-including ragged n, transposed matrices and batches.
+including ragged n, a ragged last 256-row tile (m = 2176), transposed
+matrices and batches.
 """
 import os
 
@@ -42,7 +43,8 @@ def handles():
     return pkg, pair, single
 
 
-@pytest.mark.parametrize("shape", [(256, 1024), (512, 700), (768, 3072), (3072, 768), (2048, 2304), (512, 512)])
+@pytest.mark.parametrize("shape", [(256, 1024), (512, 700), (768, 3072), (3072, 768), (2048, 2304), (512, 512),
+                                   (2176, 2400)])
 def test_pair_kernels_match_oracle_and_single(handles, shape):
     pkg, pair, single = handles
     X = wl.lowrank_grad(70, shape[0], shape[1], 64)
@@ -93,4 +95,36 @@ def test_pair_gram_matches_oracle_and_single(handles, shape):
     ga, gb = a.double().cpu().numpy(), b.double().cpu().numpy()
     assert _rel(ga, ref) < TOL_BF16
     assert _rel(gb, ref) < TOL_BF16
+    assert _rel(ga, gb) < TOL_BF16
+
+
+@pytest.fixture(scope="module")
+def ragged_handle(handles):
+    """A handle that runs groups with m >= 1024 on pairs even when m is not a
+    multiple of 256 (the last 256-row tile is ragged)."""
+    pkg = handles[0]
+    old = os.environ.get("MUON_TC_PAIR_MIN_M")
+    os.environ["MUON_TC_PAIR_MIN_M"] = "1024"
+    try:
+        return pkg.MuonHandle(0)
+    finally:
+        if old is None:
+            del os.environ["MUON_TC_PAIR_MIN_M"]
+        else:
+            os.environ["MUON_TC_PAIR_MIN_M"] = old
+
+
+@pytest.mark.parametrize("shape", [(1408, 2048), (1152, 1600), (2048, 1408)])
+def test_ragged_pair_tiles_match_oracle_and_single(handles, ragged_handle, shape):
+    pkg, _, single = handles
+    X = wl.lowrank_grad(72, shape[0], shape[1], 64)
+    t = torch.tensor(X).to(torch.bfloat16).cuda()
+    ref = oracle.newton_schulz(t.double().cpu().numpy())
+    a, b = t.clone(), t.clone()
+    pkg.muon_orthogonalize(a, handle=ragged_handle)
+    pkg.muon_orthogonalize(b, handle=single)
+    torch.cuda.synchronize()
+    assert ragged_handle.check() == 0 and single.check() == 0
+    ga, gb = a.double().cpu().numpy(), b.double().cpu().numpy()
+    assert _rel(ga, ref) < TOL_BF16
     assert _rel(ga, gb) < TOL_BF16

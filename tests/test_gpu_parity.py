@@ -130,7 +130,8 @@ def test_orthogonalize_zero_and_empty(pkg):
 
 # ----------------------------------------------------------- muon_step
 
-def run_step(pkg, specs, dtype, steps=1, ns_steps=5, lr=0.02, wd=0.1, mu=0.95, nesterov=True, seed=0):
+def run_step(pkg, specs, dtype, steps=1, ns_steps=5, lr=0.02, wd=0.1, mu=0.95, nesterov=True, seed=0,
+             **scale):
     """Run `steps` Muon steps on GPU and in the oracle from the same start;
     return per-param (W_gpu, W_ref, W_decay_only, M_gpu, M_ref) after the
     last step, W_decay_only = W0 * (1 - lr*wd)^steps (so W - W_decay_only is
@@ -145,10 +146,11 @@ def run_step(pkg, specs, dtype, steps=1, ns_steps=5, lr=0.02, wd=0.1, mu=0.95, n
         G = [wl.lowrank_grad(seed + 1000 * k + i, s.shape[0], s.shape[1], 16, scale=1.0) for i, s in enumerate(specs)]
         Gd = [to_dev(g, dtype) for g in G]
         pkg.muon_step(Wd, Gd, Md, lr=lr, wd=wd, mu=mu, nesterov=nesterov, ns_steps=ns_steps,
-                      split_heads=[s.split_heads for s in specs])
+                      split_heads=[s.split_heads for s in specs], **scale)
         for i, s in enumerate(specs):
             W_ref[i], M_ref[i] = oracle.muon_step(W_ref[i], host64(Gd[i]), M_ref[i], lr=lr, wd=wd, mu=mu,
-                                                  nesterov=nesterov, steps=ns_steps, split_heads=s.split_heads)
+                                                  nesterov=nesterov, steps=ns_steps, split_heads=s.split_heads,
+                                                  **scale)
     torch.cuda.synchronize()
     assert pkg.default_handle().check() == 0
     return [(host64(Wd[i]), W_ref[i], W_decay[i], host64(Md[i]), M_ref[i]) for i in range(len(specs))]
@@ -216,6 +218,21 @@ def test_step_bf16_split_heads(pkg):
         assert delta_err_bf16(w_gpu, w_ref, base, 1) < TOL_BF16
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("scale", [dict(scale_mode="mup"), dict(scale_mode="mup", extra_scale=1.5),
+                                   dict(update_rms=0.18, extra_scale=0.5)])
+def test_step_scale_modes(pkg, dtype, scale):
+    # muP sqrt(d_out / d_in), DeepSeek-V4 gamma as update_rms, and the extra
+    # scale factor, on wide, tall and square parameters
+    specs = [wl.ParamSpec("a", (128, 384)), wl.ParamSpec("b", (384, 128)), wl.ParamSpec("c", (192, 192))]
+    for w_gpu, w_ref, base, m_gpu, m_ref in run_step(pkg, specs, dtype, steps=1, **scale):
+        if dtype == torch.float32:
+            assert delta_err(w_gpu, w_ref, base) < TOL_F32
+        else:
+            assert delta_err_bf16(w_gpu, w_ref, base, 1) < TOL_BF16
+        assert rel(m_gpu, m_ref) < TOL_EXACT
+
+
 def test_step_is_deterministic(pkg):
     specs = [wl.ParamSpec("a", (200, 640)), wl.ParamSpec("b", (640, 200))]
     outs = []
@@ -243,6 +260,11 @@ def test_step_rejects_bad_arguments(pkg):
     assert e.value.status == 1
     with pytest.raises(ValueError):
         pkg.muon_step([W], [W], [M.to(torch.bfloat16)], lr=0.02, wd=0.1)
+    with pytest.raises(pkg.MuonError) as e:
+        pkg.muon_step([W], [W], [M], lr=0.02, wd=0.1, extra_scale=float("inf"))
+    assert e.value.status == 1
+    with pytest.raises(ValueError):
+        pkg.muon_step([W], [W], [M], lr=0.02, wd=0.1, scale_mode="spectral")
     pkg.muon_step([], [], [], lr=0.02, wd=0.1)     # no-op
 
 

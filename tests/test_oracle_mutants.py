@@ -58,13 +58,37 @@ def test_update_scale_mutants_fail_rms_pin(monkeypatch):
     W = np.zeros(shape)
     G = np.random.default_rng(2).standard_normal(shape) + 4 * np.eye(*shape)
     newton = tuple(GOLD["newton_cubic"]["value"])
-    for bad in (lambda s, r=0.2: r * math.sqrt(min(s[0], s[1])),
-                lambda s, r=0.2: math.sqrt(max(s[0], s[1])),
-                lambda s, r=0.2: r * max(s[0], s[1])):
+    for bad in (lambda s, r=0.2, *_: r * math.sqrt(min(s[0], s[1])),
+                lambda s, r=0.2, *_: math.sqrt(max(s[0], s[1])),
+                lambda s, r=0.2, *_: r * max(s[0], s[1])):
         monkeypatch.setattr(mo, "update_scale", bad)
         Wn, _ = mo.muon_step(W, G, np.zeros(shape), lr=0.02, wd=0.0, steps=80, coeffs=newton)
         rms = math.sqrt(np.mean((Wn - W) ** 2)) / 0.02
         assert abs(rms - 0.2) > 1e-3
+
+
+def test_mup_scale_mutants_fail_rms_to_rms_pin(monkeypatch):
+    # inverted ratio, RMS-mode factor, or no square root: the update's
+    # RMS -> RMS operator norm is no longer 1 on a non-square parameter
+    newton = tuple(GOLD["newton_cubic"]["value"])
+    real = mo.update_scale
+    for bad_base in (lambda A, B: math.sqrt(B / A), lambda A, B: 0.2 * math.sqrt(max(A, B)), lambda A, B: A / B):
+        def bad(shape, update_rms=0.2, mode="rms", extra=1.0, f=bad_base):
+            if mode == "mup":
+                return extra * f(int(shape[0]), int(shape[1]))
+            return real(shape, update_rms, mode, extra)
+        monkeypatch.setattr(mo, "update_scale", bad)
+        for shape in ((24, 96), (96, 24)):
+            G = np.random.default_rng(4).standard_normal(shape)
+            Wn, _ = mo.muon_step(np.zeros(shape), G, np.zeros(shape), lr=0.02, wd=0.0, steps=80, coeffs=newton,
+                                 scale_mode="mup")
+            D = (Wn / -0.02)
+            norm = math.sqrt(shape[1] / shape[0]) * np.linalg.svd(D, compute_uv=False)[0]
+            if abs(norm - 1.0) > 1e-3:
+                break
+        else:
+            raise AssertionError("mutant passed the RMS->RMS pin")
+    monkeypatch.undo()
 
 
 def test_nesterov_and_decay_mutants_fail_pins(monkeypatch):
@@ -81,7 +105,7 @@ def test_nesterov_and_decay_mutants_fail_pins(monkeypatch):
     assert rel(U, G * (1 - mu ** 3) / (1 - mu)) > 1e-3
     monkeypatch.undo()
 
-    def no_decay(W, O, lr, wd, shape, update_rms=0.2):
+    def no_decay(W, O, lr, wd, shape, update_rms=0.2, *_):
         return np.asarray(W, np.float64) - lr * mo.update_scale(shape, update_rms) * O
     monkeypatch.setattr(mo, "apply_update", no_decay)
     W = np.random.default_rng(3).standard_normal((8, 12))

@@ -183,6 +183,44 @@ def test_update_rms_is_0p2_for_exact_msign(shape):
     assert np.sum((Wn - W) * msign_svd(G)) < 0     # a descent step along -msign
 
 
+@pytest.mark.parametrize("shape", [(48, 192), (192, 48), (80, 80)])
+def test_mup_update_has_unit_rms_to_rms_norm(shape):
+    # Chensy §Variation of Muon Optimizer: the dual of G under the RMS->RMS
+    # operator norm, ||A||_{RMS->RMS} = sqrt(d_in / d_out) ||A||_2, is the
+    # update of RMS->RMS norm 1, sqrt(d_out / d_in) msign(G).  With the weight
+    # stored (d_out, d_in) and O = msign (Newton cubic run to convergence),
+    # the muP step's direction must have that norm exactly, and be a descent
+    # direction along -msign(G).
+    d_out, d_in = shape
+    W = wl.weight(6, shape).astype(np.float64)
+    G = rand(7, shape)
+    lr = 0.02
+    Wn, _ = oracle.muon_step(W, G, np.zeros(shape), lr=lr, wd=0.0, steps=80,
+                             coeffs=tuple(GOLD["newton_cubic"]["value"]), scale_mode="mup")
+    D = (W - Wn) / lr
+    sig = np.linalg.svd(D, compute_uv=False)
+    assert abs(math.sqrt(d_in / d_out) * sig[0] - 1.0) < 1e-10
+    assert abs(sig[-1] - sig[0]) < 1e-10 * sig[0]          # every direction equally scaled
+    assert np.sum(D * msign_svd(G)) > 0
+
+
+@pytest.mark.parametrize("gamma", [0.18, 0.25])
+def test_deepseek_gamma_sets_the_update_rms(gamma):
+    # Chensy §Variation (DeepSeek-V4): O' sqrt(max(n, m)) gamma makes the
+    # update RMS gamma for an orthogonal O'; here gamma is update_rms, and
+    # the extra scale factor multiplies the step on top of it.
+    shape = (64, 160)
+    W = wl.weight(8, shape).astype(np.float64)
+    G = rand(9, shape)
+    lr = 0.02
+    for extra in (1.0, 1.5):
+        Wn, _ = oracle.muon_step(W, G, np.zeros(shape), lr=lr, wd=0.0, steps=80,
+                                 coeffs=tuple(GOLD["newton_cubic"]["value"]), update_rms=gamma,
+                                 extra_scale=extra)
+        rms = math.sqrt(np.mean((Wn - W) ** 2)) / lr
+        assert abs(rms - gamma * extra) < 1e-10
+
+
 def test_weight_decay_only_when_grad_zero():
     W = wl.weight(3, (8, 12)).astype(np.float64)
     Wn, Mn = oracle.muon_step(W, np.zeros((8, 12)), np.zeros((8, 12)), lr=0.02, wd=0.1)
