@@ -164,6 +164,10 @@ typedef struct {
   int32_t scale_mode;      /* muon_scale_mode_t */
   float update_rms;        /* MUON_SCALE_RMS factor (0.2); ignored by MUON_SCALE_MUP */
   float extra_scale;       /* multiplies the update in every mode (1.0) */
+  int32_t coeffs_per_step; /* 0: coeffs is one (a, b, c) used by every step; 1: coeffs holds ns_steps
+                              triples, step k uses coeffs[3k .. 3k+2] (a schedule such as the
+                              hybrid iteration of DeepSeek-V4: "Muon Optimizer and the Distributed
+                              Implementation", §Variation of Muon Optimizer) */
 } muon_step_options_t;
 
 /* muon_step with the update scale chosen by opts (host struct, read during

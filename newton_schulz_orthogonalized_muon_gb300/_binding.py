@@ -50,7 +50,8 @@ class MuonStepOptionsC(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("wd", ctypes.c_float), ("mu", ctypes.c_float), ("nesterov", ctypes.c_int32),
                 ("ns_method", ctypes.c_int32), ("ns_steps", ctypes.c_int32),
                 ("coeffs", ctypes.POINTER(ctypes.c_float)), ("ns_dtype", ctypes.c_int32),
-                ("scale_mode", ctypes.c_int32), ("update_rms", ctypes.c_float), ("extra_scale", ctypes.c_float)]
+                ("scale_mode", ctypes.c_int32), ("update_rms", ctypes.c_float), ("extra_scale", ctypes.c_float),
+                ("coeffs_per_step", ctypes.c_int32)]
 
 
 _lib = None
@@ -252,7 +253,8 @@ def muon_step(params, grads, momenta, *, lr: float, wd: float, mu: float = 0.95,
     """One Muon step over lists of 2-D params (updated in place), grads and
     fp32 momentum buffers (updated in place).  scale_mode "rms":
     update_rms * sqrt(max(A, B)); "mup": sqrt(rows / cols); either times
-    extra_scale (muon_step_ex)."""
+    extra_scale (muon_step_ex).  coeffs: one (a, b, c), or a list of
+    ns_steps triples (a per-step schedule)."""
     n = len(params)
     if len(grads) != n or len(momenta) != n:
         raise ValueError("params, grads and momenta must have the same length")
@@ -276,9 +278,17 @@ def muon_step(params, grads, momenta, *, lr: float, wd: float, mu: float = 0.95,
     modes = {"rms": MUON_SCALE_RMS, "mup": MUON_SCALE_MUP}
     if scale_mode not in modes:
         raise ValueError(f"scale_mode must be one of {tuple(modes)}")
-    cf = _coeffs(coeffs)
+    per_step = coeffs is not None and len(coeffs) > 0 and hasattr(coeffs[0], "__len__")
+    if per_step:
+        # a schedule: one (a, b, c) per Newton-Schulz step
+        if len(coeffs) != int(ns_steps) or any(len(c) != 3 for c in coeffs):
+            raise ValueError("a coefficient schedule needs one (a, b, c) per step")
+        cf = (ctypes.c_float * (3 * len(coeffs)))(*[float(x) for c in coeffs for x in c])
+    else:
+        cf = _coeffs(coeffs)
     opts = MuonStepOptionsC(float(lr), float(wd), float(mu), 1 if nesterov else 0, _method(ns_method), int(ns_steps),
-                            cf, int(ns_dtype), modes[scale_mode], float(update_rms), float(extra_scale))
+                            ctypes.cast(cf, ctypes.POINTER(ctypes.c_float)), int(ns_dtype), modes[scale_mode],
+                            float(update_rms), float(extra_scale), 1 if per_step else 0)
     dev = params[0].device.index if n else None
     h = handle or default_handle(dev)
     st = h._lib.muon_step_ex(h.ptr, arr, n, ctypes.byref(opts), ctypes.c_void_p(_stream_ptr(stream)))

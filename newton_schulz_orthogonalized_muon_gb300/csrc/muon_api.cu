@@ -317,7 +317,7 @@ Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
 // All m x m iterates are polynomials in R_0, so they commute and are
 // symmetric: every product is computed on its upper tiles and mirrored.
 muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions& R, uint8_t* ws, uint8_t* dbase,
-                             int steps, float ca, float cb, float cc, bool tc, float mu, int nesterov,
+                             int steps, const float* coeffs, int coeff_stride, bool tc, float mu, int nesterov,
                              cudaStream_t stream) {
   float* xf = reinterpret_cast<float*>(ws + R.xf);
   __nv_bfloat16* xb = tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb0) : nullptr;
@@ -365,9 +365,6 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     p.m = g.m;
     p.n = g.n;
     p.batch = cnt;
-    p.ca = ca;
-    p.cb = cb;
-    p.cc = cc;
     p.ldm = g.ldm;
     p.ldx = g.ldx;
     p.out = out_d;
@@ -427,6 +424,9 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     int qcur = -1, qnext = SLOT_Q0;
     for (int k = 0; k < steps; ++k) {
       const int pk = SLOT_P0 + (k & 1);
+      q.ca = coeffs[k * coeff_stride];           // this step's (a, b, c)
+      q.cb = coeffs[k * coeff_stride + 1];
+      q.cc = coeffs[k * coeff_stride + 2];
       muon_status_t st = sym_product(MODE_G_P, SLOT_R, SLOT_R, pk, MUON_K_POLY);     // P = aI + bR + cR^2
       if (st != MUON_OK) return st;
       if (k == 0) {
@@ -465,11 +465,12 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
 }
 
 // Run prepare + Newton-Schulz + final write for every block.
+// coeffs: (a, b, c) of step k at coeffs[k * coeff_stride] (stride 0: one
+// triple for every step, 3: a schedule of `steps` triples).
 muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, float mu, int nesterov, int steps,
-                         const float* coeffs, int ns_method, bool tc, cudaStream_t stream) {
+                         const float* coeffs, int coeff_stride, int ns_method, bool tc, cudaStream_t stream) {
   if (blocks.empty()) return MUON_OK;
   const bool gram = (ns_method == MUON_NS_GRAM);
-  const float ca = coeffs[0], cb = coeffs[1], cc = coeffs[2];
 
   std::map<std::pair<int, int>, GroupPlan> groups;
   for (size_t i = 0; i < blocks.size(); ++i) {
@@ -545,7 +546,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     h->prof_tag = group_index++;
     const Regions R = regions(g, g.chunk, tc, gram, steps);
     if (gram) {
-      muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, ca, cb, cc, tc, mu, nesterov, stream);
+      muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, tc, mu, nesterov, stream);
       if (gst != MUON_OK) return gst;
       continue;
     }
@@ -606,9 +607,9 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         p.n = g.n;
         p.batch = cnt;
         p.scale = it == 0 ? scale : nullptr;
-        p.ca = ca;
-        p.cb = cb;
-        p.cc = cc;
+        p.ca = coeffs[it * coeff_stride];        // this iteration's (a, b, c)
+        p.cb = coeffs[it * coeff_stride + 1];
+        p.cc = coeffs[it * coeff_stride + 2];
         p.ldm = g.ldm;
         p.ldx = g.ldx;
         p.out = out_d;
@@ -833,7 +834,7 @@ muon_status_t muon_orthogonalize(muon_handle_t h, void* X, int32_t dtype, int64_
     bl.m = static_cast<int>(std::min(m, n));
     bl.n = static_cast<int>(std::max(m, n));
   }
-  return run_blocks(h, blocks, 0.f, 0, steps, cf, ns_method, dtype == MUON_BF16, static_cast<cudaStream_t>(stream));
+  return run_blocks(h, blocks, 0.f, 0, steps, cf, 0, ns_method, dtype == MUON_BF16, static_cast<cudaStream_t>(stream));
 }
 
 muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t n_params,
@@ -849,6 +850,15 @@ muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t 
   if (o.ns_steps < 0 || o.ns_steps > 100) return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 100]");
   if (o.scale_mode != MUON_SCALE_RMS && o.scale_mode != MUON_SCALE_MUP)
     return fail(h, MUON_ERR_INVALID_ARG, "unknown scale_mode");
+  if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
+    return fail(h, MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
+  if (o.coeffs_per_step && o.coeffs == nullptr && o.ns_steps > 0)
+    return fail(h, MUON_ERR_INVALID_ARG, "a coefficient schedule needs coeffs");
+  if (o.coeffs != nullptr) {
+    const int nc = 3 * (o.coeffs_per_step ? o.ns_steps : 1);
+    for (int k = 0; k < nc; ++k)
+      if (!std::isfinite(o.coeffs[k])) return fail(h, MUON_ERR_INVALID_ARG, "non-finite coefficient");
+  }
   if (!std::isfinite(o.lr) || !std::isfinite(o.wd) || !std::isfinite(o.mu) || !std::isfinite(o.update_rms) ||
       !std::isfinite(o.extra_scale))
     return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
@@ -894,8 +904,8 @@ muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t 
   if (blocks.empty()) return MUON_OK;
   DeviceGuard guard(h->device);
   const float* cf = o.coeffs ? o.coeffs : kDefaultCoeffs;
-  return run_blocks(h, blocks, o.mu, o.nesterov ? 1 : 0, o.ns_steps, cf, o.ns_method, o.ns_dtype == MUON_BF16,
-                    static_cast<cudaStream_t>(stream));
+  return run_blocks(h, blocks, o.mu, o.nesterov ? 1 : 0, o.ns_steps, cf, o.coeffs_per_step ? 3 : 0, o.ns_method,
+                    o.ns_dtype == MUON_BF16, static_cast<cudaStream_t>(stream));
 }
 
 muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_params, float lr, float wd,
@@ -913,6 +923,7 @@ muon_status_t muon_step(muon_handle_t h, const muon_param_t* params, int32_t n_p
   o.scale_mode = MUON_SCALE_RMS;
   o.update_rms = update_rms;
   o.extra_scale = 1.0f;
+  o.coeffs_per_step = 0;
   return muon_step_ex(h, params, n_params, &o, stream);
 }
 

@@ -85,11 +85,24 @@ def frobenius_normalize(X, eps: float = NORM_EPS):
     return X / (math.sqrt(float(np.sum(X * X))) + eps)
 
 
+def step_coeffs(coeffs, steps: int):
+    """The (a, b, c) of every step: one triple repeated, or a schedule of
+    ``steps`` triples (a hybrid iteration such as DeepSeek-V4's, whose last
+    steps use other coefficients: [Chensy] §Variation of Muon Optimizer)."""
+    if len(coeffs) == 3 and not hasattr(coeffs[0], "__len__"):
+        return [tuple(float(v) for v in coeffs)] * steps
+    sched = [tuple(float(v) for v in c) for c in coeffs]
+    if len(sched) != steps or any(len(c) != 3 for c in sched):
+        raise ValueError("a coefficient schedule needs one (a, b, c) per step")
+    return sched
+
+
 def newton_schulz(X, steps: int = NS_STEPS, coeffs=QUINTIC, eps: float = NORM_EPS):
     """Quintic Newton-Schulz orthogonalisation ("standard" method).
 
     phi(X) = (aI + b XX^T + c (XX^T)^2) X applied ``steps`` times to the
-    Frobenius-normalised input, evaluated in Horner form as
+    Frobenius-normalised input (``coeffs``: one (a, b, c), or one per step),
+    evaluated in Horner form as
     A = XX^T, B = bA + cA^2, X <- aX + BX ([Chensy] §Newton-Schulz
     Iteration; [DeepSpeed] §核心算子, zeropower_via_newtonschulz5).
 
@@ -97,13 +110,13 @@ def newton_schulz(X, steps: int = NS_STEPS, coeffs=QUINTIC, eps: float = NORM_EP
     Gram matrix) and the result is transposed back; phi commutes with
     transposition, so this changes cost only.
     """
-    a, b, c = (float(v) for v in coeffs)
+    sched = step_coeffs(coeffs, steps)
     X = _f64(X)
     transposed = X.shape[0] > X.shape[1]
     if transposed:
         X = X.T
     X = frobenius_normalize(X, eps)
-    for _ in range(steps):
+    for a, b, c in sched:
         A = X @ X.T
         B = b * A + c * (A @ A)
         X = a * X + B @ X
@@ -122,7 +135,7 @@ def gram_newton_schulz(X, steps: int = NS_STEPS, coeffs=QUINTIC, eps: float = NO
     the standard method in exact arithmetic.  No restarts (the page names
     none).  Rows > cols is handled by transposition as in newton_schulz.
     """
-    a, b, c = (float(v) for v in coeffs)
+    sched = step_coeffs(coeffs, steps)
     X = _f64(X)
     transposed = X.shape[0] > X.shape[1]
     if transposed:
@@ -132,7 +145,7 @@ def gram_newton_schulz(X, steps: int = NS_STEPS, coeffs=QUINTIC, eps: float = NO
     I = np.eye(m)
     R = X0 @ X0.T
     Q = I.copy()
-    for _ in range(steps):
+    for a, b, c in sched:
         P = a * I + b * R + c * (R @ R)
         Q = P @ Q
         R = P @ R @ P

@@ -88,19 +88,20 @@ def test_struct_layouts_match_the_c_compiler(tmp_path):
         "int main(void) { printf(\"%zu %zu %zu %zu %zu %zu %zu\\n\", sizeof(muon_param_t),"
         " offsetof(muon_param_t, scale_dim), sizeof(muon_step_options_t), offsetof(muon_step_options_t, coeffs),"
         " offsetof(muon_step_options_t, ns_dtype), offsetof(muon_step_options_t, update_rms),"
-        " offsetof(muon_step_options_t, extra_scale)); return 0; }\n")
+        " offsetof(muon_step_options_t, extra_scale)); printf(\"%zu\\n\", offsetof(muon_step_options_t, coeffs_per_step));"
+        " return 0; }\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
     want = [ctypes.sizeof(MuonParamC), MuonParamC.scale_dim.offset, ctypes.sizeof(MuonStepOptionsC),
             MuonStepOptionsC.coeffs.offset, MuonStepOptionsC.ns_dtype.offset, MuonStepOptionsC.update_rms.offset,
-            MuonStepOptionsC.extra_scale.offset]
+            MuonStepOptionsC.extra_scale.offset, MuonStepOptionsC.coeffs_per_step.offset]
     assert got == want
 
 
 def test_step_ex_rejects_bad_arguments_without_a_device(lib):
     from newton_schulz_orthogonalized_muon_gb300._binding import MuonStepOptionsC
-    opts = MuonStepOptionsC(0.02, 0.1, 0.95, 1, 0, 5, None, 1, 0, 0.2, 1.0)
+    opts = MuonStepOptionsC(0.02, 0.1, 0.95, 1, 0, 5, None, 1, 0, 0.2, 1.0, 0)
     assert lib.muon_step_ex(None, None, 0, ctypes.byref(opts), None) == 1
 
 

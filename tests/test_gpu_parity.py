@@ -233,6 +233,32 @@ def test_step_scale_modes(pkg, dtype, scale):
         assert rel(m_gpu, m_ref) < TOL_EXACT
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_step_coefficient_schedule(pkg, dtype, method):
+    # a hybrid 10-step iteration: 8 quintic steps, then 2 Newton cubic steps
+    sched = [oracle.QUINTIC] * 8 + [(1.5, -0.5, 0.0)] * 2
+    specs = [wl.ParamSpec("a", (128, 384)), wl.ParamSpec("b", (384, 128))]
+    W = [wl.weight(300 + i, s.shape) for i, s in enumerate(specs)]
+    G = [wl.lowrank_grad(310 + i, s.shape[0], s.shape[1], 16, scale=1.0) for i, s in enumerate(specs)]
+    Wd, Gd = [to_dev(w, dtype) for w in W], [to_dev(g, dtype) for g in G]
+    Md = [torch.zeros(s.shape, device="cuda") for s in specs]
+    W0 = [host64(w) for w in Wd]
+    pkg.muon_step(Wd, Gd, Md, lr=0.02, wd=0.1, ns_steps=10, coeffs=sched, ns_method=method)
+    torch.cuda.synchronize()
+    assert pkg.default_handle().check() == 0
+    for i, s_ in enumerate(specs):
+        w_ref, _ = oracle.muon_step(W0[i], host64(Gd[i]), np.zeros(s_.shape), lr=0.02, wd=0.1, steps=10,
+                                    coeffs=sched, method=method)
+        base = W0[i] * (1 - 0.02 * 0.1)
+        if dtype == torch.float32:
+            assert delta_err(host64(Wd[i]), w_ref, base) < TOL_F32
+        else:
+            assert delta_err_bf16(host64(Wd[i]), w_ref, base, 1) < TOL_BF16
+    with pytest.raises(ValueError):
+        pkg.muon_step(Wd, Gd, Md, lr=0.02, wd=0.1, ns_steps=5, coeffs=sched)
+
+
 def test_step_is_deterministic(pkg):
     specs = [wl.ParamSpec("a", (200, 640)), wl.ParamSpec("b", (640, 200))]
     outs = []

@@ -139,3 +139,18 @@ def test_gram_mutant_q_order_still_commutes_but_missing_p_fails():
         Q = P @ Q
         R = P @ R
     assert rel(Q @ X0, svd_closed_form(X, 5, QUINTIC)) > 1e-3
+
+
+def test_schedule_mutant_using_the_first_triple_fails_the_closed_form(monkeypatch):
+    # an oracle that ignored the schedule (every step with the first triple)
+    newton = tuple(GOLD["newton_cubic"]["value"])
+    sched = [mo.QUINTIC] * 8 + [newton] * 2
+    X = np.random.default_rng(13).standard_normal((16, 40))
+    monkeypatch.setattr(mo, "step_coeffs", lambda coeffs, steps: [tuple(coeffs[0])] * steps)
+    bad = mo.newton_schulz(X, steps=10, coeffs=sched)
+    monkeypatch.undo()
+    U, s, Vt = np.linalg.svd(X, full_matrices=False)
+    x = s / np.linalg.norm(X)
+    for a, b, c in sched:
+        x = a * x + b * x ** 3 + c * x ** 5
+    assert rel(bad, (U * x) @ Vt) > 1e-3

@@ -321,3 +321,42 @@ def test_flattened_grad_and_shape_scale():
     Wn, Mn = oracle.muon_step(W, G, np.zeros_like(G), lr=0.01, wd=0.0)
     O = oracle.newton_schulz(1.95 * G.reshape(6, 20))    # Nesterov, zero buffer: U = (1+mu) G
     assert rel((W - Wn).reshape(6, 20), 0.01 * 0.2 * math.sqrt(6) * O) < 1e-13
+
+
+# ------------------------------------------------ per-step coefficient schedules
+
+def svd_closed_form_schedule(X, schedule):
+    """As svd_closed_form, with step k moving each normalised singular value by
+    its own odd quintic g_k(x) = a_k x + b_k x^3 + c_k x^5 (applied in order)."""
+    X = np.asarray(X, np.float64)
+    U, s, Vt = np.linalg.svd(X, full_matrices=False)
+    x = s / np.linalg.norm(X)
+    for a, b, c in schedule:
+        x = a * x + b * x ** 3 + c * x ** 5
+    return (U * x) @ Vt
+
+
+HYBRID = [QUINTIC] * 8 + [tuple(GOLD["newton_cubic"]["value"])] * 2
+
+
+@pytest.mark.parametrize("shape", [(16, 40), (40, 16), (24, 24)])
+@pytest.mark.parametrize("method", ["standard", "gram"])
+def test_hybrid_schedule_matches_composed_closed_form(shape, method):
+    # Chensy §Variation of Muon Optimizer (DeepSeek-V4): 8 steps with the
+    # quintic's magic numbers, then steps with other coefficients; here the
+    # last two are the Newton cubic of §Sign of a Matrix.  The singular
+    # values follow the composition of the per-step scalar maps.
+    X = rand(11, shape)
+    got = oracle.orthogonalize(X, steps=10, coeffs=HYBRID, method=method, eps=0.0)
+    assert rel(got, svd_closed_form_schedule(X, HYBRID)) < 1e-11
+    # the polynomials do not commute: reversing the schedule changes the result
+    assert rel(got, svd_closed_form_schedule(X, HYBRID[::-1])) > 1e-3
+
+
+def test_hybrid_newton_tail_tightens_the_singular_values():
+    # the Newton tail pulls every singular value of the quintic's output
+    # toward 1 (g_N(x) = 1.5x - 0.5x^3 has g_N(1) = 1 and g_N'(1) = 0)
+    X = rand(12, (32, 96))
+    plain = np.linalg.svd(oracle.newton_schulz(X, steps=8), compute_uv=False)
+    hybrid = np.linalg.svd(oracle.newton_schulz(X, steps=10, coeffs=HYBRID), compute_uv=False)
+    assert np.max(np.abs(hybrid - 1)) < 0.5 * np.max(np.abs(plain - 1))
