@@ -69,7 +69,7 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;            // one plane of the A tile
   static constexpr int B_BYTES = BN * BK * 2;            // one plane of the B tile
   static constexpr int STAGE_BYTES = AP * A_BYTES + BP * B_BYTES;
-  static constexpr int EPI_BYTES = EpiLayout<MODE>::BYTES;
+  static constexpr int EPI_BYTES = EpiLayout<MODE>::BYTES + SymEpi<MODE>::BYTES;
   static constexpr int BAR_BYTES = 512;
   // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
   static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tma_prefetch_map(&map_xh);
       tma_prefetch_map(&map_xl);
     }
-    if (MODE == MODE_UPDATE) tma_prefetch_map(&map_xo);
+    if (MODE == MODE_UPDATE || SymEpi<MODE>::kTma) tma_prefetch_map(&map_xo);
   }
   tc_fence_before();
   __syncthreads();
@@ -240,8 +240,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       umma_commit(drain);
       mbar_wait_bounded(drain, 0, nullptr, DRAIN_NS);
     }
+  } else if constexpr (SymEpi<MODE>::kTma) {
+    // --------------------------------------------------------- epilogue
+    // SYRK / POLY: blocks staged in shared memory, TMA bulk stores (map_xo
+    // carries the output matrix's 32 x 32 map)
+    EpiTiles et{};
+    et.t0 = blockIdx.x;
+    et.tstep = gridDim.x;
+    et.row_off = 0;
+    et.remote = false;
+    et.tempty = tempty;
+    sym_epilogue<MODE, BN, BM>(p, &map_xo, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp, lane);
   } else if constexpr (kSym) {
     // --------------------------------------------------------- epilogue
+    // Gram products (plane outputs): per-thread rows from registers
     // warps 2-9: TMEM lane quadrant = warp % 4 (hardware rule), column half =
     // (warp - 2) / 4; each thread owns one output row of its half.
     const int quad = warp & 3;
@@ -289,7 +301,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     et.row_off = 0;
     et.remote = false;
     et.tempty = tempty;
-    mn_epilogue<MODE, BN, BM>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES, xfull + 2 * (warp - 2),
+    mn_epilogue<MODE, BN, BM, 2>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES, xfull + 2 * (warp - 2),
                               tfull, et, abort, tmem_base, warp, lane);
   }
 
@@ -321,18 +333,18 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
 }  // namespace
 
 cudaError_t launch_ns_gemm_tc(int mode, int bn, const CUtensorMap& ma, const CUtensorMap& mb,
-                              const NsGemmParams& p, int grid, cudaStream_t s) {
+                              const CUtensorMap& mso, const NsGemmParams& p, int grid, cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   if (bn == 256) {
     switch (mode) {
-      case MODE_SYRK: return launch_one<MODE_SYRK, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
-      case MODE_POLY: return launch_one<MODE_POLY, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
+      case MODE_SYRK: return launch_one<MODE_SYRK, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
+      case MODE_POLY: return launch_one<MODE_POLY, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
       case MODE_G_R0: return launch_one<MODE_G_R0, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
     }
   } else if (bn == 128) {
     switch (mode) {
-      case MODE_SYRK: return launch_one<MODE_SYRK, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
-      case MODE_POLY: return launch_one<MODE_POLY, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
+      case MODE_SYRK: return launch_one<MODE_SYRK, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
+      case MODE_POLY: return launch_one<MODE_POLY, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
       case MODE_G_R0: return launch_one<MODE_G_R0, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
     }
   }

@@ -6,7 +6,7 @@
 //   * each CTA loads its own 128 rows of the A operand and its half (128 of
 //     256 columns) of the B operand per K step, 32 KB per stage instead of
 //     the 48 KB a single CTA needs for a 128 x 256 tile, so six stages (five
-//     beside the UPDATE / FINAL epilogue buffers) fit in shared memory and
+//     beside FINAL's epilogue buffers) fit in shared memory and
 //     each SM pulls a third less data through L2;
 //   * the leader CTA (cluster rank 0) issues tcgen05.mma.cta_group::2
 //     (M = 256 across the pair, N = 256, K = 16); the hardware reads the
@@ -29,13 +29,20 @@ using namespace tc;
 
 constexpr int PBM = 256;       // rows of the pair's tile (128 per CTA)
 constexpr int PBN = 256;       // columns of the tile = N of the pair MMA (128 loaded per CTA)
+// UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
+// 4 KB slot, which leaves room for six main-loop stages; FINAL keeps two
+// (five stages), as one slot costs it register spills.
+template <int MODE>
+struct PairSlots {
+  static constexpr int v = MODE == MODE_FINAL ? 2 : 1;
+};
 
 template <int MODE, int AP, int BP>
 struct PairCfg {
   static constexpr int A_BYTES = 128 * BK * 2;           // one plane of this CTA's 128 rows of A
   static constexpr int B_BYTES = 128 * BK * 2;           // one plane of this CTA's half of B
   static constexpr int STAGE_BYTES = AP * A_BYTES + BP * B_BYTES;   // 32 KB with one plane each
-  static constexpr int EPI_BYTES = EpiLayout<MODE>::BYTES;
+  static constexpr int EPI_BYTES = EpiLayout<MODE, PairSlots<MODE>::v>::BYTES + SymEpi<MODE>::BYTES;
   static constexpr int BAR_BYTES = 512;
   // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
   static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -52,7 +59,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                         const __grid_constant__ CUtensorMap map_xh, const __grid_constant__ CUtensorMap map_xl,
                         const __grid_constant__ CUtensorMap map_xo, const NsGemmParams p) {
   using C = PairCfg<MODE, AP, BP>;
-  using L = EpiLayout<MODE>;
+  using L = EpiLayout<MODE, PairSlots<MODE>::v>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
   static_assert(MODE != MODE_G_FINAL, "G_FINAL runs on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
@@ -99,7 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       tma_prefetch_map(&map_xh);
       tma_prefetch_map(&map_xl);
     }
-    if (MODE == MODE_UPDATE) tma_prefetch_map(&map_xo);
+    if (MODE == MODE_UPDATE || SymEpi<MODE>::kTma) tma_prefetch_map(&map_xo);
   }
   tc_fence_before();
   cluster_sync_all();      // the peer's barriers are initialised and TMEM is allocated in both CTAs
@@ -211,8 +218,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       umma_commit_pair_mc(drain, 0x1);
       mbar_wait_bounded(drain, 0, nullptr, DRAIN_NS);
     }
+  } else if constexpr (SymEpi<MODE>::kTma) {
+    // --------------------------------------------------------- epilogue
+    // SYRK / POLY: each CTA stages its 128 rows of the tile block by block
+    // and writes them (and their mirror) with TMA bulk stores
+    EpiTiles et{};
+    et.t0 = pair;
+    et.tstep = npairs;
+    et.row_off = static_cast<int>(rank) * 128;
+    et.remote = true;
+    et.tempty = nullptr;
+    et.tempty_remote[0] = mapa_shared(smem_u32(&tempty[0]), 0);
+    et.tempty_remote[1] = mapa_shared(smem_u32(&tempty[1]), 0);
+    sym_epilogue<MODE, PBN, PBM>(p, &map_xo, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp,
+                                 lane);
   } else if constexpr (ModeTraits<MODE>::kSym) {
     // --------------------------------------------------------- epilogue
+    // Gram products (plane outputs): per-thread rows from registers
     // warps 2-9: TMEM lane quadrant = warp % 4 (hardware rule), column half =
     // (warp - 2) / 4; each thread owns one output row of its half.
     const int quad = warp & 3;
@@ -267,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     et.tempty = nullptr;
     et.tempty_remote[0] = mapa_shared(smem_u32(&tempty[0]), 0);
     et.tempty_remote[1] = mapa_shared(smem_u32(&tempty[1]), 0);
-    mn_epilogue<MODE, PBN, PBM>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES,
+    mn_epilogue<MODE, PBN, PBM, PairSlots<MODE>::v>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES,
                                 xfull + 2 * (warp - 2), tfull, et, abort, tmem_base, warp, lane);
   }
 
@@ -332,12 +354,12 @@ int ns_gemm_pair_max_pairs() {
   return cached;
 }
 
-cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& a, const CUtensorMap& b, const NsGemmParams& p,
-                               int pairs, cudaStream_t s) {
+cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& so,
+                               const NsGemmParams& p, int pairs, cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   switch (mode) {
-    case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
-    case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
+    case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b, b, b, so, p, pairs, s);
+    case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b, b, b, so, p, pairs, s);
     case MODE_G_R0: return launch_pair<MODE_G_R0, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
   }
   return cudaErrorInvalidValue;

@@ -387,13 +387,13 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
         r0.num_tiles = cnt * g.tri256_count;
         r0.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
         const int pairs = std::min(r0.num_tiles, h->max_pairs);
-        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_G_R0, map_x, map_x, r0, pairs, stream), "gram r0");
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_G_R0, map_x, map_x, map_x, r0, pairs, stream), "gram r0");
       } else if (tc) {
         r0.tiles_per_mat = g.tri_count;
         r0.num_tiles = cnt * g.tri_count;
         r0.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
         const int grid = std::min(r0.num_tiles, h->num_sms);
-        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_G_R0, g.bn_sym, map_x, map_x, r0, grid, stream), "gram r0");
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_G_R0, g.bn_sym, map_x, map_x, map_x, r0, grid, stream), "gram r0");
       } else {
         r0.xf_in = xf;
         MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_G_R0, r0, stream, 1), "gram r0");
@@ -561,7 +561,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     float* scale = reinterpret_cast<float*>(ws + R.scale);
 
     __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(ws + R.xlo) : nullptr;
-    CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl;
+    CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
     if (tc && steps > 0) {
       if (!encode_map(h, &map_x[0], xb[0], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &map_x[1], xb[1], g.n, g.m, g.chunk, g.ldx) ||
@@ -569,7 +569,9 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm) ||
           !encode_box32(h->encode, &map_xh[0], xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
           !encode_box32(h->encode, &map_xh[1], xb[1], false, g.n, g.m, g.chunk, g.ldx) ||
-          !encode_box32(h->encode, &map_xl, xlo, false, g.n, g.m, g.chunk, g.ldx))
+          !encode_box32(h->encode, &map_xl, xlo, false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_box32(h->encode, &map_sa, symA, false, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_box32(h->encode, &map_sb, symB, false, g.m, g.m, g.chunk, g.ldm))
         return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
     const int mi = static_cast<int>(ceil_div(g.m, 128));
@@ -625,12 +627,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
           q.sym_out = symA;
           const int pairs = std::min(q.num_tiles, h->max_pairs);
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], q, pairs, stream),
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], map_sa, q, pairs, stream),
                       "syrk launch");
           q.scale = nullptr;
           q.sym_in = symA;
           q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, q, pairs, stream), "poly launch");
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, q, pairs, stream), "poly launch");
           NsGemmParams u = p;
           if (h->pair_update) {
             const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
@@ -660,13 +662,13 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
           q.sym_out = symA;
           int grid = std::min(q.num_tiles, h->num_sms);
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], q, grid, stream),
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], map_sa, q, grid, stream),
                       "syrk launch");
           // POLY: P = a I + b A + c A A
           q.scale = nullptr;
           q.sym_in = symA;
           q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, q, grid, stream), "poly launch");
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, map_sb, q, grid, stream), "poly launch");
           // UPDATE / FINAL: X = s (P^ X^ + P_rr X - P^_rr X^)
           NsGemmParams u = p;
           u.mi = mi;

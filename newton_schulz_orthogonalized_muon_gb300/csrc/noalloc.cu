@@ -178,12 +178,14 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
     ApplyParams ap{out_d, scale, xf, ldx, M, N};
     return launch_apply(ap, 1, stream) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
   }
-  CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl;
+  CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
   if (tc && !(encode_map(S->encode, &map_x[0], xb0, N, M, ldx) && encode_map(S->encode, &map_x[1], xb1, N, M, ldx) &&
               encode_map(S->encode, &map_A, symA, M, M, ldm) && encode_map(S->encode, &map_B, symB, M, M, ldm) &&
               encode_box32(S->encode, &map_xh[0], xb0, false, N, M, 1, ldx) &&
               encode_box32(S->encode, &map_xh[1], xb1, false, N, M, 1, ldx) &&
-              encode_box32(S->encode, &map_xl, xlo, false, N, M, 1, ldx)))
+              encode_box32(S->encode, &map_xl, xlo, false, N, M, 1, ldx) &&
+              encode_box32(S->encode, &map_sa, symA, false, M, M, 1, ldm) &&
+              encode_box32(S->encode, &map_sb, symB, false, M, M, 1, ldm)))
     return MUON_ERR_CUDA;
   const int mi = (M + 127) / 128, nj = (N + bn_upd - 1) / bn_upd;
   for (int it = 0; it < steps; ++it) {
@@ -210,12 +212,12 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
       q.tri = tri_d;
       q.sym_out = symA;
       const int gs = q.num_tiles < S->num_sms ? q.num_tiles : S->num_sms;
-      e = launch_ns_gemm_tc(MODE_SYRK, bn_sym, map_x[it & 1], map_x[it & 1], q, gs, stream);
+      e = launch_ns_gemm_tc(MODE_SYRK, bn_sym, map_x[it & 1], map_x[it & 1], map_sa, q, gs, stream);
       if (e != cudaSuccess) return MUON_ERR_CUDA;
       q.scale = nullptr;
       q.sym_in = symA;
       q.sym_out = symB;
-      e = launch_ns_gemm_tc(MODE_POLY, bn_sym, map_A, map_A, q, gs, stream);
+      e = launch_ns_gemm_tc(MODE_POLY, bn_sym, map_A, map_A, map_sb, q, gs, stream);
       if (e != cudaSuccess) return MUON_ERR_CUDA;
       NsGemmParams u = p;
       u.mi = mi;

@@ -166,7 +166,7 @@ __device__ __forceinline__ void epilogue_sym(const NsGemmParams& p, int b, int g
 // lane quadrant) and half of the tile's columns, which it walks in 32 x 32
 // blocks.  Per warp, in shared memory, SLOTS slots of 4 KB:
 //   UPDATE / FINAL: [hi 32 x 32 bf16 | lo 32 x 32 bf16], 64-byte rows with
-//   64-byte swizzle, loaded by TMA up to two blocks ahead (across tile
+//   64-byte swizzle, loaded by TMA up to SLOTS blocks ahead (across tile
 //   boundaries) so the loads overlap the main loop.  UPDATE writes the new
 //   hi and lo back in place and stores both with TMA (hi to the other
 //   operand buffer, lo in place).
@@ -177,11 +177,11 @@ __device__ __forceinline__ void epilogue_sym(const NsGemmParams& p, int b, int g
 //   destination row.
 // With the swizzles, one lane per row accessing 16-byte chunks of its row,
 // and eight lanes covering one row, are free of bank conflicts.
-template <int MODE>
+template <int MODE, int XSLOTS = 2>
 struct EpiLayout {
   static constexpr bool kMN = ModeTraits<MODE>::kMN;
   static constexpr bool kLoadX = (MODE == MODE_UPDATE || MODE == MODE_FINAL);
-  static constexpr int SLOTS = kLoadX ? 2 : 1;
+  static constexpr int SLOTS = kLoadX ? XSLOTS : 1;        // input blocks in flight per warp
   static constexpr int SLOT_BYTES = 4096;
   static constexpr int LO_OFF = 2048;                 // lo plane within a slot
   static constexpr int WARP_BYTES = SLOTS * SLOT_BYTES;   // a multiple of 1024
@@ -325,12 +325,12 @@ struct EpiTiles {
 // lo plane (read and written in place), map_xo = hi plane written for the
 // next iteration.  On return (also after a timeout, already recorded) the
 // warp's loads have landed and its stores have completed.
-template <int MODE, int BN, int TROWS>
+template <int MODE, int BN, int TROWS, int XSLOTS>
 __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtensorMap* map_xh,
                                             const CUtensorMap* map_xl, const CUtensorMap* map_xo, uint8_t* wbuf,
                                             uint64_t* xfull, uint64_t* tfull, const EpiTiles& et, volatile int* abort,
                                             uint32_t tmem_base, int warp, int lane) {
-  using L = EpiLayout<MODE>;
+  using L = EpiLayout<MODE, XSLOTS>;
   constexpr int NB = BN / 64;                          // 32-column blocks per warp per tile
   const int quad = warp & 3;
   const int cbeg = ((warp - 2) >> 2) * (BN / 2);
@@ -347,7 +347,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
       const int nb = g0 >= p.n ? 0 : min(NB, (p.n - g0 + 31) >> 5);
       if (pf_blk < nb) {
         if (lane == 0) {
-          const int slot = static_cast<int>(issued & 1u);
+          const int slot = static_cast<int>(issued % L::SLOTS);
           const uint32_t dst = wsm + slot * L::SLOT_BYTES;
           const int x = g0 + 32 * pf_blk, y = i * TROWS + et.row_off + quad * 32;
           mbar_arrive_expect_tx(&xfull[slot], L::SLOT_BYTES);
@@ -363,8 +363,8 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
     }
   };
   if (L::kLoadX) {
-    issue_next();
-    issue_next();
+#pragma unroll
+    for (int k = 0; k < L::SLOTS; ++k) issue_next();
   }
 
   bool ok = true;
@@ -403,9 +403,9 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
 #pragma unroll 1
     for (int k = 0; k < nb; ++k) {
       const int gcb = g0 + 32 * k;
-      const int slot = L::kLoadX ? static_cast<int>(done & 1u) : 0;
+      const int slot = L::kLoadX ? static_cast<int>(done % L::SLOTS) : 0;
       uint8_t* sbuf = wbuf + slot * L::SLOT_BYTES;
-      if (L::kLoadX && !mbar_wait_warp(&xfull[slot], (done >> 1) & 1u, abort, p.timeout_ns)) {
+      if (L::kLoadX && !mbar_wait_warp(&xfull[slot], (done / L::SLOTS) & 1u, abort, p.timeout_ns)) {
         if (lane == 0) raise_timeout(abort, p.err);
         ok = false;
         break;
@@ -523,9 +523,171 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   // stores complete
   if (lane == 0) {
     for (uint32_t u = done; u < issued; ++u)
-      mbar_wait_bounded(&xfull[u & 1u], (u >> 1) & 1u, nullptr, DRAIN_NS);
+      mbar_wait_bounded(&xfull[u % L::SLOTS], (u / L::SLOTS) & 1u, nullptr, DRAIN_NS);
     if (MODE == MODE_UPDATE) bulk_wait_all();
   }
+  __syncwarp();
+}
+
+// ------------------------------------------------ SYRK / POLY epilogue (TMA)
+// Each epilogue warp owns 32 rows and half of the tile's columns and walks
+// them in 32 x 32 blocks.  A block entirely below the diagonal is skipped
+// (the block above writes it as its mirror).  Per warp, 4 KB of shared
+// memory: [out | mirror], two 32 x 32 bf16 blocks with 64-byte rows and
+// 64-byte swizzle.  An off-diagonal block goes out at (r, c) and, through
+// the mirror buffer, transposed at (c, r); a diagonal block is assembled
+// symmetric in the out buffer from its c >= r half (every element written
+// once, so A and P are exactly symmetric).  Both leave by TMA bulk stores,
+// clipped at the m x m edge.  POLY's b*A term reads the block's rows of A
+// with 16-byte loads issued one block ahead.
+constexpr int SYM_WARP_BYTES = 4096;
+
+template <int MODE>
+struct SymEpi {
+  static constexpr bool kTma = (MODE == MODE_SYRK || MODE == MODE_POLY);
+  static constexpr int BYTES = kTma ? EPI_WARPS * SYM_WARP_BYTES : 0;
+};
+
+// byte offset of bf16 element (r, c) of a 32 x 32 block, 64-byte rows, 64-byte swizzle
+__device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_off(r, c >> 3) + 2u * (c & 7); }
+
+// 32 bf16 of one row from column gc (zeros at and beyond column m), raw
+__device__ __forceinline__ void load_row32_bf16(const __nv_bfloat16* rowp, int gc, int m, uint4* a) {
+  if (gc + 31 < m) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a[q] = *reinterpret_cast<const uint4*>(rowp + gc + 8 * q);
+  } else {
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float lo = gc + 2 * e < m ? bf2f(rowp[gc + 2 * e]) : 0.f;
+      const float hi = gc + 2 * e + 1 < m ? bf2f(rowp[gc + 2 * e + 1]) : 0.f;
+      w[e] = pack_bf16x2(lo, hi);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+// The tile loop of one epilogue warp for SYRK / POLY.  map_so: the output
+// (A or P, bf16 [batch][m][ldm]) with 32 x 32 boxes, 64-byte swizzle.
+template <int MODE, int BN, int TROWS>
+__device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtensorMap* map_so, uint8_t* wbuf,
+                                             uint64_t* tfull, const EpiTiles& et, volatile int* abort,
+                                             uint32_t tmem_base, int warp, int lane) {
+  constexpr int NB = BN / 64;                          // 32-column blocks per warp per tile
+  const int quad = warp & 3;
+  const int cbeg = ((warp - 2) >> 2) * (BN / 2);
+  const int m = p.m;
+  const uint32_t out_s = smem_u32(wbuf), mir_s = out_s + 2048;
+  bool pending = false;                                // a bulk store may still read the buffers
+  int acc = 0;
+  uint32_t acc_ph = 0;
+  uint4 apre[4];                                       // POLY: the next block's 32 values of A (raw bf16)
+  for (int t = et.t0; t < p.num_tiles; t += et.tstep) {
+    int b, i, j;
+    decode_tile<MODE>(p, t, b, i, j);
+    const int row0 = i * TROWS + et.row_off + quad * 32;
+    const int gr = row0 + lane;
+    const int g0 = j * BN + cbeg;
+    // first block of this warp that is not below the diagonal
+    int k0 = 0;
+    while (k0 < NB && g0 + 32 * k0 + 31 < row0) ++k0;
+    const __nv_bfloat16* arow = nullptr;
+    if (MODE == MODE_POLY) {
+      arow = reinterpret_cast<const __nv_bfloat16*>(p.sym_in) + (static_cast<size_t>(b) * m + (gr < m ? gr : 0)) * p.ldm;
+      if (k0 < NB && g0 + 32 * k0 < m && gr < m) load_row32_bf16(arow, g0 + 32 * k0, m, apre);
+    }
+    if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
+      if (lane == 0) raise_timeout(abort, p.err);
+      break;
+    }
+    tc_fence_after();
+    float s = 1.f;
+    if (p.scale != nullptr) {
+      s = p.scale[b];
+      s = s * s;                                       // SYRK of the first iteration: s^2 X X^T
+    }
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + cbeg);
+#pragma unroll 1
+    for (int k = k0; k < NB; ++k) {
+      const int gcb = g0 + 32 * k;
+      if (gcb >= m) break;
+      float v[32];
+      tmem_ld16(tb + static_cast<uint32_t>(32 * k), v);
+      tmem_ld16(tb + static_cast<uint32_t>(32 * k + 16), v + 16);
+      const bool diag = (gcb == row0);
+      if (MODE == MODE_SYRK) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] *= s;
+      } else {
+        float a[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unpack8(apre[q], a + 8 * q);
+        // the next block's A, under this block's stores
+        if (k + 1 < NB && gcb + 32 < m && gr < m) load_row32_bf16(arow, gcb + 32, m, apre);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = fmaf(p.cb, a[c], p.cc * v[c]);
+        if (diag && gr < m) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c == lane) {
+              v[c] += p.ca;
+              p.pdiag[static_cast<size_t>(b) * m + gr] = v[c];
+            }
+        }
+      }
+      // the buffers are free once the previous block's bulk stores have read them
+      if (lane == 0 && pending) bulk_wait_read_all();
+      __syncwarp();
+      if (!diag) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 pk = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(out_s + sw64_off(lane, q)), "r"(pk.x),
+                       "r"(pk.y), "r"(pk.z), "r"(pk.w)
+                       : "memory");
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const __nv_bfloat16 h = f2bf(v[c]);
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(mir_s + sw64_elem(c, lane)),
+                       "h"(*reinterpret_cast<const unsigned short*>(&h))
+                       : "memory");
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c >= lane) {
+            const __nv_bfloat16 h = f2bf(v[c]);
+            const unsigned short hb = *reinterpret_cast<const unsigned short*>(&h);
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(out_s + sw64_elem(lane, c)), "h"(hb) : "memory");
+            if (c > lane) asm volatile("st.shared.u16 [%0], %1;" ::"r"(out_s + sw64_elem(c, lane)), "h"(hb) : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && row0 < m) {
+        tma_store_3d(map_so, out_s, gcb, row0, b);
+        if (!diag) tma_store_3d(map_so, mir_s, row0, gcb, b);
+        bulk_commit_group();
+        pending = true;
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (et.remote)
+        mbar_arrive_cluster(et.tempty_remote[acc]);
+      else
+        mbar_arrive(&et.tempty[acc]);
+    }
+    acc ^= 1;
+    if (acc == 0) acc_ph ^= 1u;
+  }
+  if (lane == 0) bulk_wait_all();
   __syncwarp();
 }
 
