@@ -119,10 +119,13 @@ struct NsGemmParams {
 // BN: output tile width (128 or 256).  Maps are 3-D (x = column, y = row,
 // z = matrix) bf16 maps with a 64 x 64 box and 128-byte swizzle.
 // Operands with two planes (Gram modes) pass their lo-plane maps in a1 / b1.
-// SYRK / POLY: map_so is the output matrix (A or P) with 32 x 32 boxes
-// (encode_box32, bf16), written by TMA; G_R0 ignores it.
+// Symmetric products write their output through TMA: map_so is the output
+// matrix (A or P), or for G_R0 / G_P / G_PROD its hi plane, and map_so_lo
+// the lo plane (SYRK / POLY ignore it); bf16 with 32 x 32 boxes
+// (encode_box32).
 cudaError_t launch_ns_gemm_tc(int mode, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                              const CUtensorMap& map_so, const NsGemmParams& p, int grid, cudaStream_t s);
+                              const CUtensorMap& map_so, const CUtensorMap& map_so_lo, const NsGemmParams& p,
+                              int grid, cudaStream_t s);
 // UPDATE / FINAL: the master X is hi + lo, hi being the bf16 operand copy.
 // map_xh: hi plane of this iteration (= the B operand), map_xl: lo plane
 // (updated in place), map_xo: hi plane of the next iteration (UPDATE); all
@@ -131,19 +134,20 @@ cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& map_a,
                                      const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
                                      const NsGemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
-                                     const CUtensorMap& map_b0, const CUtensorMap& map_b1, const NsGemmParams& p,
-                                     int grid, cudaStream_t s);
+                                     const CUtensorMap& map_b0, const CUtensorMap& map_b1, const CUtensorMap& map_so,
+                                     const CUtensorMap& map_so_lo, const NsGemmParams& p, int grid, cudaStream_t s);
 // CTA-pair variant (tcgen05 cta_group::2, 256 x 256 tiles): `pairs`
 // clusters of two CTAs; tiles use 256-row blocks (p.tri / p.mi in 256-row
 // units) and, for UPDATE / FINAL, 256-column blocks.
 cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                               const CUtensorMap& map_so, const NsGemmParams& p, int pairs, cudaStream_t s);
+                               const CUtensorMap& map_so, const CUtensorMap& map_so_lo, const NsGemmParams& p,
+                               int pairs, cudaStream_t s);
 cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                       const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
                                       const NsGemmParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
-                                      const CUtensorMap& b0, const CUtensorMap& b1, const NsGemmParams& p, int pairs,
-                                      cudaStream_t s);
+                                      const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& so,
+                                      const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s);
 int ns_gemm_pair_max_pairs();
 
 // 3-D map {cols, rows, batch} (row stride ld elements, matrices rows * ld

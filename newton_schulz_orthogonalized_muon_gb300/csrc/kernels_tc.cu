@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tma_prefetch_map(&map_xl);
     }
     if (MODE == MODE_UPDATE || SymEpi<MODE>::kTma) tma_prefetch_map(&map_xo);
+    if (ModeTraits<MODE>::kPlanesOut) tma_prefetch_map(&map_xl);
   }
   tc_fence_before();
   __syncthreads();
@@ -242,57 +243,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else if constexpr (SymEpi<MODE>::kTma) {
     // --------------------------------------------------------- epilogue
-    // SYRK / POLY: blocks staged in shared memory, TMA bulk stores (map_xo
-    // carries the output matrix's 32 x 32 map)
+    // symmetric products: blocks staged in shared memory, TMA bulk stores
+    // (map_xo / map_xl carry the output's 32 x 32 maps: the matrix, or the
+    // hi / lo planes of a Gram-method matrix)
     EpiTiles et{};
     et.t0 = blockIdx.x;
     et.tstep = gridDim.x;
     et.row_off = 0;
     et.remote = false;
     et.tempty = tempty;
-    sym_epilogue<MODE, BN, BM>(p, &map_xo, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp, lane);
-  } else if constexpr (kSym) {
-    // --------------------------------------------------------- epilogue
-    // Gram products (plane outputs): per-thread rows from registers
-    // warps 2-9: TMEM lane quadrant = warp % 4 (hardware rule), column half =
-    // (warp - 2) / 4; each thread owns one output row of its half.
-    const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int ncols = p.m;
-    const int cbeg = half * (BN / 2), cend = cbeg + BN / 2;
-    int acc = 0;
-    uint32_t acc_ph = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      int b, i, j;
-      decode_tile<MODE>(p, t, b, i, j);
-      if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
-        if (lane == 0) raise_timeout(abort, p.err);
-        break;
-      }
-      tc_fence_after();
-      const int warp_row0 = i * BM + quad * 32;
-      const int gr = warp_row0 + lane;
-      float s = 1.f;
-      if (p.scale != nullptr) {
-        s = p.scale[b];
-        if (ModeTraits<MODE>::kKn) s = s * s;
-      }
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int c0 = cbeg; c0 < cend; c0 += 16) {
-        const int gc0 = j * BN + c0;
-        if (gc0 >= ncols) break;
-        if (gc0 + 15 < warp_row0) continue;  // below the diagonal
-        float v[16];
-        tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
-        epilogue_sym<MODE>(p, b, gr, gc0, v, s);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_ph ^= 1u;
-    }
+    sym_epilogue<MODE, BN, BM>(p, &map_xo, &map_xl, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp, lane);
   } else {
     // --------------------------------------------------------- epilogue
     EpiTiles et{};
@@ -333,19 +293,20 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
 }  // namespace
 
 cudaError_t launch_ns_gemm_tc(int mode, int bn, const CUtensorMap& ma, const CUtensorMap& mb,
-                              const CUtensorMap& mso, const NsGemmParams& p, int grid, cudaStream_t s) {
+                              const CUtensorMap& mso, const CUtensorMap& mso_lo, const NsGemmParams& p, int grid,
+                              cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   if (bn == 256) {
     switch (mode) {
       case MODE_SYRK: return launch_one<MODE_SYRK, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
       case MODE_POLY: return launch_one<MODE_POLY, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
-      case MODE_G_R0: return launch_one<MODE_G_R0, 256, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
+      case MODE_G_R0: return launch_one<MODE_G_R0, 256, 1, 1>(ma, ma, mb, mb, mb, mso_lo, mso, p, grid, s);
     }
   } else if (bn == 128) {
     switch (mode) {
       case MODE_SYRK: return launch_one<MODE_SYRK, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
       case MODE_POLY: return launch_one<MODE_POLY, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mso, p, grid, s);
-      case MODE_G_R0: return launch_one<MODE_G_R0, 128, 1, 1>(ma, ma, mb, mb, mb, mb, mb, p, grid, s);
+      case MODE_G_R0: return launch_one<MODE_G_R0, 128, 1, 1>(ma, ma, mb, mb, mb, mso_lo, mso, p, grid, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -370,19 +331,19 @@ cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& ma, co
 }
 
 cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& a0, const CUtensorMap& a1,
-                                     const CUtensorMap& b0, const CUtensorMap& b1, const NsGemmParams& p, int grid,
-                                     cudaStream_t s) {
+                                     const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& so,
+                                     const CUtensorMap& so_lo, const NsGemmParams& p, int grid, cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   if (bn == 128) {
     switch (mode) {
-      case MODE_G_P: return launch_one<MODE_G_P, 128, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, grid, s);
-      case MODE_G_PROD: return launch_one<MODE_G_PROD, 128, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, grid, s);
+      case MODE_G_P: return launch_one<MODE_G_P, 128, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
+      case MODE_G_PROD: return launch_one<MODE_G_PROD, 128, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
       case MODE_G_FINAL: return launch_one<MODE_G_FINAL, 128, 2, 1>(a0, a1, b0, b0, b0, b0, b0, p, grid, s);
     }
   } else if (bn == 256) {
     switch (mode) {
-      case MODE_G_P: return launch_one<MODE_G_P, 256, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, grid, s);
-      case MODE_G_PROD: return launch_one<MODE_G_PROD, 256, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, grid, s);
+      case MODE_G_P: return launch_one<MODE_G_P, 256, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
+      case MODE_G_PROD: return launch_one<MODE_G_PROD, 256, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
       case MODE_G_FINAL: return launch_one<MODE_G_FINAL, 256, 2, 1>(a0, a1, b0, b0, b0, b0, b0, p, grid, s);
     }
   }

@@ -107,6 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       tma_prefetch_map(&map_xl);
     }
     if (MODE == MODE_UPDATE || SymEpi<MODE>::kTma) tma_prefetch_map(&map_xo);
+    if (ModeTraits<MODE>::kPlanesOut) tma_prefetch_map(&map_xl);
   }
   tc_fence_before();
   cluster_sync_all();      // the peer's barriers are initialised and TMEM is allocated in both CTAs
@@ -220,8 +221,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     }
   } else if constexpr (SymEpi<MODE>::kTma) {
     // --------------------------------------------------------- epilogue
-    // SYRK / POLY: each CTA stages its 128 rows of the tile block by block
-    // and writes them (and their mirror) with TMA bulk stores
+    // symmetric products: each CTA stages its 128 rows of the tile block by
+    // block and writes them (and their mirror) with TMA bulk stores
     EpiTiles et{};
     et.t0 = pair;
     et.tstep = npairs;
@@ -230,52 +231,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     et.tempty = nullptr;
     et.tempty_remote[0] = mapa_shared(smem_u32(&tempty[0]), 0);
     et.tempty_remote[1] = mapa_shared(smem_u32(&tempty[1]), 0);
-    sym_epilogue<MODE, PBN, PBM>(p, &map_xo, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp,
+    sym_epilogue<MODE, PBN, PBM>(p, &map_xo, &map_xl, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp,
                                  lane);
-  } else if constexpr (ModeTraits<MODE>::kSym) {
-    // --------------------------------------------------------- epilogue
-    // Gram products (plane outputs): per-thread rows from registers
-    // warps 2-9: TMEM lane quadrant = warp % 4 (hardware rule), column half =
-    // (warp - 2) / 4; each thread owns one output row of its half.
-    const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int ncols = p.m;
-    const int cbeg = half * (PBN / 2), cend = cbeg + PBN / 2;
-    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
-    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
-    int acc = 0;
-    uint32_t acc_ph = 0;
-    for (int t = pair; t < p.num_tiles; t += npairs) {
-      int b, i, j;
-      decode_tile<MODE>(p, t, b, i, j);
-      if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
-        if (lane == 0) raise_timeout(abort, p.err);
-        break;
-      }
-      tc_fence_after();
-      const int warp_row0 = i * PBM + static_cast<int>(rank) * 128 + quad * 32;
-      const int gr = warp_row0 + lane;
-      float s = 1.f;
-      if (p.scale != nullptr) {
-        s = p.scale[b];
-        if (ModeTraits<MODE>::kKn) s = s * s;
-      }
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * PBN);
-#pragma unroll 1
-      for (int c0 = cbeg; c0 < cend; c0 += 16) {
-        const int gc0 = j * PBN + c0;
-        if (gc0 >= ncols) break;
-        if (gc0 + 15 < warp_row0) continue;  // below the diagonal
-        float v[16];
-        tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
-        epilogue_sym<MODE>(p, b, gr, gc0, v, s);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
-      acc ^= 1;
-      if (acc == 0) acc_ph ^= 1u;
-    }
   } else {
     // --------------------------------------------------------- epilogue
     // UPDATE / FINAL: each CTA drains its own 128 accumulator rows of the
@@ -355,12 +312,12 @@ int ns_gemm_pair_max_pairs() {
 }
 
 cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& so,
-                               const NsGemmParams& p, int pairs, cudaStream_t s) {
+                               const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   switch (mode) {
     case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b, b, b, so, p, pairs, s);
     case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b, b, b, so, p, pairs, s);
-    case MODE_G_R0: return launch_pair<MODE_G_R0, 1, 1>(a, a, b, b, b, b, b, p, pairs, s);
+    case MODE_G_R0: return launch_pair<MODE_G_R0, 1, 1>(a, a, b, b, b, so_lo, so, p, pairs, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -377,12 +334,12 @@ cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& a, const CUt
 }
 
 cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
-                                      const CUtensorMap& b0, const CUtensorMap& b1, const NsGemmParams& p, int pairs,
-                                      cudaStream_t s) {
+                                      const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& so,
+                                      const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s) {
   if (p.num_tiles == 0) return cudaSuccess;
   switch (mode) {
-    case MODE_G_P: return launch_pair<MODE_G_P, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, pairs, s);
-    case MODE_G_PROD: return launch_pair<MODE_G_PROD, 2, 2>(a0, a1, b0, b1, b0, b0, b0, p, pairs, s);
+    case MODE_G_P: return launch_pair<MODE_G_P, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, pairs, s);
+    case MODE_G_PROD: return launch_pair<MODE_G_PROD, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, pairs, s);
   }
   return cudaErrorInvalidValue;
 }

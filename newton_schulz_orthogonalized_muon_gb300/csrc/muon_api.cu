@@ -329,12 +329,15 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     hi[k] = ws + R.slot[k];
     lo[k] = tc ? static_cast<void*>(ws + R.slot_lo[k]) : nullptr;
   }
-  CUtensorMap map_x, mhi[kGramSlots], mlo[kGramSlots];
+  // per slot: 64 x 64 operand maps of both planes, and 32 x 32 output maps
+  CUtensorMap map_x, mhi[kGramSlots], mlo[kGramSlots], ohi[kGramSlots], olo[kGramSlots];
   if (tc) {
     bool ok = encode_map(h, &map_x, xb, g.n, g.m, g.chunk, g.ldx);
     for (int k = 0; k < kGramSlots && ok; ++k)
       ok = encode_map(h, &mhi[k], hi[k], g.m, g.m, g.chunk, g.ldm) &&
-           encode_map(h, &mlo[k], lo[k], g.m, g.m, g.chunk, g.ldm);
+           encode_map(h, &mlo[k], lo[k], g.m, g.m, g.chunk, g.ldm) &&
+           encode_box32(h->encode, &ohi[k], hi[k], false, g.m, g.m, g.chunk, g.ldm) &&
+           encode_box32(h->encode, &olo[k], lo[k], false, g.m, g.m, g.chunk, g.ldm);
     if (!ok) return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   }
   const int mi = static_cast<int>(ceil_div(g.m, 128));
@@ -387,13 +390,13 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
         r0.num_tiles = cnt * g.tri256_count;
         r0.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
         const int pairs = std::min(r0.num_tiles, h->max_pairs);
-        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_G_R0, map_x, map_x, map_x, r0, pairs, stream), "gram r0");
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_G_R0, map_x, map_x, ohi[SLOT_R], olo[SLOT_R], r0, pairs, stream), "gram r0");
       } else if (tc) {
         r0.tiles_per_mat = g.tri_count;
         r0.num_tiles = cnt * g.tri_count;
         r0.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
         const int grid = std::min(r0.num_tiles, h->num_sms);
-        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_G_R0, g.bn_sym, map_x, map_x, map_x, r0, grid, stream), "gram r0");
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_G_R0, g.bn_sym, map_x, map_x, ohi[SLOT_R], olo[SLOT_R], r0, grid, stream), "gram r0");
       } else {
         r0.xf_in = xf;
         MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_G_R0, r0, stream, 1), "gram r0");
@@ -411,10 +414,11 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
         t.num_tiles = cnt * g.tri256_count;
         t.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
         const int pairs = std::min(t.num_tiles, h->max_pairs);
-        MUON_LAUNCH(cls, launch_ns_gemm_pair_planes(mode, mhi[a], mlo[a], mhi[b], mlo[b], t, pairs, stream),
+        MUON_LAUNCH(cls, launch_ns_gemm_pair_planes(mode, mhi[a], mlo[a], mhi[b], mlo[b], ohi[out], olo[out], t, pairs, stream),
                     "gram product");
       } else if (tc) {
-        MUON_LAUNCH(cls, launch_ns_gemm_tc_planes(mode, 128, mhi[a], mlo[a], mhi[b], mlo[b], t, grid_sym, stream),
+        MUON_LAUNCH(cls, launch_ns_gemm_tc_planes(mode, 128, mhi[a], mlo[a], mhi[b], mlo[b], ohi[out], olo[out], t, grid_sym,
+                                                  stream),
                     "gram product");
       } else {
         MUON_LAUNCH(cls, launch_ns_gemm_simt(mode, t, stream, 1), "gram product");
@@ -454,7 +458,8 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
       f.num_tiles = cnt * mi * nj;
       const int grid = std::min(f.num_tiles, h->num_sms);
       MUON_LAUNCH(MUON_K_FINAL,
-                  launch_ns_gemm_tc_planes(MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur], map_x, map_x, f, grid, stream),
+                  launch_ns_gemm_tc_planes(MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur], map_x, map_x, map_x, map_x, f,
+                                           grid, stream),
                   "gram final");
     } else {
       f.xf_in = xf;
@@ -627,12 +632,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
           q.sym_out = symA;
           const int pairs = std::min(q.num_tiles, h->max_pairs);
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], map_sa, q, pairs, stream),
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, pairs, stream),
                       "syrk launch");
           q.scale = nullptr;
           q.sym_in = symA;
           q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, q, pairs, stream), "poly launch");
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream), "poly launch");
           NsGemmParams u = p;
           if (h->pair_update) {
             const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
@@ -662,13 +667,14 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
           q.sym_out = symA;
           int grid = std::min(q.num_tiles, h->num_sms);
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], map_sa, q, grid, stream),
+          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, grid,
+                                                         stream),
                       "syrk launch");
           // POLY: P = a I + b A + c A A
           q.scale = nullptr;
           q.sym_in = symA;
           q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, map_sb, q, grid, stream), "poly launch");
+          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, map_sb, map_sb, q, grid, stream), "poly launch");
           // UPDATE / FINAL: X = s (P^ X^ + P_rr X - P^_rr X^)
           NsGemmParams u = p;
           u.mi = mi;

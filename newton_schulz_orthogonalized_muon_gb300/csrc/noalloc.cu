@@ -212,12 +212,12 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
       q.tri = tri_d;
       q.sym_out = symA;
       const int gs = q.num_tiles < S->num_sms ? q.num_tiles : S->num_sms;
-      e = launch_ns_gemm_tc(MODE_SYRK, bn_sym, map_x[it & 1], map_x[it & 1], map_sa, q, gs, stream);
+      e = launch_ns_gemm_tc(MODE_SYRK, bn_sym, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, gs, stream);
       if (e != cudaSuccess) return MUON_ERR_CUDA;
       q.scale = nullptr;
       q.sym_in = symA;
       q.sym_out = symB;
-      e = launch_ns_gemm_tc(MODE_POLY, bn_sym, map_A, map_A, map_sb, q, gs, stream);
+      e = launch_ns_gemm_tc(MODE_POLY, bn_sym, map_A, map_A, map_sb, map_sb, q, gs, stream);
       if (e != cudaSuccess) return MUON_ERR_CUDA;
       NsGemmParams u = p;
       u.mi = mi;

@@ -61,104 +61,6 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
   }
 }
 
-// ------------------------------------------------------------ epilogues
-// v[16]: accumulator values of row gr, columns gc0 .. gc0+15.
-template <int MODE>
-__device__ __forceinline__ void epilogue_sym(const NsGemmParams& p, int b, int gr, int gc0, float* v, float s) {
-  const int m = p.m;
-  if (gr >= m) return;
-  const size_t mat = static_cast<size_t>(b) * m;
-  if (MODE == MODE_SYRK || MODE == MODE_G_R0) {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] *= s;
-  } else if (MODE == MODE_POLY || MODE == MODE_G_P) {
-    // v = b * A + c * acc (G_P: A = R = hi + lo planes, plus a on the diagonal)
-    const __nv_bfloat16* ain = reinterpret_cast<const __nv_bfloat16*>(p.sym_in) + (mat + gr) * p.ldm;
-    const __nv_bfloat16* alo =
-        MODE == MODE_G_P ? reinterpret_cast<const __nv_bfloat16*>(p.sym_in_lo) + (mat + gr) * p.ldm : nullptr;
-    float a[16];
-    if (gc0 + 15 < m) {
-      uint4 raw[2];
-      raw[0] = *reinterpret_cast<const uint4*>(ain + gc0);
-      raw[1] = *reinterpret_cast<const uint4*>(ain + gc0 + 8);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(raw);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 f = __bfloat1622float2(h[e]);
-        a[2 * e] = f.x;
-        a[2 * e + 1] = f.y;
-      }
-      if (MODE == MODE_G_P) {
-        raw[0] = *reinterpret_cast<const uint4*>(alo + gc0);
-        raw[1] = *reinterpret_cast<const uint4*>(alo + gc0 + 8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 f = __bfloat1622float2(h[e]);
-          a[2 * e] += f.x;
-          a[2 * e + 1] += f.y;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int gc = gc0 + e;
-        a[e] = gc < m ? bf2f(ain[gc]) + (MODE == MODE_G_P ? bf2f(alo[gc]) : 0.f) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      v[e] = fmaf(p.cb, a[e], p.cc * v[e]);
-      if (gc0 + e == gr) {
-        v[e] += p.ca;
-        if (MODE == MODE_POLY) p.pdiag[mat + gr] = v[e];
-      }
-    }
-  }
-  constexpr bool kPlanes = ModeTraits<MODE>::kPlanesOut;
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.sym_out);
-  __nv_bfloat16* outlo = kPlanes ? reinterpret_cast<__nv_bfloat16*>(p.sym_out_lo) : nullptr;
-  float lo[16];
-  if (kPlanes) {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) lo[e] = v[e] - bf2f(f2bf(v[e]));
-  }
-  __nv_bfloat16* row = out + (mat + gr) * p.ldm;
-  __nv_bfloat16* rowlo = kPlanes ? outlo + (mat + gr) * p.ldm : nullptr;
-  if (gc0 >= gr && gc0 + 15 < m) {
-    uint4 pk[2];
-    uint32_t* w = reinterpret_cast<uint32_t*>(pk);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-    *reinterpret_cast<uint4*>(row + gc0) = pk[0];
-    *reinterpret_cast<uint4*>(row + gc0 + 8) = pk[1];
-    if (kPlanes) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(lo[2 * e], lo[2 * e + 1]);
-      *reinterpret_cast<uint4*>(rowlo + gc0) = pk[0];
-      *reinterpret_cast<uint4*>(rowlo + gc0 + 8) = pk[1];
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int gc = gc0 + e;
-      if (gc >= gr && gc < m) {
-        row[gc] = f2bf(v[e]);
-        if (kPlanes) rowlo[gc] = f2bf(lo[e]);
-      }
-    }
-  }
-  // mirror below the diagonal: lanes hold consecutive rows, so each store
-  // of the warp covers 32 consecutive elements of row gc.
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const int gc = gc0 + e;
-    if (gc > gr && gc < m) {
-      out[(mat + gc) * p.ldm + gr] = f2bf(v[e]);
-      if (kPlanes) outlo[(mat + gc) * p.ldm + gr] = f2bf(lo[e]);
-    }
-  }
-}
-
 // ------------------------------------------- UPDATE / FINAL / G_FINAL epilogue
 // The master X of the tensor-core path is held as two bf16 planes, X = hi +
 // lo: hi = bf16(X) is the MMA operand copy itself, lo = bf16(X - hi) keeps
@@ -529,7 +431,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   __syncwarp();
 }
 
-// ------------------------------------------------ SYRK / POLY epilogue (TMA)
+// ------------------------------------------- symmetric-product epilogue (TMA)
 // Each epilogue warp owns 32 rows and half of the tile's columns and walks
 // them in 32 x 32 blocks.  A block entirely below the diagonal is skipped
 // (the block above writes it as its mirror).  Per warp, 4 KB of shared
@@ -538,13 +440,15 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
 // the mirror buffer, transposed at (c, r); a diagonal block is assembled
 // symmetric in the out buffer from its c >= r half (every element written
 // once, so A and P are exactly symmetric).  Both leave by TMA bulk stores,
-// clipped at the m x m edge.  POLY's b*A term reads the block's rows of A
-// with 16-byte loads issued one block ahead.
+// clipped at the m x m edge.  POLY's b*A term (G_P's b*R) reads the block's
+// rows of A (both planes of R) with 16-byte loads issued one block ahead.
+// Gram-method outputs leave as two planes, hi then lo, through the same
+// buffers.
 constexpr int SYM_WARP_BYTES = 4096;
 
 template <int MODE>
 struct SymEpi {
-  static constexpr bool kTma = (MODE == MODE_SYRK || MODE == MODE_POLY);
+  static constexpr bool kTma = ModeTraits<MODE>::kSym;
   static constexpr int BYTES = kTma ? EPI_WARPS * SYM_WARP_BYTES : 0;
 };
 
@@ -569,12 +473,18 @@ __device__ __forceinline__ void load_row32_bf16(const __nv_bfloat16* rowp, int g
   }
 }
 
-// The tile loop of one epilogue warp for SYRK / POLY.  map_so: the output
-// (A or P, bf16 [batch][m][ldm]) with 32 x 32 boxes, 64-byte swizzle.
+// The tile loop of one epilogue warp for the symmetric products.  map_so:
+// the output (A, P, or the hi plane of a Gram-method matrix; bf16
+// [batch][m][ldm]) with 32 x 32 boxes, 64-byte swizzle; map_so_lo: the lo
+// plane of a Gram-method output (value - bf16(value)), written after the hi
+// plane through the same buffers.
 template <int MODE, int BN, int TROWS>
-__device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtensorMap* map_so, uint8_t* wbuf,
-                                             uint64_t* tfull, const EpiTiles& et, volatile int* abort,
-                                             uint32_t tmem_base, int warp, int lane) {
+__device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtensorMap* map_so,
+                                             const CUtensorMap* map_so_lo, uint8_t* wbuf, uint64_t* tfull,
+                                             const EpiTiles& et, volatile int* abort, uint32_t tmem_base, int warp,
+                                             int lane) {
+  constexpr bool kPlanes = ModeTraits<MODE>::kPlanesOut;
+  constexpr bool kReadIn = (MODE == MODE_POLY || MODE == MODE_G_P);   // the b * A (b * R) term
   constexpr int NB = BN / 64;                          // 32-column blocks per warp per tile
   const int quad = warp & 3;
   const int cbeg = ((warp - 2) >> 2) * (BN / 2);
@@ -583,7 +493,8 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
   bool pending = false;                                // a bulk store may still read the buffers
   int acc = 0;
   uint32_t acc_ph = 0;
-  uint4 apre[4];                                       // POLY: the next block's 32 values of A (raw bf16)
+  uint4 apre[4];                                       // POLY / G_P: the next block's 32 values of A (R hi)
+  uint4 apre_lo[4];                                    // G_P: and of R's lo plane
   for (int t = et.t0; t < p.num_tiles; t += et.tstep) {
     int b, i, j;
     decode_tile<MODE>(p, t, b, i, j);
@@ -594,9 +505,15 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
     int k0 = 0;
     while (k0 < NB && g0 + 32 * k0 + 31 < row0) ++k0;
     const __nv_bfloat16* arow = nullptr;
-    if (MODE == MODE_POLY) {
-      arow = reinterpret_cast<const __nv_bfloat16*>(p.sym_in) + (static_cast<size_t>(b) * m + (gr < m ? gr : 0)) * p.ldm;
-      if (k0 < NB && g0 + 32 * k0 < m && gr < m) load_row32_bf16(arow, g0 + 32 * k0, m, apre);
+    const __nv_bfloat16* arow_lo = nullptr;
+    if (kReadIn) {
+      const size_t roff = (static_cast<size_t>(b) * m + (gr < m ? gr : 0)) * p.ldm;
+      arow = reinterpret_cast<const __nv_bfloat16*>(p.sym_in) + roff;
+      if (MODE == MODE_G_P) arow_lo = reinterpret_cast<const __nv_bfloat16*>(p.sym_in_lo) + roff;
+      if (k0 < NB && g0 + 32 * k0 < m && gr < m) {
+        load_row32_bf16(arow, g0 + 32 * k0, m, apre);
+        if (MODE == MODE_G_P) load_row32_bf16(arow_lo, g0 + 32 * k0, m, apre_lo);
+      }
     }
     if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
       if (lane == 0) raise_timeout(abort, p.err);
@@ -606,7 +523,7 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
     float s = 1.f;
     if (p.scale != nullptr) {
       s = p.scale[b];
-      s = s * s;                                       // SYRK of the first iteration: s^2 X X^T
+      s = s * s;                                       // SYRK / G_R0 of the first iteration: s^2 X X^T
     }
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + cbeg);
 #pragma unroll 1
@@ -617,15 +534,25 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
       tmem_ld16(tb + static_cast<uint32_t>(32 * k), v);
       tmem_ld16(tb + static_cast<uint32_t>(32 * k + 16), v + 16);
       const bool diag = (gcb == row0);
-      if (MODE == MODE_SYRK) {
+      if (MODE == MODE_SYRK || MODE == MODE_G_R0) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] *= s;
-      } else {
+      } else if (kReadIn) {
         float a[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) unpack8(apre[q], a + 8 * q);
+        if (MODE == MODE_G_P) {
+          float al[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) unpack8(apre_lo[q], al + 8 * q);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) a[c] += al[c];
+        }
         // the next block's A, under this block's stores
-        if (k + 1 < NB && gcb + 32 < m && gr < m) load_row32_bf16(arow, gcb + 32, m, apre);
+        if (k + 1 < NB && gcb + 32 < m && gr < m) {
+          load_row32_bf16(arow, gcb + 32, m, apre);
+          if (MODE == MODE_G_P) load_row32_bf16(arow_lo, gcb + 32, m, apre_lo);
+        }
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = fmaf(p.cb, a[c], p.cc * v[c]);
         if (diag && gr < m) {
@@ -633,11 +560,18 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
           for (int c = 0; c < 32; ++c)
             if (c == lane) {
               v[c] += p.ca;
-              p.pdiag[static_cast<size_t>(b) * m + gr] = v[c];
+              if (MODE == MODE_POLY) p.pdiag[static_cast<size_t>(b) * m + gr] = v[c];
             }
         }
       }
-      // the buffers are free once the previous block's bulk stores have read them
+#pragma unroll 1
+      for (int pl = 0; pl < (kPlanes ? 2 : 1); ++pl) {
+      if (pl == 1) {
+        // lo plane: the rounding residual of the hi plane just written
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] -= bf2f(f2bf(v[c]));
+      }
+      // the buffers are free once the previous bulk stores have read them
       if (lane == 0 && pending) bulk_wait_read_all();
       __syncwarp();
       if (!diag) {
@@ -670,10 +604,12 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && row0 < m) {
-        tma_store_3d(map_so, out_s, gcb, row0, b);
-        if (!diag) tma_store_3d(map_so, mir_s, row0, gcb, b);
+        const CUtensorMap* mo = pl == 0 ? map_so : map_so_lo;
+        tma_store_3d(mo, out_s, gcb, row0, b);
+        if (!diag) tma_store_3d(mo, mir_s, row0, gcb, b);
         bulk_commit_group();
         pending = true;
+      }
       }
     }
     tc_fence_before();
