@@ -162,17 +162,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int pa = 0; pa < AP; ++pa) {
             const CUtensorMap* ma = pa == 0 ? &map_a0 : &map_a1;
-            tma_load_3d(sa + pa * C::A_BYTES, ma, &full[s], kb * BK, i * BM, b);
-            tma_load_3d(sa + pa * C::A_BYTES + BOX_BYTES, ma, &full[s], kb * BK, i * BM + 64, b);
+            tma_load_3d(sa + pa * C::A_BYTES, ma, &full[s], kb * BK, i * BM, b);     // one 128-row box
           }
 #pragma unroll
           for (int pb = 0; pb < BP; ++pb) {
             const CUtensorMap* mb = pb == 0 ? &map_b0 : &map_b1;
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q) {
-              if (kUpd)
+              if (kUpd)        // MN-major: 64 columns x 64 K rows per box
                 tma_load_3d(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, &full[s], j * BN + q * 64, kb * BK, b);
-              else
+              else if ((q & 1) == 0)   // K-major: one 128-row box per two 64-row halves
                 tma_load_3d(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, &full[s], kb * BK, j * BN + q * 64, b);
             }
           }

@@ -139,18 +139,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int pa = 0; pa < AP; ++pa) {
             const CUtensorMap* ma = pa == 0 ? &map_a0 : &map_a1;
-            tma_load_3d_pair(sa + pa * C::A_BYTES, ma, fb, kb * BK, arow, b);
-            tma_load_3d_pair(sa + pa * C::A_BYTES + BOX_BYTES, ma, fb, kb * BK, arow + 64, b);
+            tma_load_3d_pair(sa + pa * C::A_BYTES, ma, fb, kb * BK, arow, b);        // one 128-row box
           }
 #pragma unroll
           for (int pb = 0; pb < BP; ++pb) {
             const CUtensorMap* mb = pb == 0 ? &map_b0 : &map_b1;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              if (kUpd)      // X^ read MN-major: 64 columns x 64 K rows per box
-                tma_load_3d_pair(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, fb, bcol + q * 64, kb * BK, b);
-              else
-                tma_load_3d_pair(sb + pb * C::B_BYTES + q * BOX_BYTES, mb, fb, kb * BK, bcol + q * 64, b);
+            if (kUpd) {      // X^ read MN-major: 64 columns x 64 K rows per box
+              tma_load_3d_pair(sb + pb * C::B_BYTES, mb, fb, bcol, kb * BK, b);
+              tma_load_3d_pair(sb + pb * C::B_BYTES + BOX_BYTES, mb, fb, bcol + 64, kb * BK, b);
+            } else {         // K-major: this CTA's 128 rows of B in one box
+              tma_load_3d_pair(sb + pb * C::B_BYTES, mb, fb, kb * BK, bcol, b);
             }
           }
           ++issued;

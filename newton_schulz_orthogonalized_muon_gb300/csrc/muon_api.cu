@@ -204,11 +204,14 @@ size_t arena_push(std::vector<uint8_t>& arena, const T* data, size_t count) {
   return off;
 }
 
+// Operand map: 64-column boxes with 128-byte swizzle, box_rows rows (128 for
+// K-major operands, one box per 128-row block; 64 for the MN-major reads of
+// X by the update product).
 bool encode_map(muon_handle_t h, CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t batch,
-                uint64_t ld) {
+                uint64_t ld, uint32_t box_rows = 128) {
   cuuint64_t dims[3] = {cols, rows, batch};
   cuuint64_t strides[2] = {ld * 2, rows * ld * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -330,9 +333,10 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     lo[k] = tc ? static_cast<void*>(ws + R.slot_lo[k]) : nullptr;
   }
   // per slot: 64 x 64 operand maps of both planes, and 32 x 32 output maps
-  CUtensorMap map_x, mhi[kGramSlots], mlo[kGramSlots], ohi[kGramSlots], olo[kGramSlots];
+  CUtensorMap map_x, map_xmn, mhi[kGramSlots], mlo[kGramSlots], ohi[kGramSlots], olo[kGramSlots];
   if (tc) {
-    bool ok = encode_map(h, &map_x, xb, g.n, g.m, g.chunk, g.ldx);
+    bool ok = encode_map(h, &map_x, xb, g.n, g.m, g.chunk, g.ldx) &&
+              encode_map(h, &map_xmn, xb, g.n, g.m, g.chunk, g.ldx, 64);
     for (int k = 0; k < kGramSlots && ok; ++k)
       ok = encode_map(h, &mhi[k], hi[k], g.m, g.m, g.chunk, g.ldm) &&
            encode_map(h, &mlo[k], lo[k], g.m, g.m, g.chunk, g.ldm) &&
@@ -458,7 +462,7 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
       f.num_tiles = cnt * mi * nj;
       const int grid = std::min(f.num_tiles, h->num_sms);
       MUON_LAUNCH(MUON_K_FINAL,
-                  launch_ns_gemm_tc_planes(MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur], map_x, map_x, map_x, map_x, f,
+                  launch_ns_gemm_tc_planes(MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur], map_xmn, map_xmn, map_xmn, map_xmn, f,
                                            grid, stream),
                   "gram final");
     } else {
@@ -566,10 +570,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     float* scale = reinterpret_cast<float*>(ws + R.scale);
 
     __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(ws + R.xlo) : nullptr;
-    CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
+    CUtensorMap map_x[2], map_xmn[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
     if (tc && steps > 0) {
       if (!encode_map(h, &map_x[0], xb[0], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &map_x[1], xb[1], g.n, g.m, g.chunk, g.ldx) ||
+          !encode_map(h, &map_xmn[0], xb[0], g.n, g.m, g.chunk, g.ldx, 64) ||
+          !encode_map(h, &map_xmn[1], xb[1], g.n, g.m, g.chunk, g.ldx, 64) ||
           !encode_map(h, &map_A, symA, g.m, g.m, g.chunk, g.ldm) ||
           !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm) ||
           !encode_box32(h->encode, &map_xh[0], xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
@@ -646,7 +652,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
             u.num_tiles = cnt * mi2 * nj2;
             const int upairs = std::min(u.num_tiles, h->max_pairs);
             MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                        launch_ns_gemm_pair_update(last ? MODE_FINAL : MODE_UPDATE, map_B, map_x[it & 1],
+                        launch_ns_gemm_pair_update(last ? MODE_FINAL : MODE_UPDATE, map_B, map_xmn[it & 1],
                                                    map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream),
                         "update launch");
           } else {
@@ -655,7 +661,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
             u.num_tiles = cnt * mi * nj;
             const int grid = std::min(u.num_tiles, h->num_sms);
             MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                        launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1],
+                        launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
                                                  map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
                         "update launch");
           }
@@ -682,7 +688,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           u.num_tiles = cnt * mi * nj;
           grid = std::min(u.num_tiles, h->num_sms);
           MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                      launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_x[it & 1],
+                      launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
                                                map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
                       "update launch");
         } else {

@@ -61,10 +61,10 @@ __global__ void noalloc_setup_kernel(NoAllocDesc d, unsigned* err, SrcEntry* src
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
 bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, uint64_t cols, uint64_t rows,
-                uint64_t ld) {
+                uint64_t ld, uint32_t box_rows = 128) {
   cuuint64_t dims[3] = {cols, rows, 1};
   cuuint64_t strides[2] = {ld * 2, rows * ld * 2};
-  cuuint32_t box[3] = {64, 64, 1};
+  cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -178,8 +178,10 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
     ApplyParams ap{out_d, scale, xf, ldx, M, N};
     return launch_apply(ap, 1, stream) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
   }
-  CUtensorMap map_x[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
+  CUtensorMap map_x[2], map_xmn[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
   if (tc && !(encode_map(S->encode, &map_x[0], xb0, N, M, ldx) && encode_map(S->encode, &map_x[1], xb1, N, M, ldx) &&
+              encode_map(S->encode, &map_xmn[0], xb0, N, M, ldx, 64) &&
+              encode_map(S->encode, &map_xmn[1], xb1, N, M, ldx, 64) &&
               encode_map(S->encode, &map_A, symA, M, M, ldm) && encode_map(S->encode, &map_B, symB, M, M, ldm) &&
               encode_box32(S->encode, &map_xh[0], xb0, false, N, M, 1, ldx) &&
               encode_box32(S->encode, &map_xh[1], xb1, false, N, M, 1, ldx) &&
@@ -224,7 +226,7 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
       u.tiles_per_mat = mi * nj;
       u.num_tiles = mi * nj;
       const int gu = u.num_tiles < S->num_sms ? u.num_tiles : S->num_sms;
-      e = launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, bn_upd, map_B, map_x[it & 1], map_xh[it & 1],
+      e = launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, bn_upd, map_B, map_xmn[it & 1], map_xh[it & 1],
                                    map_xl, map_xh[(it + 1) & 1], u, gu, stream);
     } else {
       float* xin = (it & 1) ? xf2 : xf;
