@@ -473,22 +473,36 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
                       split_heads=split, handle=h)
 
     # serial
-    def serial_one():
+    # events around the copies of the serial variant: the link rates the
+    # e2e figure is bounded by (they differ from box to box)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+
+    def serial_one(marks=None):
+        if marks:
+            marks[0].record(stream)
         for gd, gh in zip(G, Gh):
             gd.copy_(gh, non_blocking=True)
+        if marks:
+            marks[1].record(stream)
         step(G)
+        if marks:
+            marks[2].record(stream)
         for wh, wd in zip(Wh, W):
             wh.copy_(wd, non_blocking=True)
+        if marks:
+            marks[3].record(stream)
 
     serial_one()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        serial_one()
+    for k in range(steps):
+        serial_one(ev[k])
     e1.record(stream)
     torch.cuda.synchronize()
     serial_ms = e0.elapsed_time(e1) / steps
+    h2d_ms = sum(m[0].elapsed_time(m[1]) for m in ev) / steps
+    d2h_ms = sum(m[2].elapsed_time(m[3]) for m in ev) / steps
 
     # pipelined: two device gradient buffers, one device snapshot of the params
     G2 = [torch.empty_like(g) for g in G]
@@ -545,7 +559,8 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     torch.cuda.empty_cache()
     return {"value": alg_all / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "mode": "pipelined (copies overlapped with compute)",
-            "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12}
+            "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
+            "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9}
 
 
 def uses_pairs(m):

@@ -80,7 +80,7 @@ def test_pair_kernels_batched_step(handles):
         assert err < TOL_BF16
 
 
-@pytest.mark.parametrize("shape", [(256, 2048), (512, 4100), (1024, 768), (256, 512)])
+@pytest.mark.parametrize("shape", [(256, 2048), (512, 4100), (1024, 768), (256, 512), (2176, 2400)])
 def test_pair_gram_matches_oracle_and_single(handles, shape):
     pkg, pair, single = handles
     rank = min(shape) if shape == (256, 512) else 64
