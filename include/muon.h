@@ -179,6 +179,21 @@ typedef struct {
 muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t n_params,
                            const muon_step_options_t* opts, void* stream);
 
+/* Device workspace, in bytes, that muon_step / muon_step_ex would need for
+ * this parameter list on this handle: same-shape groups are processed in
+ * chunks sized to the handle's workspace limit
+ * (muon_handle_set_workspace_limit), and the workspace must hold the
+ * largest chunk.  The handle allocates it on first use, rounded up to a
+ * multiple of 64 MiB, keeps it until destroyed, and grows it when a later
+ * call needs more; a small descriptor buffer comes on top.  Only shapes,
+ * dtypes and split_heads of params are read (pointers may be NULL).
+ * Host-only: enqueues nothing.  (Sizing has no counterpart on the source
+ * pages; it lets a caller budget device memory before the first step.)
+ *   ns_method, ns_steps, ns_dtype: as in muon_step.
+ *   bytes: host pointer, receives the size (0 for an empty list). */
+muon_status_t muon_workspace_size(muon_handle_t h, const muon_param_t* params, int32_t n_params, int32_t ns_method,
+                                  int32_t ns_steps, int32_t ns_dtype, uint64_t* bytes);
+
 /* AdamW fallback for non-Muon parameters (the AdamW backup of the printed
  * Muon class, "迎接DeepSeek开源周…Muon优化器", §代码):
  *   m <- m + (1-beta1)(g - m);  v <- v + (1-beta2)(g^2 - v);

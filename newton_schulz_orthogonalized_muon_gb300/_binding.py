@@ -28,7 +28,7 @@ EXPORTS = ("muon_handle_create", "muon_handle_destroy", "muon_handle_set_workspa
            "muon_handle_set_timeout_ns", "muon_handle_check", "muon_orthogonalize", "muon_step",
            "adamw_step", "muon_selftest_timeout", "muon_status_string", "muon_last_error", "muon_version",
            "muon_handle_set_profiling", "muon_handle_profile", "muon_handle_launch_count",
-           "muon_orthogonalize_noalloc", "muon_handle_profile_records", "muon_step_ex")
+           "muon_orthogonalize_noalloc", "muon_handle_profile_records", "muon_step_ex", "muon_workspace_size")
 KERNEL_CLASSES = ("prepare", "norm", "syrk", "poly", "update", "final", "apply", "adamw")
 
 
@@ -93,6 +93,7 @@ def load_library(path: str | None = None):
             "muon_handle_profile_records": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), fptr, i32,
                                                   ctypes.POINTER(i32)]),
             "muon_step_ex": (i32, [vp, ctypes.POINTER(MuonParamC), i32, ctypes.POINTER(MuonStepOptionsC), vp]),
+            "muon_workspace_size": (i32, [vp, ctypes.POINTER(MuonParamC), i32, i32, i32, i32, ctypes.POINTER(u64)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -293,6 +294,24 @@ def muon_step(params, grads, momenta, *, lr: float, wd: float, mu: float = 0.95,
     h = handle or default_handle(dev)
     st = h._lib.muon_step_ex(h.ptr, arr, n, ctypes.byref(opts), ctypes.c_void_p(_stream_ptr(stream)))
     h._raise(st, "muon_step_ex")
+
+
+def workspace_size(shapes, *, ns_method="standard", ns_steps: int = 5, ns_dtype=torch.bfloat16, split_heads=None,
+                   handle: MuonHandle | None = None, device=None) -> int:
+    """Device workspace bytes muon_step would need for parameters of these
+    (rows, cols) shapes on this handle (its workspace limit decides the
+    chunking); nothing is enqueued."""
+    n = len(shapes)
+    split_heads = [1] * n if split_heads is None else list(split_heads)
+    code = MUON_BF16 if ns_dtype in (torch.bfloat16, MUON_BF16) else MUON_F32
+    arr = (MuonParamC * max(n, 1))()
+    for i, (r, c) in enumerate(shapes):
+        arr[i] = MuonParamC(None, None, None, int(r), int(c), code, code, int(split_heads[i]), 0, 0)
+    h = handle or default_handle(device)
+    out = ctypes.c_uint64(0)
+    st = h._lib.muon_workspace_size(h.ptr, arr, n, _method(ns_method), int(ns_steps), int(code), ctypes.byref(out))
+    h._raise(st, "muon_workspace_size")
+    return int(out.value)
 
 
 def adamw_step(params, grads, exp_avgs, exp_avg_sqs, *, step: int, lr: float, beta1: float, beta2: float,

@@ -474,6 +474,30 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
 }
 
 // Run prepare + Newton-Schulz + final write for every block.
+// Strides, tile widths and the chunk (matrices per launch) of one same-shape
+// group under the handle's workspace limit; returns the workspace bytes the
+// group's chunk needs.
+size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps) {
+  g.ldx = static_cast<long long>(align_up(g.n, 8));
+  g.ldm = static_cast<long long>(align_up(g.m, 8));
+  g.prep_tiles = static_cast<int>(ceil_div(g.m, 64) * ceil_div(g.n, 64));
+  g.bn_sym = g.m <= 128 ? 128 : 256;
+  g.bn_upd = g.n <= 128 ? 128 : 256;
+  const size_t per1 = regions(g, 1, tc, gram, steps).total;
+  const size_t per2 = regions(g, 2, tc, gram, steps).total;
+  g.per_mat = per2 > per1 ? per2 - per1 : per1;
+  const size_t fixed = per1 > g.per_mat ? per1 - g.per_mat : 0;
+  size_t fit = h->ws_limit > fixed ? (h->ws_limit - fixed) / std::max<size_t>(g.per_mat, 1) : 1;
+  fit = std::max<size_t>(fit, 1);
+  fit = std::min<size_t>(fit, g.members.size());
+  fit = std::min<size_t>(fit, 65535);
+  const int tiles_upd = static_cast<int>(ceil_div(g.m, 128) * ceil_div(g.n, g.bn_upd));
+  const int tiles_max = std::max({tiles_upd, g.prep_tiles, 1});
+  fit = std::min<size_t>(fit, static_cast<size_t>((1u << 31) - 1) / static_cast<size_t>(tiles_max));
+  g.chunk = static_cast<int>(fit);
+  return regions(g, g.chunk, tc, gram, steps).total;
+}
+
 // coeffs: (a, b, c) of step k at coeffs[k * coeff_stride] (stride 0: one
 // triple for every step, 3: a schedule of `steps` triples).
 muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, float mu, int nesterov, int steps,
@@ -493,24 +517,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   size_t ws_need = 0;
   for (auto& kv : groups) {
     GroupPlan& g = kv.second;
-    g.ldx = static_cast<long long>(align_up(g.n, 8));
-    g.ldm = static_cast<long long>(align_up(g.m, 8));
-    g.prep_tiles = static_cast<int>(ceil_div(g.m, 64) * ceil_div(g.n, 64));
-    g.bn_sym = g.m <= 128 ? 128 : 256;
-    g.bn_upd = g.n <= 128 ? 128 : 256;
-    const size_t per1 = regions(g, 1, tc, gram, steps).total;
-    const size_t per2 = regions(g, 2, tc, gram, steps).total;
-    g.per_mat = per2 > per1 ? per2 - per1 : per1;
-    const size_t fixed = per1 > g.per_mat ? per1 - g.per_mat : 0;
-    size_t fit = h->ws_limit > fixed ? (h->ws_limit - fixed) / std::max<size_t>(g.per_mat, 1) : 1;
-    fit = std::max<size_t>(fit, 1);
-    fit = std::min<size_t>(fit, g.members.size());
-    fit = std::min<size_t>(fit, 65535);
-    const int tiles_upd = static_cast<int>(ceil_div(g.m, 128) * ceil_div(g.n, g.bn_upd));
-    const int tiles_max = std::max({tiles_upd, g.prep_tiles, 1});
-    fit = std::min<size_t>(fit, static_cast<size_t>((1u << 31) - 1) / static_cast<size_t>(tiles_max));
-    g.chunk = static_cast<int>(fit);
-    ws_need = std::max(ws_need, regions(g, g.chunk, tc, gram, steps).total);
+    ws_need = std::max(ws_need, plan_group(h, g, tc, gram, steps));
     if (tc) {
       std::vector<int2> tri = sym_tiles(g.m, g.bn_sym);
       g.tri_count = static_cast<int>(tri.size());
@@ -717,6 +724,52 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
 
 bool valid_dtype(int32_t d) { return d == MUON_F32 || d == MUON_BF16; }
 
+// Validate the parameter descriptors and expand them into NS blocks (one per
+// Muon-Split head block, rows <= cols after the transpose rule) with their
+// source / destination entries.  need_ptrs = false: shapes only (sizing).
+muon_status_t build_blocks(muon_handle_t h, const muon_param_t* params, int32_t n_params,
+                           const muon_step_options_t& o, bool need_ptrs, std::vector<Block>* out) {
+  for (int32_t i = 0; i < n_params; ++i) {
+    const muon_param_t& P = params[i];
+    const std::string where = "param " + std::to_string(i) + ": ";
+    if (!valid_dtype(P.param_dtype) || !valid_dtype(P.grad_dtype))
+      return fail(h, MUON_ERR_INVALID_ARG, where + "bad dtype");
+    if (P.rows < 0 || P.cols < 0 || P.rows > kMaxDim || P.cols > kMaxDim)
+      return fail(h, MUON_ERR_INVALID_ARG, where + "negative or oversized shape");
+    if (P.split_heads < 1 || (P.rows > 0 && P.rows % P.split_heads != 0))
+      return fail(h, MUON_ERR_INVALID_ARG, where + "split_heads must be >= 1 and divide rows");
+    if (P.reserved != 0 || P.scale_dim < 0) return fail(h, MUON_ERR_INVALID_ARG, where + "bad reserved/scale_dim");
+    if (P.rows == 0 || P.cols == 0) continue;
+    if (need_ptrs && (P.param == nullptr || P.grad == nullptr || P.momentum == nullptr))
+      return fail(h, MUON_ERR_INVALID_ARG, where + "NULL pointer");
+    const int64_t rb = P.rows / P.split_heads;
+    // update scale: RMS matching update_rms * sqrt(max(A, B)) (or scale_dim),
+    // or muP sqrt(d_out / d_in) of the stored (out x in) parameter
+    double scale;
+    if (o.scale_mode == MUON_SCALE_MUP) {
+      scale = std::sqrt(static_cast<double>(P.rows) / static_cast<double>(P.cols));
+    } else {
+      const double sdim = static_cast<double>(P.scale_dim > 0 ? P.scale_dim : std::max(P.rows, P.cols));
+      scale = static_cast<double>(o.update_rms) * std::sqrt(sdim);
+    }
+    const float beta = static_cast<float>(-static_cast<double>(o.lr) * o.extra_scale * scale);
+    const float alpha = static_cast<float>(1.0 - static_cast<double>(o.lr) * o.wd);
+    const size_t ge = dtype_size(P.grad_dtype), pe = dtype_size(P.param_dtype);
+    for (int32_t hb = 0; hb < P.split_heads; ++hb) {
+      const size_t off = static_cast<size_t>(hb) * rb * P.cols;
+      Block bl;
+      const int transposed = rb > P.cols ? 1 : 0;
+      bl.src = SrcEntry{static_cast<const uint8_t*>(P.grad) + off * ge, P.momentum + off, P.cols,
+                        static_cast<int>(rb), static_cast<int>(P.cols), transposed, P.grad_dtype};
+      bl.out = OutEntry{static_cast<uint8_t*>(P.param) + off * pe, P.cols, transposed, P.param_dtype, alpha, beta};
+      bl.m = static_cast<int>(std::min<int64_t>(rb, P.cols));
+      bl.n = static_cast<int>(std::max<int64_t>(rb, P.cols));
+      out->push_back(bl);
+    }
+  }
+  return MUON_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -851,6 +904,38 @@ muon_status_t muon_orthogonalize(muon_handle_t h, void* X, int32_t dtype, int64_
   return run_blocks(h, blocks, 0.f, 0, steps, cf, 0, ns_method, dtype == MUON_BF16, static_cast<cudaStream_t>(stream));
 }
 
+muon_status_t muon_workspace_size(muon_handle_t h, const muon_param_t* params, int32_t n_params, int32_t ns_method,
+                                  int32_t ns_steps, int32_t ns_dtype, uint64_t* bytes) {
+  if (h == nullptr) return MUON_ERR_INVALID_ARG;
+  if (bytes == nullptr) return fail(h, MUON_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = 0;
+  if (n_params < 0) return fail(h, MUON_ERR_INVALID_ARG, "n_params < 0");
+  if (n_params > 0 && params == nullptr) return fail(h, MUON_ERR_INVALID_ARG, "params is NULL");
+  if (!valid_dtype(ns_dtype)) return fail(h, MUON_ERR_INVALID_ARG, "ns_dtype must be MUON_F32 or MUON_BF16");
+  if (ns_method != MUON_NS_STANDARD && ns_method != MUON_NS_GRAM)
+    return fail(h, MUON_ERR_INVALID_ARG, "unknown ns_method");
+  if (ns_steps < 0 || ns_steps > 100) return fail(h, MUON_ERR_INVALID_ARG, "ns_steps must be in [0, 100]");
+  muon_step_options_t o{};
+  o.update_rms = 0.2f;
+  o.extra_scale = 1.0f;
+  std::vector<Block> blocks;
+  const muon_status_t st = build_blocks(h, params, n_params, o, false, &blocks);
+  if (st != MUON_OK) return st;
+  // the same grouping and chunking muon_step plans
+  std::map<std::pair<int, int>, GroupPlan> groups;
+  for (size_t i = 0; i < blocks.size(); ++i) {
+    GroupPlan& g = groups[{blocks[i].m, blocks[i].n}];
+    g.m = blocks[i].m;
+    g.n = blocks[i].n;
+    g.members.push_back(static_cast<int>(i));
+  }
+  size_t need = 0;
+  for (auto& kv : groups)
+    need = std::max(need, plan_group(h, kv.second, ns_dtype == MUON_BF16, ns_method == MUON_NS_GRAM, ns_steps));
+  *bytes = need;
+  return MUON_OK;
+}
+
 muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t n_params,
                            const muon_step_options_t* opts, void* stream) {
   if (h == nullptr) return MUON_ERR_INVALID_ARG;
@@ -877,44 +962,8 @@ muon_status_t muon_step_ex(muon_handle_t h, const muon_param_t* params, int32_t 
       !std::isfinite(o.extra_scale))
     return fail(h, MUON_ERR_INVALID_ARG, "non-finite hyper-parameter");
   std::vector<Block> blocks;
-  for (int32_t i = 0; i < n_params; ++i) {
-    const muon_param_t& P = params[i];
-    const std::string where = "param " + std::to_string(i) + ": ";
-    if (!valid_dtype(P.param_dtype) || !valid_dtype(P.grad_dtype))
-      return fail(h, MUON_ERR_INVALID_ARG, where + "bad dtype");
-    if (P.rows < 0 || P.cols < 0 || P.rows > kMaxDim || P.cols > kMaxDim)
-      return fail(h, MUON_ERR_INVALID_ARG, where + "negative or oversized shape");
-    if (P.split_heads < 1 || (P.rows > 0 && P.rows % P.split_heads != 0))
-      return fail(h, MUON_ERR_INVALID_ARG, where + "split_heads must be >= 1 and divide rows");
-    if (P.reserved != 0 || P.scale_dim < 0) return fail(h, MUON_ERR_INVALID_ARG, where + "bad reserved/scale_dim");
-    if (P.rows == 0 || P.cols == 0) continue;
-    if (P.param == nullptr || P.grad == nullptr || P.momentum == nullptr)
-      return fail(h, MUON_ERR_INVALID_ARG, where + "NULL pointer");
-    const int64_t rb = P.rows / P.split_heads;
-    // update scale: RMS matching update_rms * sqrt(max(A, B)) (or scale_dim),
-    // or muP sqrt(d_out / d_in) of the stored (out x in) parameter
-    double scale;
-    if (o.scale_mode == MUON_SCALE_MUP) {
-      scale = std::sqrt(static_cast<double>(P.rows) / static_cast<double>(P.cols));
-    } else {
-      const double sdim = static_cast<double>(P.scale_dim > 0 ? P.scale_dim : std::max(P.rows, P.cols));
-      scale = static_cast<double>(o.update_rms) * std::sqrt(sdim);
-    }
-    const float beta = static_cast<float>(-static_cast<double>(o.lr) * o.extra_scale * scale);
-    const float alpha = static_cast<float>(1.0 - static_cast<double>(o.lr) * o.wd);
-    const size_t ge = dtype_size(P.grad_dtype), pe = dtype_size(P.param_dtype);
-    for (int32_t hb = 0; hb < P.split_heads; ++hb) {
-      const size_t off = static_cast<size_t>(hb) * rb * P.cols;
-      Block bl;
-      const int transposed = rb > P.cols ? 1 : 0;
-      bl.src = SrcEntry{static_cast<const uint8_t*>(P.grad) + off * ge, P.momentum + off, P.cols,
-                        static_cast<int>(rb), static_cast<int>(P.cols), transposed, P.grad_dtype};
-      bl.out = OutEntry{static_cast<uint8_t*>(P.param) + off * pe, P.cols, transposed, P.param_dtype, alpha, beta};
-      bl.m = static_cast<int>(std::min<int64_t>(rb, P.cols));
-      bl.n = static_cast<int>(std::max<int64_t>(rb, P.cols));
-      blocks.push_back(bl);
-    }
-  }
+  const muon_status_t bst = build_blocks(h, params, n_params, o, true, &blocks);
+  if (bst != MUON_OK) return bst;
   if (blocks.empty()) return MUON_OK;
   DeviceGuard guard(h->device);
   const float* cf = o.coeffs ? o.coeffs : kDefaultCoeffs;

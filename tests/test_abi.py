@@ -99,6 +99,11 @@ def test_struct_layouts_match_the_c_compiler(tmp_path):
     assert got == want
 
 
+def test_workspace_size_rejects_a_null_handle(lib):
+    out = ctypes.c_uint64(7)
+    assert lib.muon_workspace_size(None, None, 0, 0, 5, 1, ctypes.byref(out)) == 1
+
+
 def test_step_ex_rejects_bad_arguments_without_a_device(lib):
     from newton_schulz_orthogonalized_muon_gb300._binding import MuonStepOptionsC
     opts = MuonStepOptionsC(0.02, 0.1, 0.95, 1, 0, 5, None, 1, 0, 0.2, 1.0, 0)

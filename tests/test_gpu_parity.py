@@ -367,3 +367,40 @@ def test_step_gram_bf16(pkg):
         base = W0[i] * (1 - 0.02 * 0.1)
         assert delta_err_bf16(host64(Wd[i]), w_ref, base, 1) < TOL_BF16
         assert rel(host64(Md[i]), m_ref) < TOL_EXACT
+
+
+# ------------------------------------------------------- workspace sizing
+
+def test_workspace_size_matches_the_allocation_of_a_step():
+    """muon_workspace_size predicts what the first step allocates (rounded to
+    64 MiB), follows the handle's limit, and enqueues nothing."""
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    specs = [wl.ParamSpec("a", (1024, 4096)), wl.ParamSpec("b", (4096, 1024)), wl.ParamSpec("c", (512, 512)),
+             wl.ParamSpec("q", (512, 256), split_heads=2)]
+    shapes = [s.shape for s in specs]
+    split = [s.split_heads for s in specs]
+    h = pkg.MuonHandle(0)
+    need = pkg.workspace_size(shapes, split_heads=split, handle=h)
+    assert need > 0
+    # a limit below one group's need shrinks the chunks, never below one matrix
+    h.set_workspace_limit(need // 2)
+    small = pkg.workspace_size(shapes, split_heads=split, handle=h)
+    assert 0 < small < need
+    h.set_workspace_limit(64 << 30)
+    W = [torch.zeros(s.shape, device="cuda", dtype=torch.bfloat16) for s in specs]
+    G = [torch.randn(s.shape, device="cuda").to(torch.bfloat16) for s in specs]
+    M = [torch.zeros(s.shape, device="cuda") for s in specs]
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    pkg.muon_step(W, G, M, lr=0.02, wd=0.1, split_heads=split, handle=h)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert h.check() == 0
+    used = free0 - free1
+    rounded = -(-need // (64 << 20)) * (64 << 20)
+    # the workspace plus a descriptor buffer of at most a few MiB
+    assert rounded <= used <= rounded + (16 << 20), (need, rounded, used)
+    assert pkg.workspace_size([], handle=h) == 0
