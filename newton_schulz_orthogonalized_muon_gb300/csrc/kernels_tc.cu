@@ -64,12 +64,20 @@ namespace {
 using namespace tc;
 
 
+// UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
+// 4 KB slot, which leaves room for a fourth main-loop stage at BN = 256;
+// FINAL keeps two.
+template <int MODE>
+struct OneSlots {
+  static constexpr int v = MODE == MODE_FINAL ? 2 : 1;
+};
+
 template <int MODE, int BN, int AP, int BP>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;            // one plane of the A tile
   static constexpr int B_BYTES = BN * BK * 2;            // one plane of the B tile
   static constexpr int STAGE_BYTES = AP * A_BYTES + BP * B_BYTES;
-  static constexpr int EPI_BYTES = EpiLayout<MODE>::BYTES + SymEpi<MODE>::BYTES;
+  static constexpr int EPI_BYTES = EpiLayout<MODE, OneSlots<MODE>::v>::BYTES + SymEpi<MODE>::BYTES;
   static constexpr int BAR_BYTES = 512;
   // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
   static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -88,7 +96,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                       const __grid_constant__ CUtensorMap map_xh, const __grid_constant__ CUtensorMap map_xl,
                       const __grid_constant__ CUtensorMap map_xo, const NsGemmParams p) {
   using C = Cfg<MODE, BN, AP, BP>;
-  using L = EpiLayout<MODE>;
+  using L = EpiLayout<MODE, OneSlots<MODE>::v>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
   constexpr bool kSym = ModeTraits<MODE>::kSym;
   extern __shared__ uint8_t smem_raw[];
@@ -260,7 +268,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     et.row_off = 0;
     et.remote = false;
     et.tempty = tempty;
-    mn_epilogue<MODE, BN, BM, 2>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES, xfull + 2 * (warp - 2),
+    mn_epilogue<MODE, BN, BM, OneSlots<MODE>::v>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES, xfull + 2 * (warp - 2),
                               tfull, et, abort, tmem_base, warp, lane);
   }
 
