@@ -356,7 +356,7 @@ def run_ours(args):
             except Exception:
                 traffic = None
         m_top = int(top["group"].split("x")[0])
-        kname = "ns_gemm_pair_kernel" if uses_pairs(m_top) else "ns_gemm_tc_kernel"
+        kname = "ns_gemm_pair_kernel" if uses_pairs(m_top, top["kernel"]) else "ns_gemm_tc_kernel"
         roofline = {"bound": "tensor", "kernel": f"{kname}<{top['kernel'].upper()}> on the {top['group']} group "
                                                   f"({top['matrices']} matrices)",
                     "achieved": top["tflops"], "peak": peak, "unit": "TFLOP/s", "frac": top["tflops"] / peak,
@@ -563,18 +563,22 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9}
 
 
-def uses_pairs(m):
-    """The library's rule for which groups run on the CTA-pair kernels (m a
-    multiple of 256, or m >= MUON_TC_PAIR_MIN_M, 2048 by default; none with
-    MUON_TC_PAIR=0); standard method."""
+def uses_pairs(m, kernel_class):
+    """The library's rule for which products run on the CTA-pair kernels
+    (standard method): symmetric products when m is a multiple of 256 or
+    m >= MUON_TC_PAIR_MIN_M (1024 by default); UPDATE / FINAL when m is a
+    multiple of 256 or m >= 2048; none with MUON_TC_PAIR=0, symmetric
+    products only with MUON_TC_PAIR=sym."""
     env = os.environ.get("MUON_TC_PAIR")
-    if env == "0":
+    if env == "0" or m < 256:
         return False
+    if kernel_class in ("update", "final"):
+        return env != "sym" and (m % 256 == 0 or m >= 2048)
     try:
-        min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "2048"))
+        min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "1024"))
     except ValueError:
-        min_m = 2048
-    return m >= 256 and (m % 256 == 0 or m >= min_m)
+        min_m = 1024
+    return m % 256 == 0 or m >= min_m
 
 
 def kernel_source_hash():

@@ -85,11 +85,12 @@ typedef struct {
 /* Create a handle on CUDA device `device`.  Checks that the device is
  * sm_103 (GB300) and resolves the tensor-map encoder.  *out is NULL on error.
  * Groups with m a multiple of 256 (or m >= 2048) run the GEMMs of the bf16
- * path on two-SM CTA pairs (256 x 256 tiles); the environment variable
- * MUON_TC_PAIR, read when the handle is created, selects the one-SM kernels
- * instead ("0") or pairs for the symmetric products only ("sym");
- * MUON_TC_PAIR_MIN_M (default 2048) is the m from which groups whose m is
- * not a multiple of 256 run on pairs too. */
+ * path on two-SM CTA pairs (256 x 256 tiles); groups with a ragged last
+ * 256-row tile and m >= 1024 run their symmetric products on pairs and the
+ * update products on one SM.  The environment variables, read when the
+ * handle is created: MUON_TC_PAIR selects the one-SM kernels everywhere
+ * ("0") or pairs for the symmetric products only ("sym");
+ * MUON_TC_PAIR_MIN_M (default 1024) moves the ragged-m threshold. */
 muon_status_t muon_handle_create(muon_handle_t* out, int device);
 
 /* Destroy a handle: synchronises the device, frees the workspace. NULL is a no-op. */

@@ -74,7 +74,7 @@ struct muon_handle_s {
   uint64_t launches = 0;
   bool use_pair = true;         // CTA-pair GEMMs for large groups (MUON_TC_PAIR=0 disables)
   bool pair_update = true;      // UPDATE / FINAL on pairs too (MUON_TC_PAIR=sym: symmetric products only)
-  int pair_min_m = 2048;        // ragged m from here on runs on pairs too (MUON_TC_PAIR_MIN_M)
+  int pair_min_m = 1024;        // ragged m from here on runs its symmetric products on pairs too (MUON_TC_PAIR_MIN_M)
   int max_pairs = 0;
 };
 
@@ -248,7 +248,8 @@ struct GroupPlan {
   int tri128_count = 0;
   size_t tri256_off = 0;        // 256 x 256 symmetric tiles (CTA-pair kernels)
   int tri256_count = 0;
-  bool pair = false;
+  bool pair = false;            // symmetric products on CTA pairs
+  bool pair_upd = false;        // UPDATE / FINAL on CTA pairs
   std::vector<std::pair<size_t, size_t>> chunk_off;   // (src offset, out offset) per chunk
 };
 
@@ -532,6 +533,10 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         g.tri256_count = static_cast<int>(t256.size());
         g.tri256_off = arena_push(arena, t256.data(), t256.size());
         g.pair = true;
+        // UPDATE / FINAL on pairs only without a ragged last row tile, or
+        // from m = 2048 (a ragged tile costs them more than the symmetric
+        // products)
+        g.pair_upd = h->pair_update && (g.m % 256 == 0 || g.m >= 2048);
       }
     }
     for (size_t c0 = 0; c0 < g.members.size(); c0 += g.chunk) {
@@ -637,8 +642,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         p.timeout_ns = h->timeout_ns;
         p.pdiag = pdiag;
         if (tc && g.pair) {
-          // SYRK, POLY and (unless MUON_TC_PAIR=sym) UPDATE / FINAL on CTA
-          // pairs, 256 x 256 tiles
+          // SYRK, POLY and (pair_upd) UPDATE / FINAL on CTA pairs, 256 x 256
+          // tiles
           NsGemmParams q = p;
           q.tiles_per_mat = g.tri256_count;
           q.num_tiles = cnt * g.tri256_count;
@@ -652,7 +657,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.sym_out = symB;
           MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream), "poly launch");
           NsGemmParams u = p;
-          if (h->pair_update) {
+          if (g.pair_upd) {
             const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
             u.mi = mi2;
             u.tiles_per_mat = mi2 * nj2;

@@ -100,8 +100,9 @@ def test_pair_gram_matches_oracle_and_single(handles, shape):
 
 @pytest.fixture(scope="module")
 def ragged_handle(handles):
-    """A handle that runs groups with m >= 1024 on pairs even when m is not a
-    multiple of 256 (the last 256-row tile is ragged)."""
+    """A handle that runs the symmetric products of groups with m >= 1024 on
+    pairs even when m is not a multiple of 256 (the last 256-row tile is
+    ragged); the threshold is the default, set explicitly here."""
     pkg = handles[0]
     old = os.environ.get("MUON_TC_PAIR_MIN_M")
     os.environ["MUON_TC_PAIR_MIN_M"] = "1024"
