@@ -90,7 +90,9 @@ typedef struct {
  * update products on one SM.  The environment variables, read when the
  * handle is created: MUON_TC_PAIR selects the one-SM kernels everywhere
  * ("0") or pairs for the symmetric products only ("sym");
- * MUON_TC_PAIR_MIN_M (default 1024) moves the ragged-m threshold. */
+ * MUON_TC_PAIR_MIN_M (default 1024) moves the ragged-m threshold;
+ * MUON_FINAL_TMA=0 makes the last product write bf16 parameters element-wise
+ * instead of through per-parameter tensor maps (same results, bit for bit). */
 muon_status_t muon_handle_create(muon_handle_t* out, int device);
 
 /* Destroy a handle: synchronises the device, frees the workspace. NULL is a no-op. */

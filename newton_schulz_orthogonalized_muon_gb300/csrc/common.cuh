@@ -140,6 +140,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Makes a tensor map in global memory, written before this kernel, visible to
+// this thread's later TMA operations that name it (the map is 128 bytes).
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
 // Tiled bulk store shared -> global (3-D map; elements outside the tensor
 // are not written), committed to this thread's bulk async-group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {

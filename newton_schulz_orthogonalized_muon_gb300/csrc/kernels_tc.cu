@@ -327,11 +327,13 @@ cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& ma, co
     switch (mode) {
       case MODE_UPDATE: return launch_one<MODE_UPDATE, 256, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
       case MODE_FINAL: return launch_one<MODE_FINAL, 256, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
+      case MODE_FINAL_T: return launch_one<MODE_FINAL_T, 256, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
     }
   } else if (bn == 128) {
     switch (mode) {
       case MODE_UPDATE: return launch_one<MODE_UPDATE, 128, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
       case MODE_FINAL: return launch_one<MODE_FINAL, 128, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
+      case MODE_FINAL_T: return launch_one<MODE_FINAL_T, 128, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
     }
   }
   return cudaErrorInvalidValue;

@@ -328,6 +328,7 @@ cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& a, const CUt
   switch (mode) {
     case MODE_UPDATE: return launch_pair<MODE_UPDATE, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
     case MODE_FINAL: return launch_pair<MODE_FINAL, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
+    case MODE_FINAL_T: return launch_pair<MODE_FINAL_T, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
   }
   return cudaErrorInvalidValue;
 }

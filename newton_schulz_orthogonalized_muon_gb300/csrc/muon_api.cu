@@ -76,6 +76,7 @@ struct muon_handle_s {
   bool pair_update = true;      // UPDATE / FINAL on pairs too (MUON_TC_PAIR=sym: symmetric products only)
   int pair_min_m = 1024;        // ragged m from here on runs its symmetric products on pairs too (MUON_TC_PAIR_MIN_M)
   int max_pairs = 0;
+  bool final_tma = true;        // FINAL into bf16 destinations through tensor maps (MUON_FINAL_TMA=0 disables)
 };
 
 namespace {
@@ -251,7 +252,26 @@ struct GroupPlan {
   bool pair = false;            // symmetric products on CTA pairs
   bool pair_upd = false;        // UPDATE / FINAL on CTA pairs
   std::vector<std::pair<size_t, size_t>> chunk_off;   // (src offset, out offset) per chunk
+  std::vector<size_t> chunk_wmap;   // per chunk: offset of the destinations' tensor maps, or kNoMaps
 };
+
+constexpr size_t kNoMaps = ~size_t(0);
+
+// One tensor map per destination of a chunk, for FINAL_T: possible when every
+// destination is bf16 with a 16-byte aligned base and row stride (TMA's
+// rules); the map covers the destination in its own orientation (n x m when
+// the block was transposed).
+bool encode_dest_maps(muon_handle_t h, const GroupPlan& g, const std::vector<OutEntry>& out,
+                      std::vector<CUtensorMap>* maps) {
+  maps->resize(out.size());
+  for (size_t k = 0; k < out.size(); ++k) {
+    const OutEntry& e = out[k];
+    if (e.dtype != DT_BF16 || (reinterpret_cast<uintptr_t>(e.ptr) & 15) != 0 || ((e.ld * 2) & 15) != 0) return false;
+    const uint64_t drows = e.transposed ? g.n : g.m, dcols = e.transposed ? g.m : g.n;
+    if (!encode_box32(h->encode, &(*maps)[k], e.ptr, false, dcols, drows, 1, static_cast<uint64_t>(e.ld))) return false;
+  }
+  return true;
+}
 
 // Workspace region offsets for one chunk capacity `cap` (bytes from ws base).
 //   standard, tensor cores: fp32 master X, two bf16 operand copies (ping-pong),
@@ -550,6 +570,9 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
       const size_t so = arena_push(arena, src.data(), cnt);
       const size_t oo = arena_push(arena, out.data(), cnt);
       g.chunk_off.emplace_back(so, oo);
+      std::vector<CUtensorMap> maps;
+      const bool tma_out = tc && !gram && steps > 0 && h->final_tma && encode_dest_maps(h, g, out, &maps);
+      g.chunk_wmap.push_back(tma_out ? arena_push(arena, maps.data(), maps.size()) : kNoMaps);
     }
   }
 
@@ -604,6 +627,11 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
       const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
       const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
       const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+      const CUtensorMap* wmap_d =
+          g.chunk_wmap[c] == kNoMaps ? nullptr : reinterpret_cast<const CUtensorMap*>(dbase + g.chunk_wmap[c]);
+      // the last UPDATE writes the destinations: through their tensor maps
+      // when the chunk has them
+      const int final_mode = wmap_d != nullptr ? MODE_FINAL_T : MODE_FINAL;
 
       PrepParams pp{};
       pp.src = src_d;
@@ -638,6 +666,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         p.ldm = g.ldm;
         p.ldx = g.ldx;
         p.out = out_d;
+        p.wmap = wmap_d;
         p.err = h->err;
         p.timeout_ns = h->timeout_ns;
         p.pdiag = pdiag;
@@ -664,7 +693,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
             u.num_tiles = cnt * mi2 * nj2;
             const int upairs = std::min(u.num_tiles, h->max_pairs);
             MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                        launch_ns_gemm_pair_update(last ? MODE_FINAL : MODE_UPDATE, map_B, map_xmn[it & 1],
+                        launch_ns_gemm_pair_update(last ? final_mode : MODE_UPDATE, map_B, map_xmn[it & 1],
                                                    map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream),
                         "update launch");
           } else {
@@ -673,7 +702,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
             u.num_tiles = cnt * mi * nj;
             const int grid = std::min(u.num_tiles, h->num_sms);
             MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                        launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
+                        launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
                                                  map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
                         "update launch");
           }
@@ -700,7 +729,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           u.num_tiles = cnt * mi * nj;
           grid = std::min(u.num_tiles, h->num_sms);
           MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                      launch_ns_gemm_tc_update(last ? MODE_FINAL : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
+                      launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
                                                map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
                       "update launch");
         } else {
@@ -829,6 +858,7 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
     if (v >= 256 && v <= (1L << 30)) h->pair_min_m = static_cast<int>(v);
   }
   h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
+  if (const char* ft = std::getenv("MUON_FINAL_TMA")) h->final_tma = ft[0] != '0';
   if (cudaMalloc(&h->err, sizeof(unsigned)) != cudaSuccess || cudaMemset(h->err, 0, sizeof(unsigned)) != cudaSuccess ||
       cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) {
     cudaGetLastError();

@@ -22,7 +22,8 @@ template <int MODE>
 struct ModeTraits {
   static constexpr bool kSym = (MODE == MODE_SYRK || MODE == MODE_POLY || MODE == MODE_G_R0 ||
                                 MODE == MODE_G_P || MODE == MODE_G_PROD);
-  static constexpr bool kMN = (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_G_FINAL);
+  static constexpr bool kMN =
+      (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_G_FINAL || MODE == MODE_FINAL_T);
   static constexpr bool kKn = (MODE == MODE_SYRK || MODE == MODE_G_R0);   // K = n (else K = m)
   static constexpr bool kPlanesOut = (MODE == MODE_G_R0 || MODE == MODE_G_P || MODE == MODE_G_PROD);
 };
@@ -77,15 +78,19 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
 //   result in destination orientation (transposed when the destination is
 //   out[c][r]), then written out as 16-byte row segments, eight lanes per
 //   destination row.
+//   FINAL_T (bf16 destinations with tensor maps): [hi | lo | W], W the
+//   destination's 32 x 32 block in destination orientation, loaded by TMA
+//   with hi and lo, updated in place and stored back by TMA.
 // With the swizzles, one lane per row accessing 16-byte chunks of its row,
 // and eight lanes covering one row, are free of bank conflicts.
 template <int MODE, int XSLOTS = 2>
 struct EpiLayout {
   static constexpr bool kMN = ModeTraits<MODE>::kMN;
-  static constexpr bool kLoadX = (MODE == MODE_UPDATE || MODE == MODE_FINAL);
+  static constexpr bool kLoadX = (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_FINAL_T);
   static constexpr int SLOTS = kLoadX ? XSLOTS : 1;        // input blocks in flight per warp
-  static constexpr int SLOT_BYTES = 4096;
+  static constexpr int SLOT_BYTES = MODE == MODE_FINAL_T ? 6144 : 4096;
   static constexpr int LO_OFF = 2048;                 // lo plane within a slot
+  static constexpr int W_OFF = 4096;                  // FINAL_T: destination block within a slot
   static constexpr int WARP_BYTES = SLOTS * SLOT_BYTES;   // a multiple of 1024
   static constexpr int BYTES = kMN ? EPI_WARPS * WARP_BYTES : 0;
 };
@@ -98,6 +103,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int q) {
 __device__ __forceinline__ uint32_t sw64_off(int r, int q) {
   return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
 }
+// byte offset of bf16 element (r, c) of a 32 x 32 block, 64-byte rows, 64-byte swizzle
+__device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_off(r, c >> 3) + 2u * (c & 7); }
 
 __device__ __forceinline__ void unpack8(const uint4& raw, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -241,6 +248,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   // ---- input prefetch, in this warp's block order, at most SLOTS blocks ahead
   int pf_t = et.t0, pf_blk = 0;
   uint32_t issued = 0, done = 0;
+  int wmap_b = -1;                 // FINAL_T: the last matrix whose tensor map lane 0 acquired
   auto issue_next = [&]() {
     while (pf_t < p.num_tiles) {
       int b, i, j;
@@ -252,9 +260,26 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
           const int slot = static_cast<int>(issued % L::SLOTS);
           const uint32_t dst = wsm + slot * L::SLOT_BYTES;
           const int x = g0 + 32 * pf_blk, y = i * TROWS + et.row_off + quad * 32;
-          mbar_arrive_expect_tx(&xfull[slot], L::SLOT_BYTES);
-          tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
-          tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
+          if constexpr (MODE == MODE_FINAL_T) {
+            // the destination block too (unless alpha = 0: nothing to read)
+            const OutEntry& oe = p.out[b];
+            const bool wread = oe.alpha != 0.f;
+            if (b != wmap_b) {
+              tensormap_acquire(&p.wmap[b]);
+              wmap_b = b;
+            }
+            mbar_arrive_expect_tx(&xfull[slot], wread ? L::SLOT_BYTES : L::W_OFF);
+            tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
+            tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
+            if (wread) {
+              const bool tr = oe.transposed != 0;
+              tma_load_3d(dst + L::W_OFF, &p.wmap[b], &xfull[slot], tr ? y : x, tr ? x : y, 0);
+            }
+          } else {
+            mbar_arrive_expect_tx(&xfull[slot], L::SLOT_BYTES);
+            tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
+            tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
+          }
         }
         ++issued;
         ++pf_blk;
@@ -276,7 +301,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   for (int t = et.t0; t < p.num_tiles; t += et.tstep) {
     int b, i, j;
     decode_tile<MODE>(p, t, b, i, j);
-    if (MODE != MODE_UPDATE) {
+    if (MODE == MODE_FINAL || MODE == MODE_G_FINAL) {
       // the tile's first block of old destination values, under the main loop
       const int g0p = j * BN + cbeg;
       if (g0p < p.n) prefetch_out_block(out_block(p.out[b], i * TROWS + et.row_off + quad * 32, g0p, p.m, p.n), lane, wpre);
@@ -347,6 +372,65 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
           const uint32_t src = wsm + slot * L::SLOT_BYTES;
           tma_store_3d(map_xo, src, gcb, row0, b);
           tma_store_3d(map_xl, src + L::LO_OFF, gcb, row0, b);
+          bulk_commit_group();
+          bulk_wait_read_all();          // the slot may be refilled
+        }
+        __syncwarp();
+      } else if constexpr (MODE == MODE_FINAL_T) {
+        // the block's correction terms into registers; the destination block
+        // (destination orientation) is updated in place in the slot:
+        // W = alpha W + beta O, rounded once to bf16, then stored by TMA
+        float corr[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float hi[8], lo[8];
+          unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)), hi);
+          unpack8(*reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)), lo);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd - pdb, hi[e], pd * lo[e]);
+        }
+        const bool tr = oe.transposed != 0;
+        const bool wread = oe.alpha != 0.f;
+        uint8_t* wsl = sbuf + L::W_OFF;
+#pragma unroll
+        for (int h = 0; h < 32; h += 16) {
+          float v[16];
+          tmem_ld16(tb + static_cast<uint32_t>(32 * k + h), v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = s * (v[e] + corr[h + e]);
+          if (tr) {
+            // destination row = block column c, column = block row (this lane)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              unsigned short* wp = reinterpret_cast<unsigned short*>(wsl + sw64_elem(h + e, lane));
+              const float old = wread ? bf2f(__ushort_as_bfloat16(*wp)) : 0.f;
+              *wp = __bfloat16_as_ushort(f2bf(fmaf(oe.alpha, old, oe.beta * v[e])));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              uint4* wq = reinterpret_cast<uint4*>(wsl + sw64_off(lane, (h >> 3) + q));
+              float old[8];
+              if (wread) {
+                unpack8(*wq, old);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) old[e] = 0.f;
+              }
+              uint4 nw;
+              uint32_t* w32 = reinterpret_cast<uint32_t*>(&nw);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w32[e] = pack_bf16x2(fmaf(oe.alpha, old[2 * e], oe.beta * v[8 * q + 2 * e]),
+                                     fmaf(oe.alpha, old[2 * e + 1], oe.beta * v[8 * q + 2 * e + 1]));
+              *wq = nw;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.m) {   // a block starting past the destination stores nothing
+          tma_store_3d(&p.wmap[b], wsm + slot * L::SLOT_BYTES + L::W_OFF, tr ? row0 : gcb, tr ? gcb : row0, 0);
           bulk_commit_group();
           bulk_wait_read_all();          // the slot may be refilled
         }
@@ -426,7 +510,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   if (lane == 0) {
     for (uint32_t u = done; u < issued; ++u)
       mbar_wait_bounded(&xfull[u % L::SLOTS], (u / L::SLOTS) & 1u, nullptr, DRAIN_NS);
-    if (MODE == MODE_UPDATE) bulk_wait_all();
+    if (MODE == MODE_UPDATE || MODE == MODE_FINAL_T) bulk_wait_all();
   }
   __syncwarp();
 }
@@ -452,8 +536,6 @@ struct SymEpi {
   static constexpr int BYTES = kTma ? EPI_WARPS * SYM_WARP_BYTES : 0;
 };
 
-// byte offset of bf16 element (r, c) of a 32 x 32 block, 64-byte rows, 64-byte swizzle
-__device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_off(r, c >> 3) + 2u * (c & 7); }
 
 // 32 bf16 of one row from column gc (zeros at and beyond column m), raw
 __device__ __forceinline__ void load_row32_bf16(const __nv_bfloat16* rowp, int gc, int m, uint4* a) {
