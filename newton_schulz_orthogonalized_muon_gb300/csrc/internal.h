@@ -86,7 +86,8 @@ enum NsMode : int {
   MODE_G_P = 5,
   MODE_G_PROD = 6,
   MODE_G_FINAL = 7,
-  MODE_FINAL_T = 8          // FINAL into bf16 destinations through per-matrix tensor maps
+  MODE_FINAL_T = 8,         // FINAL into bf16 destinations through per-matrix tensor maps
+  MODE_G_FINAL_T = 9        // G_FINAL likewise
 };
 
 struct NsGemmParams {
@@ -112,7 +113,7 @@ struct NsGemmParams {
   float* xf_out;                // fp32 path: new X
   long long ldx;
   const OutEntry* out;          // FINAL destinations [batch]
-  // FINAL_T: one tensor map per destination [batch], 3-D {dest cols, dest
+  // FINAL_T / G_FINAL_T: one tensor map per destination [batch], 3-D {dest cols, dest
   // rows, 1}, bf16, 32 x 32 boxes with 64-byte swizzle (encode_box32), in
   // global memory (64-byte aligned)
   const CUtensorMap* wmap;

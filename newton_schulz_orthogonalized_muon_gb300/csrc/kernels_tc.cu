@@ -66,10 +66,11 @@ using namespace tc;
 
 // UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
 // 4 KB slot, which leaves room for a fourth main-loop stage at BN = 256;
-// FINAL keeps two.
+// FINAL keeps two, FINAL_T one (6 KB), G_FINAL_T two 2 KB slots (free: the
+// stage count is the same with one).
 template <int MODE>
 struct OneSlots {
-  static constexpr int v = MODE == MODE_FINAL ? 2 : 1;
+  static constexpr int v = (MODE == MODE_FINAL || MODE == MODE_G_FINAL_T) ? 2 : 1;
 };
 
 template <int MODE, int BN, int AP, int BP>
@@ -348,12 +349,14 @@ cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& a0, co
       case MODE_G_P: return launch_one<MODE_G_P, 128, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
       case MODE_G_PROD: return launch_one<MODE_G_PROD, 128, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
       case MODE_G_FINAL: return launch_one<MODE_G_FINAL, 128, 2, 1>(a0, a1, b0, b0, b0, b0, b0, p, grid, s);
+      case MODE_G_FINAL_T: return launch_one<MODE_G_FINAL_T, 128, 2, 1>(a0, a1, b0, b0, b0, b0, b0, p, grid, s);
     }
   } else if (bn == 256) {
     switch (mode) {
       case MODE_G_P: return launch_one<MODE_G_P, 256, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
       case MODE_G_PROD: return launch_one<MODE_G_PROD, 256, 2, 2>(a0, a1, b0, b1, b0, so_lo, so, p, grid, s);
       case MODE_G_FINAL: return launch_one<MODE_G_FINAL, 256, 2, 1>(a0, a1, b0, b0, b0, b0, b0, p, grid, s);
+      case MODE_G_FINAL_T: return launch_one<MODE_G_FINAL_T, 256, 2, 1>(a0, a1, b0, b0, b0, b0, b0, p, grid, s);
     }
   }
   return cudaErrorInvalidValue;

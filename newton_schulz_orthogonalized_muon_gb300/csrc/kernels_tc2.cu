@@ -61,7 +61,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   using C = PairCfg<MODE, AP, BP>;
   using L = EpiLayout<MODE, PairSlots<MODE>::v>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
-  static_assert(MODE != MODE_G_FINAL, "G_FINAL runs on the one-CTA kernel");
+  static_assert(MODE != MODE_G_FINAL && MODE != MODE_G_FINAL_T, "G_FINAL runs on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;                 // 1024-aligned

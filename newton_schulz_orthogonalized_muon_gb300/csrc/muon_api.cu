@@ -371,6 +371,8 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
     const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
     const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+    const CUtensorMap* wmap_d =
+        g.chunk_wmap[c] == kNoMaps ? nullptr : reinterpret_cast<const CUtensorMap*>(dbase + g.chunk_wmap[c]);
     PrepParams pp{};
     pp.src = src_d;
     pp.mu = mu;
@@ -477,13 +479,15 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     NsGemmParams f = p;
     f.scale = scale;
     f.sym_in = hi[qcur];
+    f.wmap = wmap_d;
     if (tc) {
       f.mi = mi;
       f.tiles_per_mat = mi * nj;
       f.num_tiles = cnt * mi * nj;
       const int grid = std::min(f.num_tiles, h->num_sms);
       MUON_LAUNCH(MUON_K_FINAL,
-                  launch_ns_gemm_tc_planes(MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur], map_xmn, map_xmn, map_xmn, map_xmn, f,
+                  launch_ns_gemm_tc_planes(wmap_d != nullptr ? MODE_G_FINAL_T : MODE_G_FINAL, g.bn_upd, mhi[qcur], mlo[qcur],
+                                           map_xmn, map_xmn, map_xmn, map_xmn, f,
                                            grid, stream),
                   "gram final");
     } else {
@@ -571,7 +575,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
       const size_t oo = arena_push(arena, out.data(), cnt);
       g.chunk_off.emplace_back(so, oo);
       std::vector<CUtensorMap> maps;
-      const bool tma_out = tc && !gram && steps > 0 && h->final_tma && encode_dest_maps(h, g, out, &maps);
+      const bool tma_out = tc && steps > 0 && h->final_tma && encode_dest_maps(h, g, out, &maps);
       g.chunk_wmap.push_back(tma_out ? arena_push(arena, maps.data(), maps.size()) : kNoMaps);
     }
   }

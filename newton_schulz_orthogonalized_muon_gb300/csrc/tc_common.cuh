@@ -23,7 +23,9 @@ struct ModeTraits {
   static constexpr bool kSym = (MODE == MODE_SYRK || MODE == MODE_POLY || MODE == MODE_G_R0 ||
                                 MODE == MODE_G_P || MODE == MODE_G_PROD);
   static constexpr bool kMN =
-      (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_G_FINAL || MODE == MODE_FINAL_T);
+      (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_G_FINAL || MODE == MODE_FINAL_T ||
+       MODE == MODE_G_FINAL_T);
+  static constexpr bool kTmaOut = (MODE == MODE_FINAL_T || MODE == MODE_G_FINAL_T);   // destinations by TMA
   static constexpr bool kKn = (MODE == MODE_SYRK || MODE == MODE_G_R0);   // K = n (else K = m)
   static constexpr bool kPlanesOut = (MODE == MODE_G_R0 || MODE == MODE_G_P || MODE == MODE_G_PROD);
 };
@@ -80,17 +82,18 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
 //   destination row.
 //   FINAL_T (bf16 destinations with tensor maps): [hi | lo | W], W the
 //   destination's 32 x 32 block in destination orientation, loaded by TMA
-//   with hi and lo, updated in place and stored back by TMA.
+//   with hi and lo, updated in place and stored back by TMA; G_FINAL_T: [W].
 // With the swizzles, one lane per row accessing 16-byte chunks of its row,
 // and eight lanes covering one row, are free of bank conflicts.
 template <int MODE, int XSLOTS = 2>
 struct EpiLayout {
   static constexpr bool kMN = ModeTraits<MODE>::kMN;
   static constexpr bool kLoadX = (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_FINAL_T);
-  static constexpr int SLOTS = kLoadX ? XSLOTS : 1;        // input blocks in flight per warp
-  static constexpr int SLOT_BYTES = MODE == MODE_FINAL_T ? 6144 : 4096;
+  static constexpr bool kFill = kLoadX || ModeTraits<MODE>::kTmaOut;   // slots filled by TMA
+  static constexpr int SLOTS = kFill ? XSLOTS : 1;         // input blocks in flight per warp
+  static constexpr int SLOT_BYTES = MODE == MODE_FINAL_T ? 6144 : MODE == MODE_G_FINAL_T ? 2048 : 4096;
   static constexpr int LO_OFF = 2048;                 // lo plane within a slot
-  static constexpr int W_OFF = 4096;                  // FINAL_T: destination block within a slot
+  static constexpr int W_OFF = MODE == MODE_G_FINAL_T ? 0 : 4096;   // destination block within a slot
   static constexpr int WARP_BYTES = SLOTS * SLOT_BYTES;   // a multiple of 1024
   static constexpr int BYTES = kMN ? EPI_WARPS * WARP_BYTES : 0;
 };
@@ -260,7 +263,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
           const int slot = static_cast<int>(issued % L::SLOTS);
           const uint32_t dst = wsm + slot * L::SLOT_BYTES;
           const int x = g0 + 32 * pf_blk, y = i * TROWS + et.row_off + quad * 32;
-          if constexpr (MODE == MODE_FINAL_T) {
+          if constexpr (ModeTraits<MODE>::kTmaOut) {
             // the destination block too (unless alpha = 0: nothing to read)
             const OutEntry& oe = p.out[b];
             const bool wread = oe.alpha != 0.f;
@@ -269,8 +272,10 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
               wmap_b = b;
             }
             mbar_arrive_expect_tx(&xfull[slot], wread ? L::SLOT_BYTES : L::W_OFF);
-            tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
-            tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
+            if (L::kLoadX) {
+              tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
+              tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
+            }
             if (wread) {
               const bool tr = oe.transposed != 0;
               tma_load_3d(dst + L::W_OFF, &p.wmap[b], &xfull[slot], tr ? y : x, tr ? x : y, 0);
@@ -289,7 +294,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
       pf_blk = 0;
     }
   };
-  if (L::kLoadX) {
+  if (L::kFill) {
 #pragma unroll
     for (int k = 0; k < L::SLOTS; ++k) issue_next();
   }
@@ -330,9 +335,9 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
 #pragma unroll 1
     for (int k = 0; k < nb; ++k) {
       const int gcb = g0 + 32 * k;
-      const int slot = L::kLoadX ? static_cast<int>(done % L::SLOTS) : 0;
+      const int slot = L::kFill ? static_cast<int>(done % L::SLOTS) : 0;
       uint8_t* sbuf = wbuf + slot * L::SLOT_BYTES;
-      if (L::kLoadX && !mbar_wait_warp(&xfull[slot], (done / L::SLOTS) & 1u, abort, p.timeout_ns)) {
+      if (L::kFill && !mbar_wait_warp(&xfull[slot], (done / L::SLOTS) & 1u, abort, p.timeout_ns)) {
         if (lane == 0) raise_timeout(abort, p.err);
         ok = false;
         break;
@@ -376,18 +381,24 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
           bulk_wait_read_all();          // the slot may be refilled
         }
         __syncwarp();
-      } else if constexpr (MODE == MODE_FINAL_T) {
-        // the block's correction terms into registers; the destination block
-        // (destination orientation) is updated in place in the slot:
-        // W = alpha W + beta O, rounded once to bf16, then stored by TMA
+      } else if constexpr (ModeTraits<MODE>::kTmaOut) {
+        // the block's correction terms (FINAL_T) into registers; the
+        // destination block (destination orientation) is updated in place in
+        // the slot: W = alpha W + beta O, rounded once to bf16, then stored
+        // by TMA
         float corr[32];
+        if constexpr (L::kLoadX) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float hi[8], lo[8];
-          unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)), hi);
-          unpack8(*reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)), lo);
+          for (int q = 0; q < 4; ++q) {
+            float hi[8], lo[8];
+            unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)), hi);
+            unpack8(*reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)), lo);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd - pdb, hi[e], pd * lo[e]);
+            for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd - pdb, hi[e], pd * lo[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) corr[e] = 0.f;
         }
         const bool tr = oe.transposed != 0;
         const bool wread = oe.alpha != 0.f;
@@ -491,7 +502,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         __syncwarp();
       }
       ++done;
-      if (L::kLoadX) issue_next();
+      if (L::kFill) issue_next();
     }
     if (!ok) break;
     tc_fence_before();
@@ -510,7 +521,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   if (lane == 0) {
     for (uint32_t u = done; u < issued; ++u)
       mbar_wait_bounded(&xfull[u % L::SLOTS], (u / L::SLOTS) & 1u, nullptr, DRAIN_NS);
-    if (MODE == MODE_UPDATE || MODE == MODE_FINAL_T) bulk_wait_all();
+    if (MODE == MODE_UPDATE || ModeTraits<MODE>::kTmaOut) bulk_wait_all();
   }
   __syncwarp();
 }

@@ -1,4 +1,5 @@
-"""FINAL through per-matrix tensor maps (FINAL_T) against the generic FINAL.
+"""FINAL through per-matrix tensor maps (FINAL_T, and G_FINAL_T for the Gram
+method's last product) against the generic FINAL.
 
 When every destination of a chunk is bf16 with a 16-byte aligned base and
 row stride, the last update product loads each destination block by TMA
@@ -68,8 +69,8 @@ def _inputs(seed):
     return W, G
 
 
-@pytest.mark.parametrize("kernel", ["pair", "single"])
-def test_final_tma_matches_generic_bitwise(handles, kernel):
+@pytest.mark.parametrize("kernel,method", [("pair", "standard"), ("single", "standard"), ("pair", "gram")])
+def test_final_tma_matches_generic_bitwise(handles, kernel, method):
     pkg, hs = handles
     h_tma, h_gen = hs[kernel]
     W, G = _inputs(300)
@@ -78,7 +79,7 @@ def test_final_tma_matches_generic_bitwise(handles, kernel):
     for h in (h_tma, h_gen):
         w = [x.clone() for x in W]
         m = [torch.zeros(x.shape, device="cuda") for x in W]
-        pkg.muon_step(w, G, m, lr=0.02, wd=0.1, split_heads=split, handle=h)
+        pkg.muon_step(w, G, m, lr=0.02, wd=0.1, split_heads=split, ns_method=method, handle=h)
         assert h.check() == 0
         outs.append(w)
     for (name, shape, _), a, b in zip(SPECS, outs[0], outs[1]):
@@ -127,15 +128,17 @@ def test_misaligned_destination_falls_back(handles):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("shape", [(2048, 2304), (1408, 2048), (2048, 1408), (130, 512)])
-def test_orthogonalize_in_place_matches_generic(handles, shape):
+@pytest.mark.parametrize("shape,method", [((2048, 2304), "standard"), ((1408, 2048), "standard"),
+                                          ((2048, 1408), "standard"), ((130, 512), "standard"),
+                                          ((256, 4096), "gram"), ((1024, 700), "gram")])
+def test_orthogonalize_in_place_matches_generic(handles, shape, method):
     """alpha = 0: the destination block is not read, only written."""
     pkg, hs = handles
     X = torch.tensor(wl.lowrank_grad(600, shape[0], shape[1], 64)).to(torch.bfloat16).cuda()
     outs = []
     for h in hs["pair"]:
         y = X.clone()
-        pkg.muon_orthogonalize(y, handle=h)
+        pkg.muon_orthogonalize(y, ns_method=method, handle=h)
         assert h.check() == 0
         outs.append(y)
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
