@@ -36,6 +36,7 @@ METRIC = "Muon step ms & Newton-Schulz TFLOP/s (bf16, % tensor peak) on 1 GB300"
 UNIT = "TFLOP/s"
 LR, WD, MU = 0.02, 0.1, 0.95
 NS_STEPS = 5
+E2E_SLICE_BYTES = 2 << 30      # parameters per muon_step call of the pipelined e2e loop
 
 
 def parse_args(argv=None):
@@ -441,12 +442,17 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     its gradients host->device from pinned memory and reads the updated
     parameters back device->host.
 
-    "pipelined" (the reported value): the gradients of step k+1 are copied in
-    on one side stream and the parameters of step k are read back on another
-    (from a device snapshot taken right after the step) while step k+1
-    computes, as a training loop would overlap them; every step's copies are
-    inside the timed region.  "serial": copy in, step, copy out, one after the
-    other on one stream."""
+    "pipelined" (the reported value): the step is issued as several
+    muon_step calls, one per slice of at most E2E_SLICE_BYTES of parameters
+    within a same-shape group, groups in the library's order (ascending
+    (m, n)); the gradients of step k+1 are copied in on one side stream while
+    step k computes, and each slice's parameters are read back on another
+    side stream as soon as that slice's call has finished, while the later
+    slices compute.  Step k+1's call for a slice waits for the read-back of
+    the same slice from step k (it overwrites those parameters), so no device
+    snapshot is needed and only the last slice's read-back is exposed.  Every
+    step's copies are inside the timed region.  "serial": copy in, step, copy
+    out, one after the other on one stream."""
     import torch
     import newton_schulz_orthogonalized_muon_gb300 as pkg
     # one contiguous pinned allocation per direction, viewed per tensor: many
@@ -504,13 +510,28 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     h2d_ms = sum(m[0].elapsed_time(m[1]) for m in ev) / steps
     d2h_ms = sum(m[2].elapsed_time(m[3]) for m in ev) / steps
 
-    # pipelined: two device gradient buffers, one device snapshot of the params
+    # pipelined: two device gradient buffers; calls per same-shape group
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+    by_group = {}
+    for i, s_ in enumerate(specs):
+        by_group.setdefault(flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads), []).append(i)
+    order = []
+    for key in sorted(by_group):
+        cur_slice, nbytes = [], 0
+        for i in by_group[key]:
+            b = W[i].numel() * W[i].element_size()
+            if cur_slice and nbytes + b > E2E_SLICE_BYTES:
+                order.append(cur_slice)
+                cur_slice, nbytes = [], 0
+            cur_slice.append(i)
+            nbytes += b
+        order.append(cur_slice)
     G2 = [torch.empty_like(g) for g in G]
-    Wsnap = [torch.empty_like(w) for w in W]
     gbuf = [G, G2]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     in_done = [torch.cuda.Event(), torch.cuda.Event()]
-    snap_done, out_done = torch.cuda.Event(), torch.cuda.Event()
+    group_done = [torch.cuda.Event() for _ in order]
+    out_done = [torch.cuda.Event() for _ in order]
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -532,19 +553,20 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
                     gd.copy_(gh, non_blocking=True)
                 in_done[(k + 1) % 2].record(s_in)
         stream.wait_event(in_done[k % 2])
-        step(cur)
+        for gi, idx in enumerate(order):
+            if k >= 1:
+                stream.wait_event(out_done[gi])         # step k-1's parameters of this group are read back
+            pkg.muon_step([W[i] for i in idx], [cur[i] for i in idx], [M[i] for i in idx], lr=LR, wd=WD, mu=MU,
+                          nesterov=True, ns_method=args.ns_method, ns_steps=NS_STEPS,
+                          split_heads=[split[i] for i in idx], handle=h)
+            group_done[gi].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(group_done[gi])
+                for i in idx:
+                    Wh[i].copy_(W[i], non_blocking=True)
+                out_done[gi].record(s_out)
         step_done_prev = torch.cuda.Event()
         step_done_prev.record(stream)
-        if k >= 1:
-            stream.wait_event(out_done)                 # snapshot buffer free again
-        for ws, wd in zip(Wsnap, W):
-            ws.copy_(wd, non_blocking=True)
-        snap_done.record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(snap_done)
-            for wh, ws in zip(Wh, Wsnap):
-                wh.copy_(ws, non_blocking=True)
-            out_done.record(s_out)
     stream.wait_stream(s_out)
     stream.wait_stream(s_in)
     t1.record(stream)
@@ -555,10 +577,12 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
         t = torch.tensor([ms, serial_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, serial_ms = float(t[0]), float(t[1])
-    del G2, Wsnap
+    del G2
     torch.cuda.empty_cache()
     return {"value": alg_all / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "mode": "pipelined (copies overlapped with compute)",
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "mode": f"pipelined (copies overlapped with compute; {len(order)} calls per step, one per slice of at most "
+                    f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
             "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9}
 

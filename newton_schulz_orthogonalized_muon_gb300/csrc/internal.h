@@ -156,6 +156,10 @@ cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CU
                                       const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s);
 int ns_gemm_pair_max_pairs();
 
+// Device copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from `src`, which may be mapped pinned host memory, to device memory.
+cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
+
 // 3-D map {cols, rows, batch} (row stride ld elements, matrices rows * ld
 // apart) with a 32 x 32 box: fp32 with 128-byte swizzle (32 floats = one
 // 128-byte row) or bf16 with 64-byte swizzle: the epilogue's blocks of the

@@ -301,7 +301,23 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns, unsigned* er
   }
 }
 
+// Descriptor arena upload: 16-byte words from the pinned staging buffer
+// (read through its device address) into the device descriptor buffer.
+__global__ void desc_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, size_t n16) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
 // ------------------------------------------------------------- launchers
+cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<size_t>((n16 + threads - 1) / threads, 1024));
+  desc_copy_kernel<<<blocks, threads, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
+  return cudaGetLastError();
+}
 cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s) {
   if (batch == 0 || tiles_per_mat == 0) return cudaSuccess;
   dim3 grid(tiles_per_mat, batch);

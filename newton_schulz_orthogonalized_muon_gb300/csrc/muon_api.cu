@@ -54,10 +54,15 @@ struct muon_handle_s {
   size_t ws_cap = 0;
   void* desc = nullptr;
   size_t desc_cap = 0;
-  void* hstage = nullptr;
-  size_t hstage_cap = 0;
-  cudaEvent_t stage_ev = nullptr;
-  bool stage_pending = false;
+  // pinned staging buffers of the descriptor arena, used in turn, each with
+  // the event after which the device has read it
+  static constexpr int kStages = 3;
+  void* hstage[kStages] = {};
+  const void* hstage_dev[kStages] = {};   // the same memory as the device addresses it
+  size_t hstage_cap[kStages] = {};
+  cudaEvent_t stage_ev[kStages] = {};
+  bool stage_pending[kStages] = {};
+  int stage_next = 0;
   unsigned* err = nullptr;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   std::string last;
@@ -158,13 +163,19 @@ muon_status_t ensure_ws(muon_handle_t h, size_t bytes) {
 }
 
 // Copy a host descriptor arena to the handle's device descriptor buffer on
-// `stream` through a pinned staging buffer.
+// `stream` through a pinned staging buffer (one of kStages, taken in turn).
+// The copy is a kernel reading the pinned buffer through its device address,
+// not a copy-engine transfer: a cudaMemcpyAsync here queues behind whatever
+// host<->device copies the caller has in flight on other streams (a step's
+// gradients, say), which held every call that overlapped them.
 muon_status_t upload(muon_handle_t h, const std::vector<uint8_t>& arena, cudaStream_t stream, void** dev) {
   *dev = nullptr;
   if (arena.empty()) return MUON_OK;
-  if (h->stage_pending) {
-    MUON_CUDA_TRY(cudaEventSynchronize(h->stage_ev), "descriptor staging wait");
-    h->stage_pending = false;
+  const int k = h->stage_next;
+  h->stage_next = (k + 1) % muon_handle_s::kStages;
+  if (h->stage_pending[k]) {
+    MUON_CUDA_TRY(cudaEventSynchronize(h->stage_ev[k]), "descriptor staging wait");
+    h->stage_pending[k] = false;
   }
   if (arena.size() > h->desc_cap) {
     if (h->desc != nullptr) cudaFree(h->desc);
@@ -177,22 +188,29 @@ muon_status_t upload(muon_handle_t h, const std::vector<uint8_t>& arena, cudaStr
     }
     h->desc_cap = cap;
   }
-  if (arena.size() > h->hstage_cap) {
-    if (h->hstage != nullptr) cudaFreeHost(h->hstage);
-    h->hstage = nullptr;
-    h->hstage_cap = 0;
+  if (arena.size() > h->hstage_cap[k]) {
+    if (h->hstage[k] != nullptr) cudaFreeHost(h->hstage[k]);
+    h->hstage[k] = nullptr;
+    h->hstage_dev[k] = nullptr;
+    h->hstage_cap[k] = 0;
     const size_t cap = align_up(arena.size(), size_t(1) << 20);
-    if (cudaMallocHost(&h->hstage, cap) != cudaSuccess) {
+    void* dptr = nullptr;
+    if (cudaHostAlloc(&h->hstage[k], cap, cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer(&dptr, h->hstage[k], 0) != cudaSuccess) {
       cudaGetLastError();
+      if (h->hstage[k] != nullptr) cudaFreeHost(h->hstage[k]);
+      h->hstage[k] = nullptr;
       return fail(h, MUON_ERR_WORKSPACE, "pinned staging allocation failed");
     }
-    h->hstage_cap = cap;
+    h->hstage_dev[k] = dptr;
+    h->hstage_cap[k] = cap;
   }
-  std::memcpy(h->hstage, arena.data(), arena.size());
-  MUON_CUDA_TRY(cudaMemcpyAsync(h->desc, h->hstage, arena.size(), cudaMemcpyHostToDevice, stream),
-                "descriptor upload");
-  MUON_CUDA_TRY(cudaEventRecord(h->stage_ev, stream), "descriptor staging event");
-  h->stage_pending = true;
+  std::memcpy(h->hstage[k], arena.data(), arena.size());
+  // both buffers are whole MiB, so the 16-byte rounding stays inside them
+  MUON_CUDA_TRY(launch_desc_copy(h->desc, h->hstage_dev[k], align_up(arena.size(), 16), stream), "descriptor upload");
+  ++h->launches;
+  MUON_CUDA_TRY(cudaEventRecord(h->stage_ev[k], stream), "descriptor staging event");
+  h->stage_pending[k] = true;
   *dev = h->desc;
   return MUON_OK;
 }
@@ -863,10 +881,14 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
   }
   h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
   if (const char* ft = std::getenv("MUON_FINAL_TMA")) h->final_tma = ft[0] != '0';
-  if (cudaMalloc(&h->err, sizeof(unsigned)) != cudaSuccess || cudaMemset(h->err, 0, sizeof(unsigned)) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->stage_ev, cudaEventDisableTiming) != cudaSuccess) {
+  bool ok = cudaMalloc(&h->err, sizeof(unsigned)) == cudaSuccess && cudaMemset(h->err, 0, sizeof(unsigned)) == cudaSuccess;
+  for (int k = 0; ok && k < muon_handle_s::kStages; ++k)
+    ok = cudaEventCreateWithFlags(&h->stage_ev[k], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
     cudaGetLastError();
     if (h->err) cudaFree(h->err);
+    for (int k = 0; k < muon_handle_s::kStages; ++k)
+      if (h->stage_ev[k]) cudaEventDestroy(h->stage_ev[k]);
     delete h;
     return MUON_ERR_WORKSPACE;
   }
@@ -880,9 +902,11 @@ muon_status_t muon_handle_destroy(muon_handle_t h) {
   cudaDeviceSynchronize();
   if (h->ws) cudaFree(h->ws);
   if (h->desc) cudaFree(h->desc);
-  if (h->hstage) cudaFreeHost(h->hstage);
+  for (int k = 0; k < muon_handle_s::kStages; ++k) {
+    if (h->hstage[k]) cudaFreeHost(h->hstage[k]);
+    if (h->stage_ev[k]) cudaEventDestroy(h->stage_ev[k]);
+  }
   if (h->err) cudaFree(h->err);
-  if (h->stage_ev) cudaEventDestroy(h->stage_ev);
   for (auto& r : h->prof) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
