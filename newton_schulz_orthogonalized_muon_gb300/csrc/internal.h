@@ -103,6 +103,8 @@ struct NsGemmParams {
   void* sym_out;                // bf16 (tensor-core path) or fp32 (fp32 path)
   const void* sym_in;           // POLY: the A matrix for the b*A term (G_P: R hi plane)
   void* sym_out_lo;             // Gram modes: lo plane of the output
+  int sym_n128;                 // CTA-pair symmetric products: tiles with at most 128 valid
+                                // columns run N = 128 (B through a 64-row-box map)
   const void* sym_in_lo;        // G_P: R lo plane
   const void* op_b;             // fp32 path, G_PROD: the second factor
   float* pdiag;                 // tensor-core path: fp32 diagonal of P [batch][m]
@@ -145,9 +147,12 @@ cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0
 // CTA-pair variant (tcgen05 cta_group::2, 256 x 256 tiles): `pairs`
 // clusters of two CTAs; tiles use 256-row blocks (p.tri / p.mi in 256-row
 // units) and, for UPDATE / FINAL, 256-column blocks.
+// map_b64 (SYRK / POLY, optional): the B operand again with 64-row boxes;
+// given, tiles of a ragged last column block with at most 128 valid columns
+// run N = 128 instead of 256.
 cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                const CUtensorMap& map_so, const CUtensorMap& map_so_lo, const NsGemmParams& p,
-                               int pairs, cudaStream_t s);
+                               int pairs, cudaStream_t s, const CUtensorMap* map_b64 = nullptr);
 cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                       const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
                                       const NsGemmParams& p, int pairs, cudaStream_t s);

@@ -61,6 +61,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   using C = PairCfg<MODE, AP, BP>;
   using L = EpiLayout<MODE, PairSlots<MODE>::v>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
+  // symmetric products with one B plane: a tile of the ragged last column
+  // block with at most 128 valid columns runs N = 128, each CTA loading 64
+  // rows of B through map_b1 (the same operand with 64-row boxes)
+  constexpr bool kN128 = ModeTraits<MODE>::kSym && BP == 1;
   static_assert(MODE != MODE_G_FINAL && MODE != MODE_G_FINAL_T, "G_FINAL runs on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -101,7 +105,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     tma_prefetch_map(&map_a0);
     tma_prefetch_map(&map_b0);
     if (AP == 2) tma_prefetch_map(&map_a1);
-    if (BP == 2) tma_prefetch_map(&map_b1);
+    if (BP == 2 || (kN128 && p.sym_n128 != 0)) tma_prefetch_map(&map_b1);
     if (L::kLoadX) {
       tma_prefetch_map(&map_xh);
       tma_prefetch_map(&map_xl);
@@ -124,8 +128,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       for (int t = pair; ok && t < p.num_tiles; t += npairs) {
         int b, i, j;
         decode_tile<MODE>(p, t, b, i, j);
+        const bool n128 = kN128 && p.sym_n128 != 0 && p.m - j * PBN <= 128;
         const int arow = i * PBM + static_cast<int>(rank) * 128;     // this CTA's rows of A
-        const int bcol = j * PBN + static_cast<int>(rank) * 128;     // this CTA's half of B
+        const int bcol = j * PBN + static_cast<int>(rank) * (n128 ? 64 : 128);   // this CTA's half of B
+        const uint32_t stage_tx = n128 ? 2 * (C::STAGE_BYTES - C::B_BYTES / 2) : 2 * C::STAGE_BYTES;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort, p.timeout_ns)) {
             raise_timeout(abort, p.err);
@@ -135,7 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + AP * C::A_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);   // the leader's full barrier
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], stage_tx);
 #pragma unroll
           for (int pa = 0; pa < AP; ++pa) {
             const CUtensorMap* ma = pa == 0 ? &map_a0 : &map_a1;
@@ -148,6 +154,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             if (kUpd) {      // X^ read MN-major: 64 columns x 64 K rows per box
               tma_load_3d_pair(sb + pb * C::B_BYTES, mb, fb, bcol, kb * BK, b);
               tma_load_3d_pair(sb + pb * C::B_BYTES + BOX_BYTES, mb, fb, bcol + 64, kb * BK, b);
+            } else if (n128) {   // K-major, N = 128: this CTA's 64 rows of B
+              tma_load_3d_pair(sb, &map_b1, fb, kb * BK, bcol, b);
             } else {         // K-major: this CTA's 128 rows of B in one box
               tma_load_3d_pair(sb + pb * C::B_BYTES, mb, fb, kb * BK, bcol, b);
             }
@@ -171,11 +179,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ----------------------------------------------- MMA issuer (leader)
-      const uint32_t idesc = idesc_bf16_f32(PBM, PBN, kUpd ? 1 : 0);
+      const uint32_t idesc256 = idesc_bf16_f32(PBM, PBN, kUpd ? 1 : 0);
+      const uint32_t idesc128 = idesc_bf16_f32(PBM, 128, kUpd ? 1 : 0);
       int s = 0, acc = 0;
       uint32_t ph = 0, acc_ph = 0;
       bool ok = true;
       for (int t = pair; ok && t < p.num_tiles; t += npairs) {
+        bool n128 = false;
+        if (kN128 && p.sym_n128 != 0) {
+          int b, i, j;
+          decode_tile<MODE>(p, t, b, i, j);
+          n128 = p.m - j * PBN <= 128;
+        }
+        const uint32_t idesc = n128 ? idesc128 : idesc256;
         if (!mbar_wait_bounded(&tempty[acc], acc_ph ^ 1u, abort, p.timeout_ns)) {
           raise_timeout(abort, p.err);
           break;
@@ -311,11 +327,15 @@ int ns_gemm_pair_max_pairs() {
 }
 
 cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& so,
-                               const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s) {
+                               const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s,
+                               const CUtensorMap* b64) {
   if (p.num_tiles == 0) return cudaSuccess;
+  NsGemmParams q = p;
+  q.sym_n128 = (b64 != nullptr && (mode == MODE_SYRK || mode == MODE_POLY)) ? 1 : 0;
+  const CUtensorMap& b1 = q.sym_n128 ? *b64 : b;
   switch (mode) {
-    case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b, b, b, so, p, pairs, s);
-    case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b, b, b, so, p, pairs, s);
+    case MODE_SYRK: return launch_pair<MODE_SYRK, 1, 1>(a, a, b, b1, b, b, so, q, pairs, s);
+    case MODE_POLY: return launch_pair<MODE_POLY, 1, 1>(a, a, b, b1, b, b, so, q, pairs, s);
     case MODE_G_R0: return launch_pair<MODE_G_R0, 1, 1>(a, a, b, b, b, so_lo, so, p, pairs, s);
   }
   return cudaErrorInvalidValue;

@@ -627,13 +627,17 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     float* scale = reinterpret_cast<float*>(ws + R.scale);
 
     __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(ws + R.xlo) : nullptr;
-    CUtensorMap map_x[2], map_xmn[2], map_A, map_B, map_xh[2], map_xl, map_sa, map_sb;
+    CUtensorMap map_x[2], map_xmn[2], map_A, map_A64, map_B, map_xh[2], map_xl, map_sa, map_sb;
+    // pair symmetric products of a ragged m whose last 256-column block has
+    // at most 128 valid columns: those tiles run N = 128 (64-row B boxes)
+    const bool n128 = tc && g.pair && g.m % 256 != 0 && g.m % 256 <= 128;
     if (tc && steps > 0) {
       if (!encode_map(h, &map_x[0], xb[0], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &map_x[1], xb[1], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &map_xmn[0], xb[0], g.n, g.m, g.chunk, g.ldx, 64) ||
           !encode_map(h, &map_xmn[1], xb[1], g.n, g.m, g.chunk, g.ldx, 64) ||
           !encode_map(h, &map_A, symA, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_map(h, &map_A64, symA, g.m, g.m, g.chunk, g.ldm, 64) ||
           !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm) ||
           !encode_box32(h->encode, &map_xh[0], xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
           !encode_box32(h->encode, &map_xh[1], xb[1], false, g.n, g.m, g.chunk, g.ldx) ||
@@ -701,12 +705,16 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           q.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
           q.sym_out = symA;
           const int pairs = std::min(q.num_tiles, h->max_pairs);
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, pairs, stream),
+          MUON_LAUNCH(MUON_K_SYRK,
+                      launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, pairs, stream,
+                                          n128 ? &map_xmn[it & 1] : nullptr),
                       "syrk launch");
           q.scale = nullptr;
           q.sym_in = symA;
           q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream), "poly launch");
+          MUON_LAUNCH(MUON_K_POLY,
+                      launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream, n128 ? &map_A64 : nullptr),
+                      "poly launch");
           NsGemmParams u = p;
           if (g.pair_upd) {
             const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
