@@ -150,7 +150,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int pb = 0; pb < BP; ++pb) {
             const CUtensorMap* mb = pb == 0 ? &map_b0 : &map_b1;
-#pragma unroll
             if (kUpd) {      // X^ read MN-major: 64 columns x 64 K rows per box
               tma_load_3d_pair(sb + pb * C::B_BYTES, mb, fb, bcol, kb * BK, b);
               tma_load_3d_pair(sb + pb * C::B_BYTES + BOX_BYTES, mb, fb, bcol + 64, kb * BK, b);
