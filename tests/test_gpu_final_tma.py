@@ -145,3 +145,26 @@ def test_orthogonalize_in_place_matches_generic(handles, shape, method):
     ref = oracle.newton_schulz(X.double().cpu().numpy())
     got = outs[0].double().cpu().numpy()
     assert float(np.linalg.norm(got - ref) / np.linalg.norm(ref)) < TOL_BF16
+
+
+def test_chunked_group_matches_one_chunk_bitwise(handles):
+    """A workspace limit that splits a group into several chunks gives each
+    chunk its own tensor-map array; the matrices are independent, so the
+    result is the same bits as one chunk."""
+    pkg, _ = handles
+    shape, count = (512, 1536), 6
+    W = [torch.tensor(wl.weight(700 + i, shape)).to(torch.bfloat16).cuda() for i in range(count)]
+    G = [torch.tensor(wl.lowrank_grad(720 + i, shape[0], shape[1], 64)).to(torch.bfloat16).cuda() for i in range(count)]
+    big, small = pkg.MuonHandle(0), pkg.MuonHandle(0)
+    need = pkg.workspace_size([shape] * count, handle=small)
+    small.set_workspace_limit(need // 3)
+    assert pkg.workspace_size([shape] * count, handle=small) < need
+    outs = []
+    for h in (big, small):
+        w = [x.clone() for x in W]
+        m = [torch.zeros(shape, device="cuda") for _ in range(count)]
+        pkg.muon_step(w, G, m, lr=0.02, wd=0.1, handle=h)
+        assert h.check() == 0
+        outs.append(w)
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
