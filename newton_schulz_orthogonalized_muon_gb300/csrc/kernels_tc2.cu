@@ -30,8 +30,8 @@ using namespace tc;
 constexpr int PBM = 256;       // rows of the pair's tile (128 per CTA)
 constexpr int PBN = 256;       // columns of the tile = N of the pair MMA (128 loaded per CTA)
 // UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
-// 4 KB slot, which leaves room for six main-loop stages; FINAL keeps two
-// (five stages), as one slot costs it register spills.
+// 4 KB slot (two measured no faster); FINAL keeps two, as one slot costs it
+// register spills.
 template <int MODE>
 struct PairSlots {
   static constexpr int v = MODE == MODE_FINAL ? 2 : 1;
@@ -46,7 +46,12 @@ struct PairCfg {
   static constexpr int BAR_BYTES = 512;
   // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
   static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
+  // At most five stages although six fit beside the one-slot epilogues: under
+  // the GPU's power cap the sixth stage bought no cycles (the same cycle count
+  // per launch at ~1.4 GHz, where memory latency spans fewer cycles) and the
+  // clock settled ~5% lower with it.
+  static constexpr int STAGES_MAX = 5;
+  static constexpr int STAGES = STAGES_FIT < STAGES_MAX ? STAGES_FIT : STAGES_MAX;
   static constexpr int TMEM_COLS = 2 * PBN;              // double-buffered 256-column accumulator
   static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
   static_assert(STAGES >= 2 && SMEM <= MAX_DYN_SMEM, "shared memory");
