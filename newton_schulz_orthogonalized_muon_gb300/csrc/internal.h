@@ -153,9 +153,11 @@ cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0
 cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                const CUtensorMap& map_so, const CUtensorMap& map_so_lo, const NsGemmParams& p,
                                int pairs, cudaStream_t s, const CUtensorMap* map_b64 = nullptr);
+// slots: epilogue input slots per warp of UPDATE (0: the default one; 2 for
+// short K, where the epilogue bounds a tile)
 cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                       const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
-                                      const NsGemmParams& p, int pairs, cudaStream_t s);
+                                      const NsGemmParams& p, int pairs, cudaStream_t s, int slots = 0);
 cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
                                       const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& so,
                                       const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s);

@@ -30,19 +30,21 @@ using namespace tc;
 constexpr int PBM = 256;       // rows of the pair's tile (128 per CTA)
 constexpr int PBN = 256;       // columns of the tile = N of the pair MMA (128 loaded per CTA)
 // UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
-// 4 KB slot (two measured no faster); FINAL keeps two, as one slot costs it
-// register spills.
+// 4 KB slot (two measured no faster on long K); FINAL keeps two, as one slot
+// costs it register spills.  XS overrides the default: UPDATE with two slots
+// serves short K (m <= 1024), where the epilogue's input latency, not the
+// main loop, bounds a tile; the five-stage ring leaves room for it.
 template <int MODE>
 struct PairSlots {
   static constexpr int v = MODE == MODE_FINAL ? 2 : 1;
 };
 
-template <int MODE, int AP, int BP>
+template <int MODE, int AP, int BP, int XS = PairSlots<MODE>::v>
 struct PairCfg {
   static constexpr int A_BYTES = 128 * BK * 2;           // one plane of this CTA's 128 rows of A
   static constexpr int B_BYTES = 128 * BK * 2;           // one plane of this CTA's half of B
   static constexpr int STAGE_BYTES = AP * A_BYTES + BP * B_BYTES;   // 32 KB with one plane each
-  static constexpr int EPI_BYTES = EpiLayout<MODE, PairSlots<MODE>::v>::BYTES + SymEpi<MODE>::BYTES;
+  static constexpr int EPI_BYTES = EpiLayout<MODE, XS>::BYTES + SymEpi<MODE>::BYTES;
   static constexpr int BAR_BYTES = 512;
   // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
   static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -57,14 +59,14 @@ struct PairCfg {
   static_assert(STAGES >= 2 && SMEM <= MAX_DYN_SMEM, "shared memory");
 };
 
-template <int MODE, int AP, int BP>
+template <int MODE, int AP, int BP, int XS = PairSlots<MODE>::v>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
                         const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
                         const __grid_constant__ CUtensorMap map_xh, const __grid_constant__ CUtensorMap map_xl,
                         const __grid_constant__ CUtensorMap map_xo, const NsGemmParams p) {
-  using C = PairCfg<MODE, AP, BP>;
-  using L = EpiLayout<MODE, PairSlots<MODE>::v>;
+  using C = PairCfg<MODE, AP, BP, XS>;
+  using L = EpiLayout<MODE, XS>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
   // symmetric products with one B plane: a tile of the ragged last column
   // block with at most 128 valid columns runs N = 128, each CTA loading 64
@@ -265,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     et.tempty = nullptr;
     et.tempty_remote[0] = mapa_shared(smem_u32(&tempty[0]), 0);
     et.tempty_remote[1] = mapa_shared(smem_u32(&tempty[1]), 0);
-    mn_epilogue<MODE, PBN, PBM, PairSlots<MODE>::v>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES,
+    mn_epilogue<MODE, PBN, PBM, XS>(p, &map_xh, &map_xl, &map_xo, epi + (warp - 2) * L::WARP_BYTES,
                                 xfull + 2 * (warp - 2), tfull, et, abort, tmem_base, warp, lane);
   }
 
@@ -279,12 +281,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   }
 }
 
-template <int MODE, int AP, int BP>
+template <int MODE, int AP, int BP, int XS = PairSlots<MODE>::v>
 cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
                         const CUtensorMap& xh, const CUtensorMap& xl, const CUtensorMap& xo, const NsGemmParams& p,
                         int pairs, cudaStream_t s) {
-  auto kern = ns_gemm_pair_kernel<MODE, AP, BP>;
-  using C = PairCfg<MODE, AP, BP>;
+  auto kern = ns_gemm_pair_kernel<MODE, AP, BP, XS>;
+  using C = PairCfg<MODE, AP, BP, XS>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
@@ -347,10 +349,12 @@ cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& a, const CUtensorMa
 
 cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& xh,
                                       const CUtensorMap& xl, const CUtensorMap& xo, const NsGemmParams& p, int pairs,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, int slots) {
   if (p.num_tiles == 0) return cudaSuccess;
   switch (mode) {
-    case MODE_UPDATE: return launch_pair<MODE_UPDATE, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
+    case MODE_UPDATE:
+      return slots == 2 ? launch_pair<MODE_UPDATE, 1, 1, 2>(a, a, b, b, xh, xl, xo, p, pairs, s)
+                        : launch_pair<MODE_UPDATE, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
     case MODE_FINAL: return launch_pair<MODE_FINAL, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
     case MODE_FINAL_T: return launch_pair<MODE_FINAL_T, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
   }

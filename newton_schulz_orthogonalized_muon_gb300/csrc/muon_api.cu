@@ -275,6 +275,11 @@ struct GroupPlan {
 
 constexpr size_t kNoMaps = ~size_t(0);
 
+// UPDATE products with K = m up to this run the pair kernel with two epilogue
+// input slots per warp: their main loop per tile is shorter than the latency
+// chain of a one-slot epilogue.
+constexpr int kShortK = 1024;
+
 // One tensor map per destination of a chunk, for FINAL_T: possible when every
 // destination is bf16 with a 16-byte aligned base and row stride (TMA's
 // rules); the map covers the destination in its own orientation (n x m when
@@ -724,7 +729,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
             const int upairs = std::min(u.num_tiles, h->max_pairs);
             MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
                         launch_ns_gemm_pair_update(last ? final_mode : MODE_UPDATE, map_B, map_xmn[it & 1],
-                                                   map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream),
+                                                   map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream,
+                                                   g.m <= kShortK ? 2 : 0),
                         "update launch");
           } else {
             u.mi = mi;
