@@ -437,6 +437,30 @@ def run_adamw(args, ws, dev, stream, h, peaks):
     return out
 
 
+def e2e_slices(specs, param_bytes, limit=None):
+    """The muon_step calls of one pipelined e2e step: parameter indices grouped
+    by the library's same-shape groups (NS dims after the transpose and
+    Muon-Split rules, in ascending (m, n) order, the library's own order),
+    each group cut into consecutive slices of at most `limit` bytes of
+    parameters (at least one matrix per slice)."""
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+    limit = E2E_SLICE_BYTES if limit is None else limit
+    by_group = {}
+    for i, s_ in enumerate(specs):
+        by_group.setdefault(flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads), []).append(i)
+    order = []
+    for key in sorted(by_group):
+        cur, nbytes = [], 0
+        for i in by_group[key]:
+            if cur and nbytes + param_bytes[i] > limit:
+                order.append(cur)
+                cur, nbytes = [], 0
+            cur.append(i)
+            nbytes += param_bytes[i]
+        order.append(cur)
+    return order
+
+
 def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     """Same step through the public API with host buffers: every step copies
     its gradients host->device from pinned memory and reads the updated
@@ -510,22 +534,8 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     h2d_ms = sum(m[0].elapsed_time(m[1]) for m in ev) / steps
     d2h_ms = sum(m[2].elapsed_time(m[3]) for m in ev) / steps
 
-    # pipelined: two device gradient buffers; calls per same-shape group
-    from newton_schulz_orthogonalized_muon_gb300 import flops
-    by_group = {}
-    for i, s_ in enumerate(specs):
-        by_group.setdefault(flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads), []).append(i)
-    order = []
-    for key in sorted(by_group):
-        cur_slice, nbytes = [], 0
-        for i in by_group[key]:
-            b = W[i].numel() * W[i].element_size()
-            if cur_slice and nbytes + b > E2E_SLICE_BYTES:
-                order.append(cur_slice)
-                cur_slice, nbytes = [], 0
-            cur_slice.append(i)
-            nbytes += b
-        order.append(cur_slice)
+    # pipelined: two device gradient buffers; calls per slice of a same-shape group
+    order = e2e_slices(specs, [w.numel() * w.element_size() for w in W])
     G2 = [torch.empty_like(g) for g in G]
     gbuf = [G, G2]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)

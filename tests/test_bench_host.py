@@ -1,0 +1,55 @@
+"""Host-side logic of bench.py (no GPU): the pipelined end-to-end loop's
+slicing of a step into muon_step calls, and the pair-kernel rule that
+labels the roofline kernel."""
+import pytest
+
+import bench
+from newton_schulz_orthogonalized_muon_gb300 import flops
+from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+
+
+def _bytes(specs, esz=2):
+    return [s.shape[0] * s.shape[1] * esz for s in specs]
+
+
+@pytest.mark.parametrize("name", ["llama3-8b", "moonlight-moe", "gpt2-small"])
+def test_e2e_slices_cover_every_parameter_once_in_group_order(name):
+    specs = bench.weight_set(name, None).muon
+    nb = _bytes(specs)
+    order = bench.e2e_slices(specs, nb)
+    flat = [i for sl in order for i in sl]
+    assert sorted(flat) == list(range(len(specs)))
+    dims = [flops.ns_dims(specs[sl[0]].shape[0], specs[sl[0]].shape[1], specs[sl[0]].split_heads) for sl in order]
+    for sl, d in zip(order, dims):
+        # one same-shape group per call, at most the byte limit unless a
+        # single matrix is larger
+        assert all(flops.ns_dims(specs[i].shape[0], specs[i].shape[1], specs[i].split_heads) == d for i in sl)
+        assert len(sl) == 1 or sum(nb[i] for i in sl) <= bench.E2E_SLICE_BYTES
+    assert dims == sorted(dims)                      # the library's group order
+
+
+def test_e2e_slices_cut_only_at_the_limit():
+    specs = [wl.ParamSpec(f"p{i}", (64, 128)) for i in range(10)]
+    nb = _bytes(specs)                               # 16 KiB each
+    order = bench.e2e_slices(specs, nb, limit=3 * nb[0])
+    assert [len(sl) for sl in order] == [3, 3, 3, 1]
+    order = bench.e2e_slices(specs, nb, limit=nb[0] // 2)   # smaller than one matrix
+    assert [len(sl) for sl in order] == [1] * 10
+
+
+def test_e2e_slices_keep_transposed_partners_in_their_group():
+    # 2048 x 1408 is the transpose of 1408 x 2048: one group, as in the library
+    specs = [wl.ParamSpec("up", (1408, 2048)), wl.ParamSpec("down", (2048, 1408)),
+             wl.ParamSpec("q", (2048, 2048), split_heads=16)]
+    order = bench.e2e_slices(specs, _bytes(specs))
+    assert order == [[2], [0, 1]]                    # (128, 2048) sorts before (1408, 2048)
+
+
+@pytest.mark.parametrize("m,kernel,pair", [
+    (4096, "update", True), (4096, "syrk", True), (1408, "syrk", True), (1408, "update", False),
+    (1408, "final", False), (2176, "update", True), (768, "update", True), (640, "syrk", False),
+    (128, "syrk", False)])
+def test_pair_rule_matches_the_library(m, kernel, pair, monkeypatch):
+    monkeypatch.delenv("MUON_TC_PAIR", raising=False)
+    monkeypatch.delenv("MUON_TC_PAIR_MIN_M", raising=False)
+    assert bench.uses_pairs(m, kernel) is pair
