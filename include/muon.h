@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
   MUON_OK = 0,
   MUON_ERR_INVALID_ARG = 1,   /* bad pointer, shape, dtype or count */
-  MUON_ERR_UNSUPPORTED = 2,   /* valid request this build does not run (e.g. no sm_103a device) */
+  MUON_ERR_UNSUPPORTED = 2,   /* valid request this library does not run (e.g. no sm_103a device) */
   MUON_ERR_WORKSPACE = 3,     /* device or pinned workspace allocation failed */
   MUON_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed; see muon_last_error() */
   MUON_ERR_NONFINITE = 5,     /* a Frobenius norm was NaN/Inf (from muon_handle_check) */
