@@ -587,6 +587,12 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
         t = torch.tensor([ms, serial_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, serial_ms = float(t[0]), float(t[1])
+    # this rank's host-link rates (serial copies), then the whole job's bytes
+    h2d_gbs, d2h_gbs = h2d / (h2d_ms / 1e3) / 1e9, d2h / (d2h_ms / 1e3) / 1e9
+    if world > 1:
+        nbytes = torch.tensor([h2d, d2h], device=dev, dtype=torch.float64)
+        dist.all_reduce(nbytes, op=dist.ReduceOp.SUM)
+        h2d, d2h = int(nbytes[0]), int(nbytes[1])
     del G2
     torch.cuda.empty_cache()
     return {"value": alg_all / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
@@ -594,7 +600,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             "mode": f"pipelined (copies overlapped with compute; {len(order)} calls per step, one per slice of at most "
                     f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
-            "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9}
+            "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs}
 
 
 def uses_pairs(m, kernel_class):
