@@ -13,8 +13,8 @@ Prints one JSON line.  `value` is the Newton-Schulz throughput in TFLOP/s
 copies of the set are dealt to the ranks by size-sorted ping-pong ownership
 (weak scaling, no collective inside the step).
 
---impl reference times the fp64 CPU oracle (the reference arm of this
-build) on a bounded sample of the same workload.
+--impl reference times the fp64 CPU oracle (the reference arm) on a bounded
+sample of the same workload.
 """
 from __future__ import annotations
 
