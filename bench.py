@@ -503,8 +503,8 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
                       split_heads=split, handle=h)
 
     # serial
-    # events around the copies of the serial variant: the link rates the
-    # e2e figure is bounded by (they differ from box to box)
+    # events around the copies of the serial variant: the host-link rates the
+    # e2e figure is bounded by (they differ from machine to machine)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
 
     def serial_one(marks=None):
