@@ -233,10 +233,31 @@ muon_status_t muon_selftest_timeout(muon_handle_t h, uint64_t timeout_ns, void* 
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call shares the one array and leaves its contents behind: calls
  * that may overlap on the GPU (different streams without ordering) race and
- * must be serialised by the caller.  Device-side errors (a timed-out wait)
- * are recorded in a word inside the array, which is cleared at each call. */
+ * must be serialised by the caller.  Device-side errors (a bounded wait that
+ * ran out, a NaN/Inf Frobenius norm) are OR-ed into an error word at the
+ * start of the array, which the first call on each device clears; they
+ * collect across calls until muon_noalloc_check() reads and clears them.
+ * Every bounded wait gives up after the limit set by
+ * muon_noalloc_set_timeout_ns (default 4 s). */
 muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int64_t m, int64_t n, int32_t steps,
                                          const float* coeffs, void* stream);
+
+/* Error readback of muon_orthogonalize_noalloc on the current device:
+ * synchronise `stream`, read the error word inside the library's static
+ * array, clear it (on `stream`) and return MUON_OK, MUON_ERR_TIMEOUT or
+ * MUON_ERR_NONFINITE (timeout wins if both are set).  The errors reported are
+ * those of every muon_orthogonalize_noalloc call on this device since the
+ * previous check.  Allocates nothing: a copy into a host variable and a
+ * memset of the word.  A call of muon_orthogonalize_noalloc still running on
+ * another stream races with the clear.  MUON_ERR_CUDA if a CUDA call fails.
+ * (No counterpart on the source pages: the handle's muon_handle_check for
+ * the allocation-free path.) */
+muon_status_t muon_noalloc_check(void* stream);
+
+/* Time limit of every bounded device wait of muon_orthogonalize_noalloc,
+ * process-wide, used by calls made after this one (default 4 s).
+ * 0: MUON_ERR_INVALID_ARG. */
+muon_status_t muon_noalloc_set_timeout_ns(uint64_t timeout_ns);
 
 /* Kernel classes reported by muon_handle_profile(). */
 enum {

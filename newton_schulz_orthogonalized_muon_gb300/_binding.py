@@ -28,7 +28,8 @@ EXPORTS = ("muon_handle_create", "muon_handle_destroy", "muon_handle_set_workspa
            "muon_handle_set_timeout_ns", "muon_handle_check", "muon_orthogonalize", "muon_step",
            "adamw_step", "muon_selftest_timeout", "muon_status_string", "muon_last_error", "muon_version",
            "muon_handle_set_profiling", "muon_handle_profile", "muon_handle_launch_count",
-           "muon_orthogonalize_noalloc", "muon_handle_profile_records", "muon_step_ex", "muon_workspace_size")
+           "muon_orthogonalize_noalloc", "muon_handle_profile_records", "muon_step_ex", "muon_workspace_size",
+           "muon_noalloc_check", "muon_noalloc_set_timeout_ns")
 KERNEL_CLASSES = ("prepare", "norm", "syrk", "poly", "update", "final", "apply", "adamw")
 
 
@@ -90,6 +91,8 @@ def load_library(path: str | None = None):
             "muon_handle_profile": (i32, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64), i32]),
             "muon_handle_launch_count": (i32, [vp, ctypes.POINTER(u64)]),
             "muon_orthogonalize_noalloc": (i32, [vp, i32, i64, i64, i32, fptr, vp]),
+            "muon_noalloc_check": (i32, [vp]),
+            "muon_noalloc_set_timeout_ns": (i32, [u64]),
             "muon_handle_profile_records": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), fptr, i32,
                                                   ctypes.POINTER(i32)]),
             "muon_step_ex": (i32, [vp, ctypes.POINTER(MuonParamC), i32, ctypes.POINTER(MuonStepOptionsC), vp]),
@@ -245,6 +248,16 @@ def muon_orthogonalize_noalloc(X: torch.Tensor, steps: int = 5, coeffs=None, str
     if st != 0:
         raise MuonError(st, "muon_orthogonalize_noalloc")
     return X
+
+
+def noalloc_check(device=None, stream=None) -> int:
+    """Synchronise the stream and return (then clear) the device error status
+    of the allocation-free calls on this device (0 = OK, 5 = non-finite
+    norm, 6 = a bounded wait ran out)."""
+    lib = load_library()
+    dev = torch.cuda.current_device() if device is None else int(device)
+    with torch.cuda.device(dev):
+        return int(lib.muon_noalloc_check(ctypes.c_void_p(_stream_ptr(stream))))
 
 
 def muon_step(params, grads, momenta, *, lr: float, wd: float, mu: float = 0.95, nesterov: bool = True,

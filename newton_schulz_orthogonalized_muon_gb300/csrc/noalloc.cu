@@ -9,6 +9,12 @@
 // every piece of scratch memory carved out of the file-scope device array
 // below, whose size is fixed at build time.  Nothing here calls cudaMalloc,
 // cudaFree or any allocating library routine.
+//
+// Device-side errors (a bounded wait that ran out, a non-finite Frobenius
+// norm) are OR-ed into an error word at the start of the array.  The word
+// starts at zero (cleared by the first call on each device), collects the
+// errors of every later call, and is read and cleared by muon_noalloc_check.
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -33,12 +39,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 struct DeviceSetup {
   bool done = false;
+  bool cleared = false;         // the error word has been zeroed on this device
   uint8_t* scratch = nullptr;   // device address of g_noalloc_scratch on this device
   int num_sms = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
 DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mu;
+// time limit of every bounded device wait of these calls (process-wide)
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
 
 // Descriptor block written into the scratch by a one-thread-block kernel,
 // so that no host-to-device copy (and no staging buffer) is needed.
@@ -49,9 +58,10 @@ struct NoAllocDesc {
   int2 tri[kMaxTri];
 };
 
-__global__ void noalloc_setup_kernel(NoAllocDesc d, unsigned* err, SrcEntry* src, OutEntry* out, int2* tri) {
+__global__ void noalloc_setup_kernel(NoAllocDesc d, unsigned* err, int clear_err, SrcEntry* src, OutEntry* out,
+                                     int2* tri) {
   if (threadIdx.x == 0) {
-    *err = 0u;      // the error word must start at zero on every call
+    if (clear_err) *err = 0u;   // first call on this device: the word starts at zero
     *src = d.src;
     *out = d.out;
   }
@@ -160,7 +170,13 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
   for (int i = 0; i < mi_sym; ++i)
     for (int j = 0; j < nj_sym; ++j)
       if ((j + 1) * bn_sym - 1 >= i * 128 && d.ntri < kMaxTri) d.tri[d.ntri++] = make_int2(i, j);
-  noalloc_setup_kernel<<<1, 64, 0, stream>>>(d, err, src_d, out_d, tri_d);
+  bool clear_err;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    clear_err = !S->cleared;
+    S->cleared = true;
+  }
+  noalloc_setup_kernel<<<1, 64, 0, stream>>>(d, err, clear_err ? 1 : 0, src_d, out_d, tri_d);
   if (cudaGetLastError() != cudaSuccess) return MUON_ERR_CUDA;
 
   PrepParams pp{};
@@ -204,7 +220,7 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
     p.ldx = ldx;
     p.out = out_d;
     p.err = err;
-    p.timeout_ns = 4000000000ull;
+    p.timeout_ns = g_timeout_ns.load();
     p.pdiag = pdiag;
     cudaError_t e;
     if (tc) {
@@ -249,5 +265,37 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
     }
     if (e != cudaSuccess) return MUON_ERR_CUDA;
   }
+  return MUON_OK;
+}
+
+extern "C" muon_status_t muon_noalloc_check(void* stream_arg) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MUON_ERR_CUDA;
+  DeviceSetup* S = nullptr;
+  muon_status_t st = setup_device(dev, &S);
+  if (st != MUON_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_arg);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MUON_ERR_CUDA;
+  bool cleared;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    cleared = S->cleared;
+  }
+  if (!cleared) return MUON_OK;     // no call has run on this device yet
+  // the word sits at the start of the array; a plain copy into a host
+  // variable and a memset on the caller's stream allocate nothing
+  unsigned word = 0;
+  if (cudaMemcpy(&word, S->scratch, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaMemsetAsync(S->scratch, 0, sizeof(unsigned), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  if (word & ERRBIT_TIMEOUT) return MUON_ERR_TIMEOUT;
+  if (word & ERRBIT_NONFINITE) return MUON_ERR_NONFINITE;
+  return MUON_OK;
+}
+
+extern "C" muon_status_t muon_noalloc_set_timeout_ns(uint64_t timeout_ns) {
+  if (timeout_ns == 0) return MUON_ERR_INVALID_ARG;
+  g_timeout_ns.store(timeout_ns);
   return MUON_OK;
 }
