@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-baseline-plan", action="store_true",
+                    help="time the fp64 oracle over all five configurations on the host cores and exit")
     return ap.parse_args(argv)
 
 
@@ -204,16 +206,109 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def cpu_baseline(min_seconds=10.0):
-    total_t, total_f, reps = 0.0, 0.0, 0
-    while total_t < min_seconds or reps == 0:
-        t, f = oracle_sample_step()
-        total_t += t
-        total_f += f
-        reps += 1
-    return {"value": total_f / total_t / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{reps} x {SAMPLE_TEXT}",
-            "seconds": round(total_t, 2)}
+def cpu_model():
+    """The host CPU's model name (x86 'model name', else lscpu's), and its
+    logical core count."""
+    name = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if name is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.startswith(("Model name", "Vendor ID")):
+                    name = (name + " / " if name else "") + line.split(":", 1)[1].strip()
+        except Exception:
+            pass
+    return {"model": name or "unknown", "logical_cores": os.cpu_count()}
+
+
+def oracle_matrix_seconds(shape, split_heads=1, method="standard", seed=0):
+    """Seconds of one fp64 oracle Muon step of one parameter of this shape
+    (seeded low-rank gradient, zero momentum) on the host cores."""
+    import numpy as np
+    import oracle
+    from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+    W = wl.weight(seed + 1, shape).astype(np.float64)
+    G = wl.lowrank_grad(seed + 2, shape[0], shape[1], 64).astype(np.float64)
+    M = np.zeros(shape)
+    t0 = time.perf_counter()
+    oracle.muon_step(W, G, M, lr=LR, wd=WD, mu=MU, nesterov=True, split_heads=split_heads, method=method)
+    return time.perf_counter() - t0
+
+
+def set_groups(specs):
+    """{(shape, split_heads): count} of a parameter list."""
+    groups = {}
+    for s_ in specs:
+        key = (tuple(s_.shape), s_.split_heads)
+        groups[key] = groups.get(key, 0) + 1
+    return groups
+
+
+def cpu_baseline(specs, method="standard"):
+    """The fp64 oracle on the host cores over a bounded sample of the set:
+    one parameter of every distinct (shape, split) of the set, each timed
+    once; the step time of the whole set is extrapolated by the number of
+    parameters of each shape (each shape's oracle time scales with its
+    count), and the value is the set's NS flops over that time."""
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+    rows, step_s, step_f, sample_s = [], 0.0, 0.0, 0.0
+    for (shape, split), count in sorted(set_groups(specs).items()):
+        t = oracle_matrix_seconds(shape, split, method)
+        m, n = flops.ns_dims(shape[0], shape[1], split)
+        f = split * flops.ns_flops(method, m, n, NS_STEPS)
+        rows.append({"shape": list(shape), "split_heads": split, "count": count, "seconds_one": round(t, 3)})
+        step_s += count * t
+        step_f += count * f
+        sample_s += t
+    return {"value": step_f / step_s / 1e12, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"one parameter of each of the set's {len(rows)} distinct shapes, timed once each "
+                      f"({sample_s:.1f} s); the full step extrapolated by shape counts to {step_s:.0f} s",
+            "extrapolated_step_s": step_s, "sample_seconds": round(sample_s, 2), "per_shape": rows,
+            "cpu": cpu_model(), "ns_method": method}
+
+
+def cpu_baseline_plan():
+    """The fp64 oracle on the host cores over the five configurations:
+    the single 256x512 fp32 matrix, the GPT-2-small set (three steps) and
+    the wide sweep's m <= 1024 shapes (both methods) in full; the sweep's
+    m = 2048 shapes on 4 of 64 matrices and the Llama-3-8B and Moonlight-MoE
+    sets on one layer, extrapolated by matrix count (labelled)."""
+    from newton_schulz_orthogonalized_muon_gb300 import flops, workloads as wl
+    out = {"cpu": cpu_model(), "blas_threads": blas_threads(), "rows": []}
+
+    def add(name, specs, reps, scale, method="standard", note="full"):
+        t = 0.0
+        for _ in range(reps):
+            for i, s_ in enumerate(specs):
+                t += oracle_matrix_seconds(s_.shape, s_.split_heads, method, seed=i)
+        f = reps * sum(s_.split_heads * flops.ns_flops(method, *flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads),
+                                                       NS_STEPS) for s_ in specs)
+        out["rows"].append({"config": name, "method": method, "timed_s": round(t, 2), "timed_tflops": f / t / 1e12,
+                            "step_s": t * scale / reps, "timing": note})
+        print(json.dumps(out["rows"][-1]), flush=True)
+
+    add("single fp32 256x512", wl.single_matrix_256x512().muon, 1, 1)
+    add("gpt2-small (3 steps)", wl.gpt2_small().muon, 3, 1, note="full, step_s per step")
+    for m, n in wl.WIDE_SWEEP:
+        for method in ("standard", "gram"):
+            spec = [wl.ParamSpec(f"w{m}x{n}", (m, n))]
+            if m <= 1024:
+                add(f"wide {m}x{n} x{wl.WIDE_BATCH}", spec * wl.WIDE_BATCH, 1, 1, method)
+            else:
+                add(f"wide {m}x{n} x{wl.WIDE_BATCH}", spec * 4, 1, wl.WIDE_BATCH / 4, method,
+                    note=f"4 of {wl.WIDE_BATCH} matrices timed, extrapolated x{wl.WIDE_BATCH // 4}")
+    for method in ("standard", "gram"):
+        add("llama3-8b", wl.llama3_8b(1).muon, 1, 32, method, note="one layer timed, extrapolated x32")
+    add("moonlight-moe", wl.moonlight_moe(1).muon, 1, 27, note="one layer timed, extrapolated x27")
+    print(json.dumps(out), flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -300,16 +395,20 @@ def run_ours(args):
     if status != 0:
         raise RuntimeError(f"device error during the timed region: status {status}")
 
-    alg, dense = flops.set_flops(specs, NS_STEPS)
+    method = args.ns_method
+    alg, dense = flops.set_flops(specs, NS_STEPS, method)
+    alg_std, _ = flops.set_flops(specs, NS_STEPS, "standard")
     if world > 1:
         t = torch.tensor([ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_max = float(t.item())
-        f = torch.tensor([alg, dense], device=dev, dtype=torch.float64)
+        f = torch.tensor([alg, dense, alg_std], device=dev, dtype=torch.float64)
         dist.all_reduce(f, op=dist.ReduceOp.SUM)
-        alg_all, dense_all = float(f[0]), float(f[1])
+        alg_all, dense_all, alg_std_all = float(f[0]), float(f[1]), float(f[2])
     else:
-        ms_max, alg_all, dense_all = ms, alg, dense
+        ms_max, alg_all, dense_all, alg_std_all = ms, alg, dense, alg_std
+    # the method's own algorithmic flops (standard: symmetric products on one
+    # triangle; gram: R0, the m x m iteration and O = Q X0)
     value = alg_all / (ms_max / 1e3) / 1e12
 
     # ---- per kernel class and per (class, same-shape group), timed live above
@@ -319,7 +418,7 @@ def run_ours(args):
         mn = flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads)
         groups[mn] = groups.get(mn, 0) + s_.split_heads
     group_list = sorted(groups.items())            # the library's group order: ascending (m, n)
-    iters = {"syrk": NS_STEPS, "poly": NS_STEPS, "update": NS_STEPS - 1, "final": 1}
+    iters = flops.kernel_launches(method, NS_STEPS)
     kernel_rows, per_group = {}, {}
     for k, tag, kms in records:
         row = kernel_rows.setdefault(k, {"ms_per_step": 0.0, "launches_per_step": 0.0})
@@ -334,12 +433,15 @@ def run_ours(args):
     group_rows = []
     for (k, tag), (kms, cnt) in sorted(per_group.items(), key=lambda x: -x[1][0]):
         (m, n), count = group_list[tag]
-        kf = flops.kernel_flops_standard(m, n)[k if k != "final" else "update"]
+        kf = flops.kernel_flops(method, m, n)[k]
         fl = count * iters[k] * args.steps * kf
         class_flops[k] += fl
-        group_rows.append({"kernel": k, "group": f"{m}x{n}", "matrices": count, "launches": cnt,
-                           "ms_per_launch": kms / cnt, "flops_per_launch": fl / cnt,
-                           "tflops": fl / (kms / 1e3) / 1e12})
+        row = {"kernel": k, "mode": kernel_mode(method, k), "group": f"{m}x{n}", "matrices": count, "launches": cnt,
+               "ms_per_launch": kms / cnt, "flops_per_launch": fl / cnt, "tflops": fl / (kms / 1e3) / 1e12}
+        if method == "gram":
+            # tensor-core work: bf16x3 m x m products, two-plane final product
+            row["mma_tflops"] = row["tflops"] * flops.kernel_mma_factor_gram()[k]
+        group_rows.append(row)
     for k, row in kernel_rows.items():
         if k in class_flops and row["ms_per_step"] > 0:
             row["tflops"] = class_flops[k] / (row["ms_per_step"] * args.steps / 1e3) / 1e12
@@ -357,12 +459,16 @@ def run_ours(args):
             except Exception:
                 traffic = None
         m_top = int(top["group"].split("x")[0])
-        kname = "ns_gemm_pair_kernel" if uses_pairs(m_top, top["kernel"]) else "ns_gemm_tc_kernel"
-        roofline = {"bound": "tensor", "kernel": f"{kname}<{top['kernel'].upper()}> on the {top['group']} group "
+        kname = "ns_gemm_pair_kernel" if uses_pairs(m_top, top["kernel"], method) else "ns_gemm_tc_kernel"
+        roofline = {"bound": "tensor", "kernel": f"{kname}<{top['mode']}> on the {top['group']} group "
                                                   f"({top['matrices']} matrices)",
                     "achieved": top["tflops"], "peak": peak, "unit": "TFLOP/s", "frac": top["tflops"] / peak,
                     "traffic": traffic, "flops_per_launch": top["flops_per_launch"],
-                    "ms_per_launch": top["ms_per_launch"], "peak_source": f"bf16_tflops_sustained, {peak_src}"}
+                    "ms_per_launch": top["ms_per_launch"], "peak_source": f"bf16_tflops_sustained, {peak_src}",
+                    "flops_model": "algorithmic" if method == "standard" else
+                                   "algorithmic (one product per bf16x3 product; mma_tflops counts every MMA)"}
+        if "mma_tflops" in top:
+            roofline["mma_tflops"] = top["mma_tflops"]
     hbm = None
     if "prepare" in kernel_rows:
         nb = sum(flops.prepare_bytes(s.shape[0] * s.shape[1]) for s in specs)
@@ -382,7 +488,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline()
+        cpu = cpu_baseline(specs, method)
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -394,6 +500,8 @@ def run_ours(args):
                           "lr": LR, "wd": WD, "mu": MU, "nesterov": True,
                           "parallelism": f"layer-wise ownership x{world}" if world > 1 else "single GPU"},
                "step_ms": ms_max, "ns_tflops_dense_convention": dense_all / (ms_max / 1e3) / 1e12,
+               "ns_flops_model": "standard algorithmic" if method == "standard" else "gram algorithmic",
+               "ns_tflops_standard_equivalent": alg_std_all / (ms_max / 1e3) / 1e12,
                "ns_frac_of_peak": value / peak, "roofline": roofline, "roofline_hbm": hbm,
                "kernels": kernel_rows, "kernel_groups": group_rows, "gpu_launches": launches, "clocks": clk, "e2e": e2e, "adamw": adamw,
                "cpu_baseline": cpu}
@@ -603,16 +711,28 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs}
 
 
-def uses_pairs(m, kernel_class):
-    """The library's rule for which products run on the CTA-pair kernels
-    (standard method): symmetric products when m is a multiple of 256 or
+def kernel_mode(method, kernel_class):
+    """The kernel mode behind a reported kernel class (bf16 parameters, whose
+    last product writes through tensor maps)."""
+    if method == "gram":
+        return {"syrk": "G_R0", "poly": "G_P", "update": "G_PROD", "final": "G_FINAL_T"}[kernel_class]
+    return {"syrk": "SYRK", "poly": "POLY", "update": "UPDATE", "final": "FINAL_T"}[kernel_class]
+
+
+def uses_pairs(m, kernel_class, method="standard"):
+    """The library's rule for which products run on the CTA-pair kernels.
+    Standard method: symmetric products when m is a multiple of 256 or
     m >= MUON_TC_PAIR_MIN_M (1024 by default); UPDATE / FINAL when m is a
-    multiple of 256 or m >= 2048; none with MUON_TC_PAIR=0, symmetric
-    products only with MUON_TC_PAIR=sym."""
+    multiple of 256 or m >= 2048.  Gram method: its symmetric products
+    (R0, P, the m x m products) by the same rule; O = Q X0 always on one
+    SM.  None with MUON_TC_PAIR=0, symmetric products only with
+    MUON_TC_PAIR=sym."""
     env = os.environ.get("MUON_TC_PAIR")
     if env == "0" or m < 256:
         return False
-    if kernel_class in ("update", "final"):
+    if method == "gram" and kernel_class == "final":
+        return False
+    if method == "standard" and kernel_class in ("update", "final"):
         return env != "sym" and (m % 256 == 0 or m >= 2048)
     try:
         min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "1024"))
@@ -680,6 +800,8 @@ def run_wide(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.cpu_baseline_plan:
+        return cpu_baseline_plan()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "wide":

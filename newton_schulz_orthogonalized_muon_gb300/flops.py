@@ -35,15 +35,50 @@ def ns_flops_gram(m: int, n: int, steps: int = 5) -> float:
 
 def kernel_flops_standard(m: int, n: int):
     """Algorithmic flops of one matrix in each GEMM kernel class."""
-    return {"syrk": float(m * (m + 1) * n), "poly": float(m * m * (m + 1)), "update": 2.0 * m * m * n}
+    return {"syrk": float(m * (m + 1) * n), "poly": float(m * m * (m + 1)), "update": 2.0 * m * m * n,
+            "final": 2.0 * m * m * n}
 
 
-def set_flops(specs, steps: int = 5):
-    """(algorithmic, dense) NS flops of one step over a list of ParamSpec."""
+def kernel_flops_gram(m: int, n: int):
+    """Gram method, algorithmic flops of one matrix in each kernel class the
+    library reports: "syrk" R0 = X0 X0^T (one triangle), "poly"
+    P = aI + bR + cR^2 (R^2 on one triangle), "update" one symmetric m x m
+    product (P Q, P R or (P R) P, one triangle), "final" O = Q X0."""
+    sym = float(m * m * (m + 1))
+    return {"syrk": float(m * (m + 1) * n), "poly": sym, "update": sym, "final": 2.0 * m * m * n}
+
+
+def kernel_mma_factor_gram():
+    """Tensor-core work per algorithmic flop of each Gram-method class: the
+    m x m products run as bf16x3 (hi*hi + hi*lo + lo*hi, three MMAs) and the
+    final product applies both planes of Q (two MMAs)."""
+    return {"syrk": 1.0, "poly": 3.0, "update": 3.0, "final": 2.0}
+
+
+def kernel_launches(method: str, steps: int = 5):
+    """Launches per same-shape chunk of each kernel class, by method."""
+    if method == "gram":
+        return {"syrk": 1, "poly": steps, "update": 3 * max(steps - 1, 0), "final": 1}
+    return {"syrk": steps, "poly": steps, "update": max(steps - 1, 0), "final": 1}
+
+
+def kernel_flops(method: str, m: int, n: int):
+    return kernel_flops_gram(m, n) if method == "gram" else kernel_flops_standard(m, n)
+
+
+def ns_flops(method: str, m: int, n: int, steps: int = 5) -> float:
+    return ns_flops_gram(m, n, steps) if method == "gram" else ns_flops_standard(m, n, steps)
+
+
+def set_flops(specs, steps: int = 5, method: str = "standard"):
+    """(algorithmic, dense) NS flops of one step over a list of ParamSpec.
+    Algorithmic flops are the method's own (ns_flops_standard or
+    ns_flops_gram); the dense convention is the standard method's
+    4 m^2 n + 2 m^3 per iteration whatever the method."""
     alg = dense = 0.0
     for s in specs:
         m, n = ns_dims(s.shape[0], s.shape[1], s.split_heads)
-        alg += s.split_heads * ns_flops_standard(m, n, steps)
+        alg += s.split_heads * ns_flops(method, m, n, steps)
         dense += s.split_heads * ns_flops_dense(m, n, steps)
     return alg, dense
 

@@ -53,3 +53,34 @@ def test_pair_rule_matches_the_library(m, kernel, pair, monkeypatch):
     monkeypatch.delenv("MUON_TC_PAIR", raising=False)
     monkeypatch.delenv("MUON_TC_PAIR_MIN_M", raising=False)
     assert bench.uses_pairs(m, kernel) is pair
+
+
+@pytest.mark.parametrize("m,kernel,pair", [
+    (4096, "syrk", True), (4096, "poly", True), (4096, "update", True), (4096, "final", False),
+    (1408, "update", True), (640, "update", False)])
+def test_gram_pair_rule_matches_the_library(m, kernel, pair, monkeypatch):
+    # the Gram method runs R0, P and its m x m products on pairs by the
+    # symmetric-product rule, and O = Q X0 on one SM
+    monkeypatch.delenv("MUON_TC_PAIR", raising=False)
+    monkeypatch.delenv("MUON_TC_PAIR_MIN_M", raising=False)
+    assert bench.uses_pairs(m, kernel, "gram") is pair
+
+
+@pytest.mark.parametrize("method", ["standard", "gram"])
+@pytest.mark.parametrize("m,n,steps", [(4096, 14336, 5), (1024, 4096, 5), (256, 512, 3), (128, 2048, 1)])
+def test_per_class_flops_add_up_to_the_method_total(method, m, n, steps):
+    # the bench's per-kernel rows (launches x flops per launch) sum to the
+    # method's own total, so the headline and the rows use one flop model
+    launches = flops.kernel_launches(method, steps)
+    per = flops.kernel_flops(method, m, n)
+    total = sum(launches[k] * per[k] for k in launches)
+    assert total == pytest.approx(flops.ns_flops(method, m, n, steps), rel=1e-12)
+    assert bench.kernel_mode(method, "final") in ("FINAL_T", "G_FINAL_T")
+
+
+def test_gram_flops_are_below_standard_only_for_wide_matrices():
+    # R0 and O = Q X0 carry the n-dependent work (3 m^2 n), the iteration
+    # (5 + 3 * 4) m^2 (m + 1): fewer flops than the standard method once
+    # n / m is large enough
+    assert flops.ns_flops("gram", 256, 16384) < 0.3 * flops.ns_flops("standard", 256, 16384)
+    assert flops.ns_flops("gram", 4096, 4096) > flops.ns_flops("standard", 4096, 4096)
