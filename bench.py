@@ -377,7 +377,7 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     clocks.start()
-    h.set_profiling(True)
+    # timed region 1 (the headline): the steps alone
     launches0 = h.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -388,6 +388,18 @@ def run_ours(args):
     barrier()
     ms = e0.elapsed_time(e1) / max(args.steps, 1)
     launches = h.launch_count() - launches0
+    # timed region 2: the same number of steps with a CUDA event pair around
+    # every launch on the launching stream (per-kernel times for the rows and
+    # the roofline; the events cost time between small launches)
+    h.set_profiling(True)
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e2.record(stream)
+    for _ in range(args.steps):
+        step()
+    e3.record(stream)
+    barrier()
+    ms_profiled = e2.elapsed_time(e3) / max(args.steps, 1)
     records = h.profile_records()
     h.set_profiling(False)
     clk = clocks.stop()
@@ -453,7 +465,7 @@ def run_ours(args):
         tpath = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tpath):
             try:
-                entry = json.load(open(tpath)).get(ws.name, {}).get(f"{top['kernel']}@{top['group']}")
+                entry = json.load(open(tpath)).get(ws.name, {}).get(f"{top['mode']}@{top['group']}")
                 if entry and entry.get("kernel_source_hash") == kernel_source_hash():
                     traffic = entry.get("bytes_per_launch")
             except Exception:
@@ -499,7 +511,8 @@ def run_ours(args):
                           "matrices_per_gpu": len(specs), "l2": "inputs larger than L2 (no flush needed)",
                           "lr": LR, "wd": WD, "mu": MU, "nesterov": True,
                           "parallelism": f"layer-wise ownership x{world}" if world > 1 else "single GPU"},
-               "step_ms": ms_max, "ns_tflops_dense_convention": dense_all / (ms_max / 1e3) / 1e12,
+               "step_ms": ms_max, "ms_per_step_with_launch_events": ms_profiled,
+               "ns_tflops_dense_convention": dense_all / (ms_max / 1e3) / 1e12,
                "ns_flops_model": "standard algorithmic" if method == "standard" else "gram algorithmic",
                "ns_tflops_standard_equivalent": alg_std_all / (ms_max / 1e3) / 1e12,
                "ns_frac_of_peak": value / peak, "roofline": roofline, "roofline_hbm": hbm,
@@ -723,7 +736,8 @@ def uses_pairs(m, kernel_class, method="standard"):
     """The library's rule for which products run on the CTA-pair kernels.
     Standard method: symmetric products when m is a multiple of 256 or
     m >= MUON_TC_PAIR_MIN_M (1024 by default); UPDATE / FINAL when m is a
-    multiple of 256 or m >= 2048.  Gram method: its symmetric products
+    multiple of 256, and for a ragged m on the rows below its last multiple
+    of 256 (a one-SM launch takes the rest).  Gram method: its symmetric products
     (R0, P, the m x m products) by the same rule; O = Q X0 always on one
     SM.  None with MUON_TC_PAIR=0, symmetric products only with
     MUON_TC_PAIR=sym."""
@@ -733,7 +747,15 @@ def uses_pairs(m, kernel_class, method="standard"):
     if method == "gram" and kernel_class == "final":
         return False
     if method == "standard" and kernel_class in ("update", "final"):
-        return env != "sym" and (m % 256 == 0 or m >= 2048)
+        # a ragged m runs its rows below the last multiple of 256 on pairs and
+        # the rest on one SM (MUON_TC_SPLIT=0: pairs only from m = 2048)
+        if env == "sym":
+            return False
+        if m % 256 == 0:
+            return True
+        if os.environ.get("MUON_TC_SPLIT", "1") != "0":
+            return True
+        return m >= 2048
     try:
         min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "1024"))
     except ValueError:

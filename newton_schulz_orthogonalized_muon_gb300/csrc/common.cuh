@@ -124,6 +124,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// The library's kernels are launched with programmatic stream serialization
+// (launch_k in internal.h): a kernel may be scheduled before the previous
+// kernel of the stream has finished, so that its launch and prologue overlap
+// that kernel's tail.  Every such kernel calls pdl_wait() before its first
+// access to global memory that an earlier kernel of the stream reads or
+// writes (the wait returns once the previous kernel has completed and its
+// memory is visible; without the attribute it returns at once), and then
+// pdl_launch_dependents(), which lets the next kernel be scheduled once every
+// CTA of this grid has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -10,6 +10,28 @@
 
 namespace muon {
 
+// Programmatic dependent launch of the library's kernels: on unless the
+// environment sets MUON_PDL=0 (read once).
+bool pdl_enabled();
+
+// Launch `kern` on `s` with programmatic stream serialization when enabled
+// (the kernel must call pdl_wait() before touching memory an earlier kernel
+// of the stream uses; common.cuh).
+template <typename... Params, typename... Args>
+cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 struct SrcEntry;
 struct OutEntry;
 
@@ -95,7 +117,8 @@ struct NsGemmParams {
   int batch;
   int tiles_per_mat;            // tiles of one matrix
   int num_tiles;                // batch * tiles_per_mat
-  int mi;                       // row blocks of the output (UPDATE/FINAL)
+  int mi;                       // row blocks of the output (UPDATE/FINAL) this launch covers
+  int mi0;                      // first of them (UPDATE/FINAL; 0 unless a launch covers a row tail)
   const int2* tri;              // (i, j) tile table of the symmetric modes
   const float* scale;           // per-matrix 1/||U||_F applied this iteration, or nullptr
   float ca, cb, cc;             // quintic coefficients

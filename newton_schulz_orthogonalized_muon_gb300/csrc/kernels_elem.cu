@@ -14,6 +14,8 @@
 //  * adamw_kernel: the AdamW fallback of the same printed Muon class.
 //  * wait_selftest_kernel: a bounded wait on a barrier nothing completes,
 //    so the timeout path can be exercised without hanging a GPU.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,6 +38,9 @@ constexpr int PREP_THREADS = 256;
 __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
   __shared__ float tile[PT][PT + 1];
   __shared__ float red[PREP_THREADS / 32];
+  // the workspace it writes is read by the previous group's kernels
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int b = blockIdx.y;
   const SrcEntry e = p.src[b];
@@ -186,6 +191,8 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
 // One warp per matrix: scale[b] = 1 / (sqrt(sum of partials) + eps).
 __global__ void norm_finalize_kernel(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
                                      unsigned* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= batch) return;
@@ -202,6 +209,8 @@ __global__ void norm_finalize_kernel(const float* partials, int tiles_per_mat, i
 
 // Final update with no Newton-Schulz step: O = X0 = scale * U (fp32 master).
 __global__ void apply_kernel(ApplyParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int b = blockIdx.y;
   const OutEntry e = p.out[b];
   const float s = p.scale[b];
@@ -260,6 +269,8 @@ __device__ __forceinline__ void store8(void* base, long long i, int dtype, const
 }
 
 __global__ void __launch_bounds__(256) adamw_kernel(AdamParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const AdamChunk ch = p.chunks[blockIdx.x];
   const AdamTensor t = p.tensors[ch.tensor];
   const long long beg = ch.offset;
@@ -304,25 +315,34 @@ __global__ void wait_selftest_kernel(unsigned long long timeout_ns, unsigned* er
 // Descriptor arena upload: 16-byte words from the pinned staging buffer
 // (read through its device address) into the device descriptor buffer.
 __global__ void desc_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, size_t n16) {
+  pdl_wait();               // earlier kernels may still read the descriptor buffer
+  pdl_launch_dependents();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
     dst[i] = src[i];
 }
 
 // ------------------------------------------------------------- launchers
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("MUON_PDL");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
+
 cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
   const size_t n16 = bytes / 16;
   if (n16 == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<size_t>((n16 + threads - 1) / threads, 1024));
-  desc_copy_kernel<<<blocks, threads, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
-  return cudaGetLastError();
+  return launch_k(desc_copy_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(dst),
+                  static_cast<const uint4*>(src), n16);
 }
 cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s) {
   if (batch == 0 || tiles_per_mat == 0) return cudaSuccess;
   dim3 grid(tiles_per_mat, batch);
-  muon_prepare_kernel<<<grid, PREP_THREADS, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(muon_prepare_kernel, grid, dim3(PREP_THREADS), 0, s, p);
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
@@ -330,8 +350,8 @@ cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int b
   if (batch == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (batch * 32 + threads - 1) / threads;
-  norm_finalize_kernel<<<blocks, threads, 0, s>>>(partials, tiles_per_mat, batch, eps, scale, err);
-  return cudaGetLastError();
+  return launch_k(norm_finalize_kernel, dim3(blocks), dim3(threads), 0, s, partials, tiles_per_mat, batch, eps, scale,
+                  err);
 }
 
 cudaError_t launch_apply(const ApplyParams& p, int batch, cudaStream_t s) {
@@ -340,14 +360,12 @@ cudaError_t launch_apply(const ApplyParams& p, int batch, cudaStream_t s) {
   int bx = static_cast<int>((total + 255) / 256);
   if (bx > 1024) bx = 1024;
   if (bx < 1) bx = 1;
-  apply_kernel<<<dim3(bx, batch), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(apply_kernel, dim3(bx, batch), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_adamw(const AdamParams& p, int n_chunks, cudaStream_t s) {
   if (n_chunks == 0) return cudaSuccess;
-  adamw_kernel<<<n_chunks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(adamw_kernel, dim3(n_chunks), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t s) {

@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // operands, outputs and descriptors are written or read by earlier kernels
+  pdl_wait();
+  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = ((ModeTraits<MODE>::kKn ? p.n : p.m) + BK - 1) / BK;
 
@@ -294,8 +297,8 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, TC_THREADS, C::SMEM, s>>>(a0, a1, b0, b1, xh, xl, xo, p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(kern, dim3(grid), dim3(TC_THREADS), C::SMEM, s, a0, a1, b0, b1, xh, xl, xo, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

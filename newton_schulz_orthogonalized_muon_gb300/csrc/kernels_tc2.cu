@@ -123,6 +123,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   tc_fence_before();
   cluster_sync_all();      // the peer's barriers are initialised and TMEM is allocated in both CTAs
   tc_fence_after();
+  // operands, outputs and descriptors are written or read by earlier kernels
+  pdl_wait();
+  pdl_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = ((ModeTraits<MODE>::kKn ? p.n : p.m) + BK - 1) / BK;
 
@@ -293,8 +296,8 @@ cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<2 * pairs, TC_THREADS, C::SMEM, s>>>(a0, a1, b0, b1, xh, xl, xo, p);
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(kern, dim3(2 * pairs), dim3(TC_THREADS), C::SMEM, s, a0, a1, b0, b1, xh, xl, xo, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -82,6 +82,7 @@ struct muon_handle_s {
   int pair_min_m = 1024;        // ragged m from here on runs its symmetric products on pairs too (MUON_TC_PAIR_MIN_M)
   int max_pairs = 0;
   bool final_tma = true;        // FINAL into bf16 destinations through tensor maps (MUON_FINAL_TMA=0 disables)
+  bool split_ragged = true;     // ragged-m UPDATE / FINAL split between pairs and one SM (MUON_TC_SPLIT=0 disables)
 };
 
 namespace {
@@ -269,6 +270,8 @@ struct GroupPlan {
   int tri256_count = 0;
   bool pair = false;            // symmetric products on CTA pairs
   bool pair_upd = false;        // UPDATE / FINAL on CTA pairs
+  bool split_upd = false;       // UPDATE / FINAL: rows below the last multiple of 256 on CTA
+                                // pairs, the remaining 128-row blocks on one SM
   std::vector<std::pair<size_t, size_t>> chunk_off;   // (src offset, out offset) per chunk
   std::vector<size_t> chunk_wmap;   // per chunk: offset of the destinations' tensor maps, or kNoMaps
 };
@@ -580,10 +583,13 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         g.tri256_count = static_cast<int>(t256.size());
         g.tri256_off = arena_push(arena, t256.data(), t256.size());
         g.pair = true;
-        // UPDATE / FINAL on pairs only without a ragged last row tile, or
-        // from m = 2048 (a ragged tile costs them more than the symmetric
-        // products)
-        g.pair_upd = h->pair_update && (g.m % 256 == 0 || g.m >= 2048);
+        // UPDATE / FINAL on pairs without a ragged last row tile; with one,
+        // the pairs take the rows below the last multiple of 256 and a
+        // one-SM launch the rest (a half-empty 256-row pair tile costs more
+        // than the extra launch), or, with the split switched off, pairs
+        // from m = 2048
+        g.pair_upd = h->pair_update && (g.m % 256 == 0 || (!h->split_ragged && g.m >= 2048));
+        g.split_upd = h->pair_update && h->split_ragged && g.m % 256 != 0;
       }
     }
     for (size_t c0 = 0; c0 < g.members.size(); c0 += g.chunk) {
@@ -721,9 +727,15 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                       launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream, n128 ? &map_A64 : nullptr),
                       "poly launch");
           NsGemmParams u = p;
-          if (g.pair_upd) {
-            const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
+          if (g.pair_upd || g.split_upd) {
+            // pairs: whole 256-row blocks (all of them, or those below the
+            // ragged tail); the tail's 128-row blocks on one SM after them.
+            // The two launches write disjoint rows of the new hi / lo planes
+            // and of the destinations, and both read this iteration's X^.
+            const int mi2 = static_cast<int>(g.pair_upd ? ceil_div(g.m, 256) : g.m / 256);
+            const int nj2 = static_cast<int>(ceil_div(g.n, 256));
             u.mi = mi2;
+            u.mi0 = 0;
             u.tiles_per_mat = mi2 * nj2;
             u.num_tiles = cnt * mi2 * nj2;
             const int upairs = std::min(u.num_tiles, h->max_pairs);
@@ -732,6 +744,18 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                                                    map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream,
                                                    g.m <= kShortK ? 2 : 0),
                         "update launch");
+            if (g.split_upd) {
+              NsGemmParams w = p;
+              w.mi0 = (g.m / 256) * 2;                       // first 128-row block of the tail
+              w.mi = mi - w.mi0;
+              w.tiles_per_mat = w.mi * nj;
+              w.num_tiles = cnt * w.tiles_per_mat;
+              const int grid = std::min(w.num_tiles, h->num_sms);
+              MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                          launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
+                                                   map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], w, grid, stream),
+                          "update tail launch");
+            }
           } else {
             u.mi = mi;
             u.tiles_per_mat = mi * nj;
@@ -895,6 +919,7 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
   }
   h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
   if (const char* ft = std::getenv("MUON_FINAL_TMA")) h->final_tma = ft[0] != '0';
+  if (const char* sp = std::getenv("MUON_TC_SPLIT")) h->split_ragged = sp[0] != '0';
   bool ok = cudaMalloc(&h->err, sizeof(unsigned)) == cudaSuccess && cudaMemset(h->err, 0, sizeof(unsigned)) == cudaSuccess;
   for (int k = 0; ok && k < muon_handle_s::kStages; ++k)
     ok = cudaEventCreateWithFlags(&h->stage_ev[k], cudaEventDisableTiming) == cudaSuccess;

@@ -60,7 +60,7 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
     j = ij.y;
   } else {
     j = l / p.mi;          // column-block major: neighbouring tiles share X's column block
-    i = l - j * p.mi;
+    i = l - j * p.mi + p.mi0;
   }
 }
 
