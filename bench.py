@@ -45,8 +45,12 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["llama3-8b", "gpt2-small", "moonlight-moe", "wide"], default="llama3-8b",
-                    help="wide: the standard-vs-gram sweep over 64 Gaussian m x n matrices per shape")
+    ap.add_argument("--workload", choices=["llama3-8b", "gpt2-small", "moonlight-moe", "single-fp32", "wide"],
+                    default="llama3-8b",
+                    help="wide: the standard-vs-gram sweep over 64 Gaussian m x n matrices per shape; single-fp32: "
+                         "one fp32 256x512 matrix")
+    ap.add_argument("--param-dtype", choices=["bf16", "fp32"], default=None,
+                    help="parameter and gradient dtype (default bf16; fp32 for single-fp32): fp32 runs the fp32 path")
     ap.add_argument("--ns-method", choices=["standard", "gram"], default="standard")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (parity runs only)")
     ap.add_argument("--workspace-gb", type=float, default=64.0)
@@ -61,6 +65,8 @@ def parse_args(argv=None):
 
 def weight_set(name, layers=None):
     from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+    if name == "single-fp32":
+        return wl.single_matrix_256x512()
     if name == "llama3-8b":
         return wl.llama3_8b(layers or 32)
     if name == "gpt2-small":
@@ -131,12 +137,13 @@ class ClockSampler:
 
 # ------------------------------------------------------------ workload
 
-def make_inputs(specs, device, seed, batch=32):
-    """Seeded synthetic tensors on the device: W ~ N(0, 0.02) bf16, G low-rank
+def make_inputs(specs, device, seed, batch=32, dtype=None, rank=64):
+    """Seeded synthetic tensors on the device: W ~ N(0, 0.02), G low-rank
     (rank 64, orthonormal factors from QR of Gaussians, sigma_i = 0.5**(i/8))
-    + 1e-3 N(0,1) noise, bf16, M = 0 fp32.  Same-shape matrices are drawn in
-    batches from one seeded torch.Generator per shape."""
+    + 1e-3 N(0,1) noise, both bf16 (or `dtype`), M = 0 fp32.  Same-shape
+    matrices are drawn in batches from one seeded torch.Generator per shape."""
     import torch
+    dtype = dtype or torch.bfloat16
     from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
     W, G, M = [None] * len(specs), [None] * len(specs), [None] * len(specs)
     by_shape = {}
@@ -146,7 +153,7 @@ def make_inputs(specs, device, seed, batch=32):
     for k, (shape, idx) in enumerate(sorted(by_shape.items())):
         gen.manual_seed(wl.matrix_seed(seed, k))
         rows, cols = shape
-        r = min(64, rows, cols)
+        r = min(rank, rows, cols)
         sigma = 0.5 ** (torch.arange(r, device=device, dtype=torch.float32) / 8.0)
         for c0 in range(0, len(idx), batch):
             part = idx[c0:c0 + batch]
@@ -157,8 +164,8 @@ def make_inputs(specs, device, seed, batch=32):
             g.add_(torch.randn(nb, rows, cols, generator=gen, device=device), alpha=1e-3)
             w = torch.randn(nb, rows, cols, generator=gen, device=device).mul_(0.02)
             for j, i in enumerate(part):
-                G[i] = g[j].to(torch.bfloat16)
-                W[i] = w[j].to(torch.bfloat16)
+                G[i] = g[j].to(dtype)
+                W[i] = w[j].to(dtype)
                 M[i] = torch.zeros(shape, dtype=torch.float32, device=device)
             del U, V, g, w
     return W, G, M
@@ -359,7 +366,9 @@ def run_ours(args):
 
     ws = weight_set(args.workload, args.layers)
     specs, _ = owned_specs(ws, world, rank)
-    W, G, M = make_inputs(specs, dev, args.seed + 7919 * rank)
+    fp32 = param_dtype(args) == "fp32"
+    W, G, M = make_inputs(specs, dev, args.seed + 7919 * rank, dtype=torch.float32 if fp32 else torch.bfloat16,
+                          rank=ws.grad_rank)
     split = [s.split_heads for s in specs]
     h = pkg.default_handle(local)
     h.set_workspace_limit(int(args.workspace_gb * (1 << 30)))
@@ -448,11 +457,14 @@ def run_ours(args):
         kf = flops.kernel_flops(method, m, n)[k]
         fl = count * iters[k] * args.steps * kf
         class_flops[k] += fl
-        row = {"kernel": k, "mode": kernel_mode(method, k), "group": f"{m}x{n}", "matrices": count, "launches": cnt,
+        row = {"kernel": k, "mode": kernel_mode(method, k, fp32), "group": f"{m}x{n}", "matrices": count, "launches": cnt,
                "ms_per_launch": kms / cnt, "flops_per_launch": fl / cnt, "tflops": fl / (kms / 1e3) / 1e12}
-        if method == "gram":
+        if method == "gram" and not fp32:
             # tensor-core work: bf16x3 m x m products, two-plane final product
             row["mma_tflops"] = row["tflops"] * flops.kernel_mma_factor_gram()[k]
+        elif fp32 and method == "standard":
+            # three-plane operands: six bf16 MMAs per product
+            row["mma_tflops"] = row["tflops"] * 6.0
         group_rows.append(row)
     for k, row in kernel_rows.items():
         if k in class_flops and row["ms_per_step"] > 0:
@@ -471,14 +483,15 @@ def run_ours(args):
             except Exception:
                 traffic = None
         m_top = int(top["group"].split("x")[0])
-        kname = "ns_gemm_pair_kernel" if uses_pairs(m_top, top["kernel"], method) else "ns_gemm_tc_kernel"
+        kname = "ns_gemm_pair_kernel" if (not fp32 and uses_pairs(m_top, top["kernel"], method)) else (
+            "ns_gemm_tc_kernel" if not fp32 or method == "standard" else "ns_gemm_simt_kernel")
         roofline = {"bound": "tensor", "kernel": f"{kname}<{top['mode']}> on the {top['group']} group "
                                                   f"({top['matrices']} matrices)",
                     "achieved": top["tflops"], "peak": peak, "unit": "TFLOP/s", "frac": top["tflops"] / peak,
                     "traffic": traffic, "flops_per_launch": top["flops_per_launch"],
                     "ms_per_launch": top["ms_per_launch"], "peak_source": f"bf16_tflops_sustained, {peak_src}",
-                    "flops_model": "algorithmic" if method == "standard" else
-                                   "algorithmic (one product per bf16x3 product; mma_tflops counts every MMA)"}
+                    "flops_model": "algorithmic" if method == "standard" and not fp32 else
+                                   "algorithmic (one product per plane-split product; mma_tflops counts every MMA)"}
         if "mma_tflops" in top:
             roofline["mma_tflops"] = top["mma_tflops"]
     hbm = None
@@ -505,11 +518,15 @@ def run_ours(args):
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "vs_baseline": None, "dtype": "f32" if fp32 else "bf16", "data": "synthetic",
                "config": {"workload": ws.name, "ns_method": args.ns_method, "ns_steps": NS_STEPS,
                           "muon_params_per_gpu": sum(s.shape[0] * s.shape[1] for s in specs),
                           "matrices_per_gpu": len(specs), "l2": "inputs larger than L2 (no flush needed)",
                           "lr": LR, "wd": WD, "mu": MU, "nesterov": True,
+                          "param_dtype": param_dtype(args),
+                          "ns_path": ("fp32 on the tensor cores: three-plane bf16 operands, six MMAs per product"
+                                      if fp32 and method == "standard" else
+                                      "fp32 on the CUDA cores" if fp32 else "bf16 tensor cores"),
                           "parallelism": f"layer-wise ownership x{world}" if world > 1 else "single GPU"},
                "step_ms": ms_max, "ms_per_step_with_launch_events": ms_profiled,
                "ns_tflops_dense_convention": dense_all / (ms_max / 1e3) / 1e12,
@@ -724,9 +741,17 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs}
 
 
-def kernel_mode(method, kernel_class):
+def param_dtype(args):
+    return args.param_dtype or ("fp32" if args.workload == "single-fp32" else "bf16")
+
+
+def kernel_mode(method, kernel_class, fp32=False):
     """The kernel mode behind a reported kernel class (bf16 parameters, whose
     last product writes through tensor maps)."""
+    if fp32:
+        if method == "gram":
+            return {"syrk": "G_R0", "poly": "G_P", "update": "G_PROD", "final": "G_FINAL"}[kernel_class]
+        return {"syrk": "F_SYRK", "poly": "F_POLY", "update": "F_UPDATE", "final": "F_FINAL"}[kernel_class]
     if method == "gram":
         return {"syrk": "G_R0", "poly": "G_P", "update": "G_PROD", "final": "G_FINAL_T"}[kernel_class]
     return {"syrk": "SYRK", "poly": "POLY", "update": "UPDATE", "final": "FINAL_T"}[kernel_class]
@@ -736,8 +761,7 @@ def uses_pairs(m, kernel_class, method="standard"):
     """The library's rule for which products run on the CTA-pair kernels.
     Standard method: symmetric products when m is a multiple of 256 or
     m >= MUON_TC_PAIR_MIN_M (1024 by default); UPDATE / FINAL when m is a
-    multiple of 256, and for a ragged m on the rows below its last multiple
-    of 256 (a one-SM launch takes the rest).  Gram method: its symmetric products
+    multiple of 256 or m >= 2048.  Gram method: its symmetric products
     (R0, P, the m x m products) by the same rule; O = Q X0 always on one
     SM.  None with MUON_TC_PAIR=0, symmetric products only with
     MUON_TC_PAIR=sym."""
@@ -747,15 +771,7 @@ def uses_pairs(m, kernel_class, method="standard"):
     if method == "gram" and kernel_class == "final":
         return False
     if method == "standard" and kernel_class in ("update", "final"):
-        # a ragged m runs its rows below the last multiple of 256 on pairs and
-        # the rest on one SM (MUON_TC_SPLIT=0: pairs only from m = 2048)
-        if env == "sym":
-            return False
-        if m % 256 == 0:
-            return True
-        if os.environ.get("MUON_TC_SPLIT", "1") != "0":
-            return True
-        return m >= 2048
+        return env != "sym" and (m % 256 == 0 or m >= 2048)
     try:
         min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "1024"))
     except ValueError:

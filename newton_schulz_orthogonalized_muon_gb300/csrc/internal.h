@@ -10,15 +10,18 @@
 
 namespace muon {
 
-// Programmatic dependent launch of the library's kernels: on unless the
-// environment sets MUON_PDL=0 (read once).
-bool pdl_enabled();
+// Programmatic dependent launch of the library's kernels, from the
+// environment variable MUON_PDL (read once): 0 off; 1 (default) for the NS
+// GEMM kernels, which cannot share an SM with the previous GEMM and so never
+// wait beside a running kernel; 2 for every kernel.
+int pdl_level();
 
-// Launch `kern` on `s` with programmatic stream serialization when enabled
+// Launch `kern` on `s`, with programmatic stream serialization when `pdl`
 // (the kernel must call pdl_wait() before touching memory an earlier kernel
 // of the stream uses; common.cuh).
 template <typename... Params, typename... Args>
-cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+cudaError_t launch_k(bool pdl, void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -28,7 +31,7 @@ cudaError_t launch_k(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
@@ -45,6 +48,7 @@ struct PrepParams {
   float* xf;               // fp32 copy [batch][m][ldx] or nullptr
   __nv_bfloat16* xb;       // bf16 operand copy = hi plane of the master, or nullptr (fp32 path)
   __nv_bfloat16* xlo;      // lo plane of the master, bf16(U - bf16(U)), or nullptr
+  __nv_bfloat16* xlo2;     // third plane bf16(U - hi - lo) (fp32 tensor-core path), or nullptr
   float* partials;         // [batch][tiles_per_mat]
   int tiles_per_mat;
 };
@@ -99,6 +103,18 @@ struct AdamParams {
 //   G_P     P = a I + b R + c R R       (planes in/out)
 //   G_PROD  C = A B                      (planes in/out; A, B commute)
 //   G_FINAL out = alpha*out + beta*s*(Q X)  (Q planes, X bf16 MN-major)
+//
+// fp32 tensor-core path (fp32 parameters at the fp32 bar): every operand is
+// held as three bf16 planes v = p0 + p1 + p2 (p0 = bf16(v), p1 = bf16(v - p0),
+// p2 = bf16(v - p0 - p1): 24 mantissa bits), and a product of two such
+// operands issues six MMAs per K step (p0q0 + p0q1 + p1q0 + p0q2 + p1q1 +
+// p2q0) into one fp32 accumulator; the terms left out are below 2^-24 of the
+// product.  The iteration is then the plain one, X' = P X:
+//   F_SYRK   A = s^2 X X^T              (planes in, symmetric planes out)
+//   F_POLY   P = a I + b A + c A A      (planes in and out)
+//   F_UPDATE X' = s P X                  (planes in, planes out, no inputs read
+//                                         in the epilogue)
+//   F_FINAL  out = alpha*out + beta*s*(P X)   (element-wise destinations)
 enum NsMode : int {
   MODE_SYRK = 0,
   MODE_POLY = 1,
@@ -109,7 +125,11 @@ enum NsMode : int {
   MODE_G_PROD = 6,
   MODE_G_FINAL = 7,
   MODE_FINAL_T = 8,         // FINAL into bf16 destinations through per-matrix tensor maps
-  MODE_G_FINAL_T = 9        // G_FINAL likewise
+  MODE_G_FINAL_T = 9,       // G_FINAL likewise
+  MODE_F_SYRK = 10,
+  MODE_F_POLY = 11,
+  MODE_F_UPDATE = 12,
+  MODE_F_FINAL = 13
 };
 
 struct NsGemmParams {
@@ -117,8 +137,7 @@ struct NsGemmParams {
   int batch;
   int tiles_per_mat;            // tiles of one matrix
   int num_tiles;                // batch * tiles_per_mat
-  int mi;                       // row blocks of the output (UPDATE/FINAL) this launch covers
-  int mi0;                      // first of them (UPDATE/FINAL; 0 unless a launch covers a row tail)
+  int mi;                       // row blocks of the output (UPDATE/FINAL)
   const int2* tri;              // (i, j) tile table of the symmetric modes
   const float* scale;           // per-matrix 1/||U||_F applied this iteration, or nullptr
   float ca, cb, cc;             // quintic coefficients
@@ -128,7 +147,8 @@ struct NsGemmParams {
   void* sym_out_lo;             // Gram modes: lo plane of the output
   int sym_n128;                 // CTA-pair symmetric products: tiles with at most 128 valid
                                 // columns run N = 128 (B through a 64-row-box map)
-  const void* sym_in_lo;        // G_P: R lo plane
+  const void* sym_in_lo;        // G_P: R lo plane; F_POLY: A's second plane
+  const void* sym_in_2;         // F_POLY: A's third plane
   const void* op_b;             // fp32 path, G_PROD: the second factor
   float* pdiag;                 // tensor-core path: fp32 diagonal of P [batch][m]
   long long ldm;
@@ -167,6 +187,13 @@ cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& map_a,
 cudaError_t launch_ns_gemm_tc_planes(int mode, int bn, const CUtensorMap& map_a0, const CUtensorMap& map_a1,
                                      const CUtensorMap& map_b0, const CUtensorMap& map_b1, const CUtensorMap& map_so,
                                      const CUtensorMap& map_so_lo, const NsGemmParams& p, int grid, cudaStream_t s);
+// fp32 tensor-core path (MODE_F_*; one CTA per SM, 128 x 128 tiles): a[3] and
+// b[3] are the operands' three planes (64 x 128 boxes for K-major operands,
+// 64 x 64 for the MN-major X of F_UPDATE / F_FINAL); o[3] are 32 x 32-box maps
+// of the output's three planes (symmetric output of F_SYRK / F_POLY, the next
+// X of F_UPDATE; unused by F_FINAL).
+cudaError_t launch_ns_gemm_tc_f32(int mode, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* o,
+                                  const NsGemmParams& p, int grid, cudaStream_t s);
 // CTA-pair variant (tcgen05 cta_group::2, 256 x 256 tiles): `pairs`
 // clusters of two CTAs; tiles use 256-row blocks (p.tri / p.mi in 256-row
 // units) and, for UPDATE / FINAL, 256-column blocks.

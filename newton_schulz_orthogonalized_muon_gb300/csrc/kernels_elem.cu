@@ -2,9 +2,11 @@
 //
 //  * muon_prepare_kernel: momentum M <- mu*M + G, Nesterov U = G + mu*M
 //    (else U = M), per-tile partial sums of U^2 for the Frobenius norm, and
-//    the NS working copy of U (fp32 for the fp32 path; for the tensor-core
-//    path the bf16 MMA operand hi = bf16(U) and the lo plane bf16(U - hi)),
-//    transposed through shared memory when the block has rows > cols.
+//    the NS working copy of U (fp32 for the fp32 CUDA-core path; for the
+//    tensor-core path the bf16 MMA operand hi = bf16(U) and the lo plane
+//    bf16(U - hi), and for the fp32 tensor-core path a third plane
+//    bf16(U - hi - lo)), transposed through shared memory when the block has
+//    rows > cols.
 //    ("迎接DeepSeek开源周…Muon优化器" (coreui.cn), §代码, Muon step;
 //     "Muon Optimizer and the Distributed Implementation", §Newton-Schulz
 //     Iteration, normalisation by the Frobenius norm.)
@@ -23,15 +25,29 @@ namespace muon {
 
 constexpr int PT = 64;           // prepare tile: 64 x 64 elements
 
-// bf16 pairs of hi = bf16(u) and lo = bf16(u - hi) for 2 * pairs values
-__device__ __forceinline__ void split_hi_lo(const float* u, uint32_t* hw, uint32_t* lw, int pairs) {
+// bf16 pairs of hi = bf16(u) and lo = bf16(u - hi) for 2 * pairs values,
+// and (l2w non-null) the third plane bf16(u - hi - lo)
+__device__ __forceinline__ void split_hi_lo(const float* u, uint32_t* hw, uint32_t* lw, int pairs,
+                                            uint32_t* l2w = nullptr) {
 #pragma unroll
   for (int k = 0; k < pairs; ++k) {
     const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
     const float2 hf = __bfloat1622float2(h2);
     hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
-    lw[k] = pack_bf16x2(u[2 * k] - hf.x, u[2 * k + 1] - hf.y);
+    const float r0 = u[2 * k] - hf.x, r1 = u[2 * k + 1] - hf.y;
+    const __nv_bfloat162 l2 = __floats2bfloat162_rn(r0, r1);
+    lw[k] = *reinterpret_cast<const uint32_t*>(&l2);
+    if (l2w != nullptr) {
+      const float2 lf = __bfloat1622float2(l2);
+      l2w[k] = pack_bf16x2(r0 - lf.x, r1 - lf.y);
+    }
   }
+}
+
+// the third plane of one value
+__device__ __forceinline__ __nv_bfloat16 third_plane(float u) {
+  const float r = u - bf2f(f2bf(u));
+  return f2bf(r - bf2f(f2bf(r)));
 }
 constexpr int PREP_THREADS = 256;
 
@@ -124,16 +140,18 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
             *reinterpret_cast<float4*>(p.xf + xo + 4) = make_float4(u[4], u[5], u[6], u[7]);
           }
           if (p.xb != nullptr) {
-            uint32_t hw[4], lw[4];
-            split_hi_lo(u, hw, lw, 4);
+            uint32_t hw[4], lw[4], l2w[4];
+            split_hi_lo(u, hw, lw, 4, l2w);
             *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            if (p.xlo2 != nullptr) *reinterpret_cast<uint4*>(p.xlo2 + xo) = make_uint4(l2w[0], l2w[1], l2w[2], l2w[3]);
           }
         } else {
           for (int k = 0; k < 8 && c + k < e.cols; ++k) {
             if (p.xf != nullptr) p.xf[xo + k] = u[k];
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
             if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
+            if (p.xlo2 != nullptr) p.xlo2[xo + k] = third_plane(u[k]);
           }
         }
       }
@@ -160,16 +178,18 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
         if (r + 3 < e.rows) {
           if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
           if (p.xb != nullptr) {
-            uint32_t hw[2], lw[2];
-            split_hi_lo(u, hw, lw, 2);
+            uint32_t hw[2], lw[2], l2w[2];
+            split_hi_lo(u, hw, lw, 2, l2w);
             *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(hw[0], hw[1]);
             if (p.xlo != nullptr) *reinterpret_cast<uint2*>(p.xlo + xo) = make_uint2(lw[0], lw[1]);
+            if (p.xlo2 != nullptr) *reinterpret_cast<uint2*>(p.xlo2 + xo) = make_uint2(l2w[0], l2w[1]);
           }
         } else {
           for (int k = 0; k < 4 && r + k < e.rows; ++k) {
             if (p.xf != nullptr) p.xf[xo + k] = u[k];
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
             if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
+            if (p.xlo2 != nullptr) p.xlo2[xo + k] = third_plane(u[k]);
           }
         }
       }
@@ -323,12 +343,13 @@ __global__ void desc_copy_kernel(uint4* __restrict__ dst, const uint4* __restric
 }
 
 // ------------------------------------------------------------- launchers
-bool pdl_enabled() {
-  static const bool on = [] {
+int pdl_level() {
+  static const int level = [] {
     const char* v = std::getenv("MUON_PDL");
-    return !(v != nullptr && v[0] == '0');
+    if (v == nullptr) return 1;
+    return v[0] == '0' ? 0 : v[0] == '2' ? 2 : 1;
   }();
-  return on;
+  return level;
 }
 
 cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
@@ -336,13 +357,13 @@ cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStrea
   if (n16 == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<size_t>((n16 + threads - 1) / threads, 1024));
-  return launch_k(desc_copy_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(dst),
+  return launch_k(pdl_level() >= 2, desc_copy_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(dst),
                   static_cast<const uint4*>(src), n16);
 }
 cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s) {
   if (batch == 0 || tiles_per_mat == 0) return cudaSuccess;
   dim3 grid(tiles_per_mat, batch);
-  return launch_k(muon_prepare_kernel, grid, dim3(PREP_THREADS), 0, s, p);
+  return launch_k(pdl_level() >= 2, muon_prepare_kernel, grid, dim3(PREP_THREADS), 0, s, p);
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
@@ -350,7 +371,7 @@ cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int b
   if (batch == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (batch * 32 + threads - 1) / threads;
-  return launch_k(norm_finalize_kernel, dim3(blocks), dim3(threads), 0, s, partials, tiles_per_mat, batch, eps, scale,
+  return launch_k(pdl_level() >= 2, norm_finalize_kernel, dim3(blocks), dim3(threads), 0, s, partials, tiles_per_mat, batch, eps, scale,
                   err);
 }
 
@@ -360,12 +381,12 @@ cudaError_t launch_apply(const ApplyParams& p, int batch, cudaStream_t s) {
   int bx = static_cast<int>((total + 255) / 256);
   if (bx > 1024) bx = 1024;
   if (bx < 1) bx = 1;
-  return launch_k(apply_kernel, dim3(bx, batch), dim3(256), 0, s, p);
+  return launch_k(pdl_level() >= 2, apply_kernel, dim3(bx, batch), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_adamw(const AdamParams& p, int n_chunks, cudaStream_t s) {
   if (n_chunks == 0) return cudaSuccess;
-  return launch_k(adamw_kernel, dim3(n_chunks), dim3(256), 0, s, p);
+  return launch_k(pdl_level() >= 2, adamw_kernel, dim3(n_chunks), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t s) {

@@ -93,9 +93,11 @@ struct Cfg {
 template <int MODE, int BN, int AP, int BP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     ns_gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-                      const __grid_constant__ CUtensorMap map_b0, const __grid_constant__ CUtensorMap map_b1,
+                      const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_b0,
+                      const __grid_constant__ CUtensorMap map_b1, const __grid_constant__ CUtensorMap map_b2,
                       const __grid_constant__ CUtensorMap map_xh, const __grid_constant__ CUtensorMap map_xl,
                       const __grid_constant__ CUtensorMap map_xo, const NsGemmParams p) {
+  static_assert(AP <= 3 && BP <= 3 && (AP < 3 || BP == 3), "operand planes");
   using C = Cfg<MODE, BN, AP, BP>;
   using L = EpiLayout<MODE, OneSlots<MODE>::v>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
@@ -135,14 +137,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 1 && lane == 0) {
     tma_prefetch_map(&map_a0);
     tma_prefetch_map(&map_b0);
-    if (AP == 2) tma_prefetch_map(&map_a1);
-    if (BP == 2) tma_prefetch_map(&map_b1);
+    if (AP >= 2) tma_prefetch_map(&map_a1);
+    if (AP >= 3) tma_prefetch_map(&map_a2);
+    if (BP >= 2) tma_prefetch_map(&map_b1);
+    if (BP >= 3) tma_prefetch_map(&map_b2);
     if (L::kLoadX) {
       tma_prefetch_map(&map_xh);
       tma_prefetch_map(&map_xl);
     }
     if (MODE == MODE_UPDATE || SymEpi<MODE>::kTma) tma_prefetch_map(&map_xo);
-    if (ModeTraits<MODE>::kPlanesOut) tma_prefetch_map(&map_xl);
+    if (ModeTraits<MODE>::kOutPlanes >= 2) tma_prefetch_map(&map_xl);
+    if (ModeTraits<MODE>::kOutPlanes >= 3) tma_prefetch_map(&map_xh);
   }
   tc_fence_before();
   __syncthreads();
@@ -173,12 +178,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
 #pragma unroll
           for (int pa = 0; pa < AP; ++pa) {
-            const CUtensorMap* ma = pa == 0 ? &map_a0 : &map_a1;
+            const CUtensorMap* ma = pa == 0 ? &map_a0 : pa == 1 ? &map_a1 : &map_a2;
             tma_load_3d(sa + pa * C::A_BYTES, ma, &full[s], kb * BK, i * BM, b);     // one 128-row box
           }
 #pragma unroll
           for (int pb = 0; pb < BP; ++pb) {
-            const CUtensorMap* mb = pb == 0 ? &map_b0 : &map_b1;
+            const CUtensorMap* mb = pb == 0 ? &map_b0 : pb == 1 ? &map_b1 : &map_b2;
 #pragma unroll
             for (int q = 0; q < BN / 64; ++q) {
               if (kUpd)        // MN-major: 64 columns x 64 K rows per box
@@ -229,12 +234,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t boff = kUpd ? kk * 2048 : kk * 32;
             const uint64_t b0 = kUpd ? sdesc_sw128(sb + boff, BOX_BYTES, 1024) : sdesc_sw128(sb + boff, 16, 1024);
             umma_bf16(d, a0, b0, idesc, (kb | kk) != 0 ? 1u : 0u);
-            if (BP == 2) {   // hi(A) * lo(B)
-              const uint32_t sb1 = sb + C::B_BYTES + boff;
-              umma_bf16(d, a0, kUpd ? sdesc_sw128(sb1, BOX_BYTES, 1024) : sdesc_sw128(sb1, 16, 1024), idesc, 1u);
-            }
-            if (AP == 2) {   // lo(A) * hi(B)
-              umma_bf16(d, sdesc_sw128(sa + C::A_BYTES + kk * 32, 16, 1024), b0, idesc, 1u);
+            // plane q of A / B in this stage
+            auto adesc = [&](int q) { return sdesc_sw128(sa + q * C::A_BYTES + kk * 32, 16, 1024); };
+            auto bdesc = [&](int q) {
+              const uint32_t sbq = sb + q * C::B_BYTES + boff;
+              return kUpd ? sdesc_sw128(sbq, BOX_BYTES, 1024) : sdesc_sw128(sbq, 16, 1024);
+            };
+            if (BP >= 2) umma_bf16(d, a0, bdesc(1), idesc, 1u);          // p0(A) * p1(B)
+            if (AP >= 2) umma_bf16(d, adesc(1), b0, idesc, 1u);          // p1(A) * p0(B)
+            if (AP == 3) {                                               // the terms of order 2^-16
+              umma_bf16(d, a0, bdesc(2), idesc, 1u);                     // p0(A) * p2(B)
+              umma_bf16(d, adesc(1), bdesc(1), idesc, 1u);               // p1(A) * p1(B)
+              umma_bf16(d, adesc(2), b0, idesc, 1u);                     // p2(A) * p0(B)
             }
           }
           umma_commit(&empty[s]);
@@ -263,7 +274,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     et.row_off = 0;
     et.remote = false;
     et.tempty = tempty;
-    sym_epilogue<MODE, BN, BM>(p, &map_xo, &map_xl, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp, lane);
+    sym_epilogue<MODE, BN, BM>(p, &map_xo, &map_xl, &map_xh, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort,
+                               tmem_base, warp, lane);
   } else {
     // --------------------------------------------------------- epilogue
     EpiTiles et{};
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 template <int MODE, int BN, int AP, int BP>
 cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
                        const CUtensorMap& xh, const CUtensorMap& xl, const CUtensorMap& xo, const NsGemmParams& p,
-                       int grid, cudaStream_t s) {
+                       int grid, cudaStream_t s, const CUtensorMap* a2 = nullptr, const CUtensorMap* b2 = nullptr) {
   auto kern = ns_gemm_tc_kernel<MODE, BN, AP, BP>;
   using C = Cfg<MODE, BN, AP, BP>;
   static bool configured = false;   // per instantiation; the attribute is per device function
@@ -297,7 +309,8 @@ cudaError_t launch_one(const CUtensorMap& a0, const CUtensorMap& a1, const CUten
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const cudaError_t e = launch_k(kern, dim3(grid), dim3(TC_THREADS), C::SMEM, s, a0, a1, b0, b1, xh, xl, xo, p);
+  const cudaError_t e = launch_k(pdl_level() >= 1, kern, dim3(grid), dim3(TC_THREADS), C::SMEM, s, a0, a1, a2 ? *a2 : a1, b0, b1,
+                                 b2 ? *b2 : b1, xh, xl, xo, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -339,6 +352,20 @@ cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& ma, co
       case MODE_FINAL: return launch_one<MODE_FINAL, 128, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
       case MODE_FINAL_T: return launch_one<MODE_FINAL_T, 128, 1, 1>(ma, ma, mb, mb, mxh, mxl, mxo, p, grid, s);
     }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ns_gemm_tc_f32(int mode, const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* o,
+                                  const NsGemmParams& p, int grid, cudaStream_t s) {
+  if (p.num_tiles == 0) return cudaSuccess;
+  switch (mode) {
+    // symmetric outputs: first plane through map_xo, then map_xl, map_xh
+    case MODE_F_SYRK: return launch_one<MODE_F_SYRK, 128, 3, 3>(a[0], a[1], b[0], b[1], o[2], o[1], o[0], p, grid, s, &a[2], &b[2]);
+    case MODE_F_POLY: return launch_one<MODE_F_POLY, 128, 3, 3>(a[0], a[1], b[0], b[1], o[2], o[1], o[0], p, grid, s, &a[2], &b[2]);
+    // the next X's planes through map_xh, map_xl, map_xo
+    case MODE_F_UPDATE: return launch_one<MODE_F_UPDATE, 128, 3, 3>(a[0], a[1], b[0], b[1], o[0], o[1], o[2], p, grid, s, &a[2], &b[2]);
+    case MODE_F_FINAL: return launch_one<MODE_F_FINAL, 128, 3, 3>(a[0], a[1], b[0], b[1], b[0], b[0], b[0], p, grid, s, &a[2], &b[2]);
   }
   return cudaErrorInvalidValue;
 }

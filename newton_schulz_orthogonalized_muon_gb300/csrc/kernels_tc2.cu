@@ -255,8 +255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     et.tempty = nullptr;
     et.tempty_remote[0] = mapa_shared(smem_u32(&tempty[0]), 0);
     et.tempty_remote[1] = mapa_shared(smem_u32(&tempty[1]), 0);
-    sym_epilogue<MODE, PBN, PBM>(p, &map_xo, &map_xl, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort, tmem_base, warp,
-                                 lane);
+    sym_epilogue<MODE, PBN, PBM>(p, &map_xo, &map_xl, &map_xl, epi + (warp - 2) * SYM_WARP_BYTES, tfull, et, abort,
+                                 tmem_base, warp, lane);
   } else {
     // --------------------------------------------------------- epilogue
     // UPDATE / FINAL: each CTA drains its own 128 accumulator rows of the
@@ -296,7 +296,7 @@ cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const cudaError_t e = launch_k(kern, dim3(2 * pairs), dim3(TC_THREADS), C::SMEM, s, a0, a1, b0, b1, xh, xl, xo, p);
+  const cudaError_t e = launch_k(pdl_level() >= 1, kern, dim3(2 * pairs), dim3(TC_THREADS), C::SMEM, s, a0, a1, b0, b1, xh, xl, xo, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -82,7 +82,8 @@ struct muon_handle_s {
   int pair_min_m = 1024;        // ragged m from here on runs its symmetric products on pairs too (MUON_TC_PAIR_MIN_M)
   int max_pairs = 0;
   bool final_tma = true;        // FINAL into bf16 destinations through tensor maps (MUON_FINAL_TMA=0 disables)
-  bool split_ragged = true;     // ragged-m UPDATE / FINAL split between pairs and one SM (MUON_TC_SPLIT=0 disables)
+  bool f32_tc = true;           // fp32 standard method on the tensor cores, three bf16 planes (MUON_F32_TC=0:
+                                // CUDA cores)
 };
 
 namespace {
@@ -270,8 +271,6 @@ struct GroupPlan {
   int tri256_count = 0;
   bool pair = false;            // symmetric products on CTA pairs
   bool pair_upd = false;        // UPDATE / FINAL on CTA pairs
-  bool split_upd = false;       // UPDATE / FINAL: rows below the last multiple of 256 on CTA
-                                // pairs, the remaining 128-row blocks on one SM
   std::vector<std::pair<size_t, size_t>> chunk_off;   // (src offset, out offset) per chunk
   std::vector<size_t> chunk_wmap;   // per chunk: offset of the destinations' tensor maps, or kNoMaps
 };
@@ -306,15 +305,19 @@ bool encode_dest_maps(muon_handle_t h, const GroupPlan& g, const std::vector<Out
 //   gram, tensor cores:     bf16 X0 (+ fp32 X0 when no NS step runs) and six
 //                           m x m slots (R, T, P0, P1, Q0, Q1) of two bf16 planes
 //   gram, fp32 path:        fp32 X0 and six fp64 m x m slots
+//   standard, fp32 path on the tensor cores (f32tc): X as three bf16 planes
+//                           in two ping-pong sets, A and P as three planes
+//                           each (+ fp32 X0 when no NS step runs)
 constexpr int kGramSlots = 6;
 enum { SLOT_R = 0, SLOT_T = 1, SLOT_P0 = 2, SLOT_Q0 = 4 };
 
 struct Regions {
   size_t xf, xf2, xlo, xb0, xb1, symA, symB, pdiag, partials, scale, total;
   size_t slot[kGramSlots], slot_lo[kGramSlots];
+  size_t xp[2][3], ap[3], pp[3];   // f32tc planes
 };
 
-Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
+Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps, bool f32tc = false) {
   Regions r{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -324,7 +327,13 @@ Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps) {
   };
   const size_t xe = static_cast<size_t>(cap) * g.m * g.ldx;
   const size_t se = static_cast<size_t>(cap) * g.m * g.ldm;
-  if (!gram) {
+  if (f32tc && !gram && !tc) {
+    r.xf = (steps == 0) ? take(xe * 4) : 0;
+    for (int q = 0; q < 2; ++q)
+      for (int k = 0; k < 3; ++k) r.xp[q][k] = take(xe * 2);
+    for (int k = 0; k < 3; ++k) r.ap[k] = take(se * 2);
+    for (int k = 0; k < 3; ++k) r.pp[k] = take(se * 2);
+  } else if (!gram) {
     if (tc) {
       // master X = hi + lo: hi is the operand copy (xb0 / xb1 ping-pong), lo
       // in place; the fp32 copy only when no NS step runs
@@ -524,29 +533,131 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
   return MUON_OK;
 }
 
+// Standard method of the fp32 path on the tensor cores for one same-shape
+// group: X, A and P held as three bf16 planes (24 mantissa bits), every
+// product six MMAs per K step with fp32 accumulation (internal.h, MODE_F_*):
+//   prepare (X0 planes) -> norm -> steps x [F_SYRK -> F_POLY -> F_UPDATE]
+// with the last F_UPDATE replaced by F_FINAL into the destinations.  The
+// iteration is the pages' X <- (aI + bA + cA^2) X, A = X X^T ("Muon Optimizer
+// and the Distributed Implementation", §Newton-Schulz Iteration).
+muon_status_t run_f32tc_group(muon_handle_t h, const GroupPlan& g, const Regions& R, uint8_t* ws, uint8_t* dbase,
+                              int steps, const float* coeffs, int coeff_stride, float mu, int nesterov,
+                              cudaStream_t stream) {
+  float* xf = reinterpret_cast<float*>(ws + R.xf);
+  float* partials = reinterpret_cast<float*>(ws + R.partials);
+  float* scale = reinterpret_cast<float*>(ws + R.scale);
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+  // per X set q and plane k: K-major (64 x 128 boxes), MN-major (64 x 64) and
+  // 32 x 32 output maps; A and P planes: K-major operand and 32 x 32 output maps
+  CUtensorMap xk[2][3], xmn[2][3], xo[2][3], ak[3], ao[3], pk[3], po[3];
+  if (steps > 0) {
+    bool ok = true;
+    for (int q = 0; q < 2 && ok; ++q)
+      for (int k = 0; k < 3 && ok; ++k)
+        ok = encode_map(h, &xk[q][k], bf(R.xp[q][k]), g.n, g.m, g.chunk, g.ldx) &&
+             encode_map(h, &xmn[q][k], bf(R.xp[q][k]), g.n, g.m, g.chunk, g.ldx, 64) &&
+             encode_box32(h->encode, &xo[q][k], bf(R.xp[q][k]), false, g.n, g.m, g.chunk, g.ldx);
+    for (int k = 0; k < 3 && ok; ++k)
+      ok = encode_map(h, &ak[k], bf(R.ap[k]), g.m, g.m, g.chunk, g.ldm) &&
+           encode_box32(h->encode, &ao[k], bf(R.ap[k]), false, g.m, g.m, g.chunk, g.ldm) &&
+           encode_map(h, &pk[k], bf(R.pp[k]), g.m, g.m, g.chunk, g.ldm) &&
+           encode_box32(h->encode, &po[k], bf(R.pp[k]), false, g.m, g.m, g.chunk, g.ldm);
+    if (!ok) return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  }
+  const int mi = static_cast<int>(ceil_div(g.m, 128));
+  const int nj = static_cast<int>(ceil_div(g.n, 128));
+  for (size_t c = 0; c < g.chunk_off.size(); ++c) {
+    const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
+    const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
+    const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+    PrepParams pp{};
+    pp.src = src_d;
+    pp.mu = mu;
+    pp.nesterov = nesterov;
+    pp.m = g.m;
+    pp.ldx = g.ldx;
+    pp.xf = steps > 0 ? nullptr : xf;
+    pp.xb = steps > 0 ? bf(R.xp[0][0]) : nullptr;
+    pp.xlo = steps > 0 ? bf(R.xp[0][1]) : nullptr;
+    pp.xlo2 = steps > 0 ? bf(R.xp[0][2]) : nullptr;
+    pp.partials = partials;
+    pp.tiles_per_mat = g.prep_tiles;
+    MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");
+    MUON_LAUNCH(MUON_K_NORM, launch_norm_finalize(partials, g.prep_tiles, cnt, kNormEps, scale, h->err, stream),
+                "norm launch");
+    if (steps == 0) {
+      ApplyParams ap{out_d, scale, xf, g.ldx, g.m, g.n};
+      MUON_LAUNCH(MUON_K_APPLY, launch_apply(ap, cnt, stream), "apply launch");
+      continue;
+    }
+    for (int it = 0; it < steps; ++it) {
+      const int cur = it & 1, nxt = cur ^ 1;
+      const bool last = (it == steps - 1);
+      NsGemmParams p{};
+      p.m = g.m;
+      p.n = g.n;
+      p.batch = cnt;
+      p.scale = it == 0 ? scale : nullptr;
+      p.ca = coeffs[it * coeff_stride];
+      p.cb = coeffs[it * coeff_stride + 1];
+      p.cc = coeffs[it * coeff_stride + 2];
+      p.ldm = g.ldm;
+      p.ldx = g.ldx;
+      p.out = out_d;
+      p.err = h->err;
+      p.timeout_ns = h->timeout_ns;
+      NsGemmParams q = p;
+      q.tiles_per_mat = g.tri128_count;
+      q.num_tiles = cnt * g.tri128_count;
+      q.tri = reinterpret_cast<const int2*>(dbase + g.tri128_off);
+      const int grid_sym = std::max(1, std::min(q.num_tiles, h->num_sms));
+      // A = s^2 X X^T
+      MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc_f32(MODE_F_SYRK, xk[cur], xk[cur], ao, q, grid_sym, stream),
+                  "f32 syrk launch");
+      // P = a I + b A + c A A
+      q.scale = nullptr;
+      q.sym_in = ws + R.ap[0];
+      q.sym_in_lo = ws + R.ap[1];
+      q.sym_in_2 = ws + R.ap[2];
+      MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc_f32(MODE_F_POLY, ak, ak, po, q, grid_sym, stream), "f32 poly launch");
+      // X' = s P X (planes), or the destination update
+      NsGemmParams u = p;
+      u.mi = mi;
+      u.tiles_per_mat = mi * nj;
+      u.num_tiles = cnt * mi * nj;
+      const int grid = std::max(1, std::min(u.num_tiles, h->num_sms));
+      MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                  launch_ns_gemm_tc_f32(last ? MODE_F_FINAL : MODE_F_UPDATE, pk, xmn[cur], xo[nxt], u, grid, stream),
+                  "f32 update launch");
+    }
+  }
+  return MUON_OK;
+}
+
 // Run prepare + Newton-Schulz + final write for every block.
 // Strides, tile widths and the chunk (matrices per launch) of one same-shape
 // group under the handle's workspace limit; returns the workspace bytes the
 // group's chunk needs.
 size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps) {
+  const bool f32tc = !tc && !gram && h->f32_tc;
   g.ldx = static_cast<long long>(align_up(g.n, 8));
   g.ldm = static_cast<long long>(align_up(g.m, 8));
   g.prep_tiles = static_cast<int>(ceil_div(g.m, 64) * ceil_div(g.n, 64));
   g.bn_sym = g.m <= 128 ? 128 : 256;
   g.bn_upd = g.n <= 128 ? 128 : 256;
-  const size_t per1 = regions(g, 1, tc, gram, steps).total;
-  const size_t per2 = regions(g, 2, tc, gram, steps).total;
+  const size_t per1 = regions(g, 1, tc, gram, steps, f32tc).total;
+  const size_t per2 = regions(g, 2, tc, gram, steps, f32tc).total;
   g.per_mat = per2 > per1 ? per2 - per1 : per1;
   const size_t fixed = per1 > g.per_mat ? per1 - g.per_mat : 0;
   size_t fit = h->ws_limit > fixed ? (h->ws_limit - fixed) / std::max<size_t>(g.per_mat, 1) : 1;
   fit = std::max<size_t>(fit, 1);
   fit = std::min<size_t>(fit, g.members.size());
   fit = std::min<size_t>(fit, 65535);
-  const int tiles_upd = static_cast<int>(ceil_div(g.m, 128) * ceil_div(g.n, g.bn_upd));
+  const int tiles_upd = static_cast<int>(ceil_div(g.m, 128) * ceil_div(g.n, f32tc ? 128 : g.bn_upd));
   const int tiles_max = std::max({tiles_upd, g.prep_tiles, 1});
   fit = std::min<size_t>(fit, static_cast<size_t>((1u << 31) - 1) / static_cast<size_t>(tiles_max));
   g.chunk = static_cast<int>(fit);
-  return regions(g, g.chunk, tc, gram, steps).total;
+  return regions(g, g.chunk, tc, gram, steps, f32tc).total;
 }
 
 // coeffs: (a, b, c) of step k at coeffs[k * coeff_stride] (stride 0: one
@@ -555,6 +666,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                          const float* coeffs, int coeff_stride, int ns_method, bool tc, cudaStream_t stream) {
   if (blocks.empty()) return MUON_OK;
   const bool gram = (ns_method == MUON_NS_GRAM);
+  const bool f32tc = !tc && !gram && h->f32_tc;
 
   std::map<std::pair<int, int>, GroupPlan> groups;
   for (size_t i = 0; i < blocks.size(); ++i) {
@@ -569,6 +681,11 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   for (auto& kv : groups) {
     GroupPlan& g = kv.second;
     ws_need = std::max(ws_need, plan_group(h, g, tc, gram, steps));
+    if (f32tc) {
+      std::vector<int2> t128 = sym_tiles(g.m, 128);
+      g.tri128_count = static_cast<int>(t128.size());
+      g.tri128_off = arena_push(arena, t128.data(), t128.size());
+    }
     if (tc) {
       std::vector<int2> tri = sym_tiles(g.m, g.bn_sym);
       g.tri_count = static_cast<int>(tri.size());
@@ -583,13 +700,10 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         g.tri256_count = static_cast<int>(t256.size());
         g.tri256_off = arena_push(arena, t256.data(), t256.size());
         g.pair = true;
-        // UPDATE / FINAL on pairs without a ragged last row tile; with one,
-        // the pairs take the rows below the last multiple of 256 and a
-        // one-SM launch the rest (a half-empty 256-row pair tile costs more
-        // than the extra launch), or, with the split switched off, pairs
-        // from m = 2048
-        g.pair_upd = h->pair_update && (g.m % 256 == 0 || (!h->split_ragged && g.m >= 2048));
-        g.split_upd = h->pair_update && h->split_ragged && g.m % 256 != 0;
+        // UPDATE / FINAL on pairs only without a ragged last row tile, or
+        // from m = 2048 (a ragged tile costs them more than the symmetric
+        // products)
+        g.pair_upd = h->pair_update && (g.m % 256 == 0 || g.m >= 2048);
       }
     }
     for (size_t c0 = 0; c0 < g.members.size(); c0 += g.chunk) {
@@ -621,7 +735,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   for (auto& kv : groups) {
     GroupPlan& g = kv.second;
     h->prof_tag = group_index++;
-    const Regions R = regions(g, g.chunk, tc, gram, steps);
+    const Regions R = regions(g, g.chunk, tc, gram, steps, f32tc);
+    if (f32tc) {
+      muon_status_t fst = run_f32tc_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, mu, nesterov, stream);
+      if (fst != MUON_OK) return fst;
+      continue;
+    }
     if (gram) {
       muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, tc, mu, nesterov, stream);
       if (gst != MUON_OK) return gst;
@@ -727,15 +846,9 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                       launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream, n128 ? &map_A64 : nullptr),
                       "poly launch");
           NsGemmParams u = p;
-          if (g.pair_upd || g.split_upd) {
-            // pairs: whole 256-row blocks (all of them, or those below the
-            // ragged tail); the tail's 128-row blocks on one SM after them.
-            // The two launches write disjoint rows of the new hi / lo planes
-            // and of the destinations, and both read this iteration's X^.
-            const int mi2 = static_cast<int>(g.pair_upd ? ceil_div(g.m, 256) : g.m / 256);
-            const int nj2 = static_cast<int>(ceil_div(g.n, 256));
+          if (g.pair_upd) {
+            const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
             u.mi = mi2;
-            u.mi0 = 0;
             u.tiles_per_mat = mi2 * nj2;
             u.num_tiles = cnt * mi2 * nj2;
             const int upairs = std::min(u.num_tiles, h->max_pairs);
@@ -744,18 +857,6 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                                                    map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream,
                                                    g.m <= kShortK ? 2 : 0),
                         "update launch");
-            if (g.split_upd) {
-              NsGemmParams w = p;
-              w.mi0 = (g.m / 256) * 2;                       // first 128-row block of the tail
-              w.mi = mi - w.mi0;
-              w.tiles_per_mat = w.mi * nj;
-              w.num_tiles = cnt * w.tiles_per_mat;
-              const int grid = std::min(w.num_tiles, h->num_sms);
-              MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                          launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
-                                                   map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], w, grid, stream),
-                          "update tail launch");
-            }
           } else {
             u.mi = mi;
             u.tiles_per_mat = mi * nj;
@@ -919,7 +1020,7 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
   }
   h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
   if (const char* ft = std::getenv("MUON_FINAL_TMA")) h->final_tma = ft[0] != '0';
-  if (const char* sp = std::getenv("MUON_TC_SPLIT")) h->split_ragged = sp[0] != '0';
+  if (const char* ft = std::getenv("MUON_F32_TC")) h->f32_tc = ft[0] != '0';
   bool ok = cudaMalloc(&h->err, sizeof(unsigned)) == cudaSuccess && cudaMemset(h->err, 0, sizeof(unsigned)) == cudaSuccess;
   for (int k = 0; ok && k < muon_handle_s::kStages; ++k)
     ok = cudaEventCreateWithFlags(&h->stage_ev[k], cudaEventDisableTiming) == cudaSuccess;

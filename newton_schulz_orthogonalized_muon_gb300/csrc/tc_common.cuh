@@ -21,13 +21,19 @@ constexpr unsigned long long DRAIN_NS = 1000000000ull;
 template <int MODE>
 struct ModeTraits {
   static constexpr bool kSym = (MODE == MODE_SYRK || MODE == MODE_POLY || MODE == MODE_G_R0 ||
-                                MODE == MODE_G_P || MODE == MODE_G_PROD);
+                                MODE == MODE_G_P || MODE == MODE_G_PROD || MODE == MODE_F_SYRK ||
+                                MODE == MODE_F_POLY);
   static constexpr bool kMN =
       (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_G_FINAL || MODE == MODE_FINAL_T ||
-       MODE == MODE_G_FINAL_T);
+       MODE == MODE_G_FINAL_T || MODE == MODE_F_UPDATE || MODE == MODE_F_FINAL);
   static constexpr bool kTmaOut = (MODE == MODE_FINAL_T || MODE == MODE_G_FINAL_T);   // destinations by TMA
-  static constexpr bool kKn = (MODE == MODE_SYRK || MODE == MODE_G_R0);   // K = n (else K = m)
+  static constexpr bool kKn = (MODE == MODE_SYRK || MODE == MODE_G_R0 || MODE == MODE_F_SYRK);   // K = n (else K = m)
   static constexpr bool kPlanesOut = (MODE == MODE_G_R0 || MODE == MODE_G_P || MODE == MODE_G_PROD);
+  // bf16 planes each output value is stored as (symmetric products and F_UPDATE)
+  static constexpr int kOutPlanes =
+      kPlanesOut ? 2 : (MODE == MODE_F_SYRK || MODE == MODE_F_POLY || MODE == MODE_F_UPDATE) ? 3 : 1;
+  static constexpr bool kF32 = (MODE == MODE_F_SYRK || MODE == MODE_F_POLY || MODE == MODE_F_UPDATE ||
+                                MODE == MODE_F_FINAL);
 };
 
 // Warp-collective bounded wait: every lane polls, the warp leaves together.
@@ -60,7 +66,7 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
     j = ij.y;
   } else {
     j = l / p.mi;          // column-block major: neighbouring tiles share X's column block
-    i = l - j * p.mi + p.mi0;
+    i = l - j * p.mi;
   }
 }
 
@@ -83,6 +89,9 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
 //   FINAL_T (bf16 destinations with tensor maps): [hi | lo | W], W the
 //   destination's 32 x 32 block in destination orientation, loaded by TMA
 //   with hi and lo, updated in place and stored back by TMA; G_FINAL_T: [W].
+//   F_UPDATE (fp32 tensor-core path): no inputs; the result's three bf16
+//   planes leave by TMA through the slot, two 32 x 32 planes at a time.
+//   F_FINAL: as G_FINAL.
 // With the swizzles, one lane per row accessing 16-byte chunks of its row,
 // and eight lanes covering one row, are free of bank conflicts.
 template <int MODE, int XSLOTS = 2>
@@ -306,7 +315,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   for (int t = et.t0; t < p.num_tiles; t += et.tstep) {
     int b, i, j;
     decode_tile<MODE>(p, t, b, i, j);
-    if (MODE == MODE_FINAL || MODE == MODE_G_FINAL) {
+    if (MODE == MODE_FINAL || MODE == MODE_G_FINAL || MODE == MODE_F_FINAL) {
       // the tile's first block of old destination values, under the main loop
       const int g0p = j * BN + cbeg;
       if (g0p < p.n) prefetch_out_block(out_block(p.out[b], i * TROWS + et.row_off + quad * 32, g0p, p.m, p.n), lane, wpre);
@@ -328,7 +337,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
       pdb = bf2f(f2bf(pd));
     }
     OutEntry oe{};
-    if (MODE != MODE_UPDATE) oe = p.out[b];
+    if (MODE != MODE_UPDATE && MODE != MODE_F_UPDATE) oe = p.out[b];
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + cbeg);
     const int g0 = j * BN + cbeg;
     const int nb = g0 >= p.n ? 0 : min(NB, (p.n - g0 + 31) >> 5);
@@ -379,6 +388,52 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
           tma_store_3d(map_xl, src + L::LO_OFF, gcb, row0, b);
           bulk_commit_group();
           bulk_wait_read_all();          // the slot may be refilled
+        }
+        __syncwarp();
+      } else if constexpr (MODE == MODE_F_UPDATE) {
+        // X' = s * acc as three bf16 planes p0 + p1 + p2, stored by TMA:
+        // p0 and p1 through the slot's two halves, then p2 through the first
+        float v[32];
+        tmem_ld16(tb + static_cast<uint32_t>(32 * k), v);
+        tmem_ld16(tb + static_cast<uint32_t>(32 * k + 16), v + 16);
+        uint32_t w0[16], w1[16], w2[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x0 = s * v[2 * e], x1 = s * v[2 * e + 1];
+          const __nv_bfloat162 h0 = __floats2bfloat162_rn(x0, x1);
+          const float2 f0 = __bfloat1622float2(h0);
+          const float r0 = x0 - f0.x, r1 = x1 - f0.y;
+          const __nv_bfloat162 h1 = __floats2bfloat162_rn(r0, r1);
+          const float2 f1 = __bfloat1622float2(h1);
+          w0[e] = *reinterpret_cast<const uint32_t*>(&h0);
+          w1[e] = *reinterpret_cast<const uint32_t*>(&h1);
+          w2[e] = pack_bf16x2(r0 - f1.x, r1 - f1.y);
+        }
+        const uint32_t src = wsm;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(sbuf + sw64_off(lane, q)) = make_uint4(w0[4 * q], w0[4 * q + 1], w0[4 * q + 2], w0[4 * q + 3]);
+          *reinterpret_cast<uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)) =
+              make_uint4(w1[4 * q], w1[4 * q + 1], w1[4 * q + 2], w1[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.m) {
+          tma_store_3d(map_xh, src, gcb, row0, b);
+          tma_store_3d(map_xl, src + L::LO_OFF, gcb, row0, b);
+          bulk_commit_group();
+          bulk_wait_read_all();          // the first half may be rewritten
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(sbuf + sw64_off(lane, q)) = make_uint4(w2[4 * q], w2[4 * q + 1], w2[4 * q + 2], w2[4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.m) {
+          tma_store_3d(map_xo, src, gcb, row0, b);
+          bulk_commit_group();
+          bulk_wait_read_all();          // the slot is free for the next block
         }
         __syncwarp();
       } else if constexpr (ModeTraits<MODE>::kTmaOut) {
@@ -521,7 +576,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   if (lane == 0) {
     for (uint32_t u = done; u < issued; ++u)
       mbar_wait_bounded(&xfull[u % L::SLOTS], (u / L::SLOTS) & 1u, nullptr, DRAIN_NS);
-    if (MODE == MODE_UPDATE || ModeTraits<MODE>::kTmaOut) bulk_wait_all();
+    if (MODE == MODE_UPDATE || MODE == MODE_F_UPDATE || ModeTraits<MODE>::kTmaOut) bulk_wait_all();
   }
   __syncwarp();
 }
@@ -567,17 +622,19 @@ __device__ __forceinline__ void load_row32_bf16(const __nv_bfloat16* rowp, int g
 }
 
 // The tile loop of one epilogue warp for the symmetric products.  map_so:
-// the output (A, P, or the hi plane of a Gram-method matrix; bf16
-// [batch][m][ldm]) with 32 x 32 boxes, 64-byte swizzle; map_so_lo: the lo
-// plane of a Gram-method output (value - bf16(value)), written after the hi
-// plane through the same buffers.
+// the output (A, P, or the first plane of a Gram-method or fp32-path matrix;
+// bf16 [batch][m][ldm]) with 32 x 32 boxes, 64-byte swizzle; map_so_lo and
+// map_so_2: the further planes of a plane-split output (the residual of the
+// planes before), written after the first through the same buffers.
 template <int MODE, int BN, int TROWS>
 __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtensorMap* map_so,
-                                             const CUtensorMap* map_so_lo, uint8_t* wbuf, uint64_t* tfull,
-                                             const EpiTiles& et, volatile int* abort, uint32_t tmem_base, int warp,
-                                             int lane) {
-  constexpr bool kPlanes = ModeTraits<MODE>::kPlanesOut;
-  constexpr bool kReadIn = (MODE == MODE_POLY || MODE == MODE_G_P);   // the b * A (b * R) term
+                                             const CUtensorMap* map_so_lo, const CUtensorMap* map_so_2, uint8_t* wbuf,
+                                             uint64_t* tfull, const EpiTiles& et, volatile int* abort,
+                                             uint32_t tmem_base, int warp, int lane) {
+  constexpr int kNP = ModeTraits<MODE>::kOutPlanes;
+  // the b * A term (b * R): A's planes read back
+  constexpr bool kReadIn = (MODE == MODE_POLY || MODE == MODE_G_P || MODE == MODE_F_POLY);
+  constexpr int kInPlanes = MODE == MODE_G_P ? 2 : MODE == MODE_F_POLY ? 3 : 1;
   constexpr int NB = BN / 64;                          // 32-column blocks per warp per tile
   const int quad = warp & 3;
   const int cbeg = ((warp - 2) >> 2) * (BN / 2);
@@ -586,8 +643,9 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
   bool pending = false;                                // a bulk store may still read the buffers
   int acc = 0;
   uint32_t acc_ph = 0;
-  uint4 apre[4];                                       // POLY / G_P: the next block's 32 values of A (R hi)
-  uint4 apre_lo[4];                                    // G_P: and of R's lo plane
+  uint4 apre[4];                                       // POLY / G_P / F_POLY: the next block's 32 values of A
+  uint4 apre_lo[4];                                    // G_P, F_POLY: of its second plane
+  uint4 apre_2[4];                                     // F_POLY: of its third plane
   for (int t = et.t0; t < p.num_tiles; t += et.tstep) {
     int b, i, j;
     decode_tile<MODE>(p, t, b, i, j);
@@ -599,13 +657,16 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
     while (k0 < NB && g0 + 32 * k0 + 31 < row0) ++k0;
     const __nv_bfloat16* arow = nullptr;
     const __nv_bfloat16* arow_lo = nullptr;
+    const __nv_bfloat16* arow_2 = nullptr;
     if (kReadIn) {
       const size_t roff = (static_cast<size_t>(b) * m + (gr < m ? gr : 0)) * p.ldm;
       arow = reinterpret_cast<const __nv_bfloat16*>(p.sym_in) + roff;
-      if (MODE == MODE_G_P) arow_lo = reinterpret_cast<const __nv_bfloat16*>(p.sym_in_lo) + roff;
+      if (kInPlanes >= 2) arow_lo = reinterpret_cast<const __nv_bfloat16*>(p.sym_in_lo) + roff;
+      if (kInPlanes >= 3) arow_2 = reinterpret_cast<const __nv_bfloat16*>(p.sym_in_2) + roff;
       if (k0 < NB && g0 + 32 * k0 < m && gr < m) {
         load_row32_bf16(arow, g0 + 32 * k0, m, apre);
-        if (MODE == MODE_G_P) load_row32_bf16(arow_lo, g0 + 32 * k0, m, apre_lo);
+        if (kInPlanes >= 2) load_row32_bf16(arow_lo, g0 + 32 * k0, m, apre_lo);
+        if (kInPlanes >= 3) load_row32_bf16(arow_2, g0 + 32 * k0, m, apre_2);
       }
     }
     if (!mbar_wait_warp(&tfull[acc], acc_ph, abort, p.timeout_ns)) {
@@ -627,24 +688,33 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
       tmem_ld16(tb + static_cast<uint32_t>(32 * k), v);
       tmem_ld16(tb + static_cast<uint32_t>(32 * k + 16), v + 16);
       const bool diag = (gcb == row0);
-      if (MODE == MODE_SYRK || MODE == MODE_G_R0) {
+      if (MODE == MODE_SYRK || MODE == MODE_G_R0 || MODE == MODE_F_SYRK) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] *= s;
       } else if (kReadIn) {
         float a[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) unpack8(apre[q], a + 8 * q);
-        if (MODE == MODE_G_P) {
+        if (kInPlanes >= 2) {
+          // planes added smallest first: a = p0 + (p1 + p2)
           float al[32];
 #pragma unroll
           for (int q = 0; q < 4; ++q) unpack8(apre_lo[q], al + 8 * q);
+          if (kInPlanes >= 3) {
+            float a2[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) unpack8(apre_2[q], a2 + 8 * q);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) al[c] += a2[c];
+          }
 #pragma unroll
           for (int c = 0; c < 32; ++c) a[c] += al[c];
         }
         // the next block's A, under this block's stores
         if (k + 1 < NB && gcb + 32 < m && gr < m) {
           load_row32_bf16(arow, gcb + 32, m, apre);
-          if (MODE == MODE_G_P) load_row32_bf16(arow_lo, gcb + 32, m, apre_lo);
+          if (kInPlanes >= 2) load_row32_bf16(arow_lo, gcb + 32, m, apre_lo);
+          if (kInPlanes >= 3) load_row32_bf16(arow_2, gcb + 32, m, apre_2);
         }
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = fmaf(p.cb, a[c], p.cc * v[c]);
@@ -658,9 +728,9 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
         }
       }
 #pragma unroll 1
-      for (int pl = 0; pl < (kPlanes ? 2 : 1); ++pl) {
-      if (pl == 1) {
-        // lo plane: the rounding residual of the hi plane just written
+      for (int pl = 0; pl < kNP; ++pl) {
+      if (pl >= 1) {
+        // next plane: the rounding residual of the plane just written
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] -= bf2f(f2bf(v[c]));
       }
@@ -697,7 +767,7 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && row0 < m) {
-        const CUtensorMap* mo = pl == 0 ? map_so : map_so_lo;
+        const CUtensorMap* mo = pl == 0 ? map_so : pl == 1 ? map_so_lo : map_so_2;
         tma_store_3d(mo, out_s, gcb, row0, b);
         if (!diag) tma_store_3d(mo, mir_s, row0, gcb, b);
         bulk_commit_group();

@@ -130,57 +130,3 @@ def test_ragged_pair_tiles_match_oracle_and_single(handles, ragged_handle, shape
     assert _rel(ga, ref) < TOL_BF16
     assert _rel(ga, gb) < TOL_BF16
 
-
-@pytest.fixture(scope="module")
-def unsplit_handle(handles):
-    """A handle that runs the UPDATE / FINAL of ragged-m groups without the
-    pair / one-SM split (MUON_TC_SPLIT=0): on one SM below m = 2048, on
-    pairs with a half-empty last tile from there."""
-    pkg = handles[0]
-    old = os.environ.get("MUON_TC_SPLIT")
-    os.environ["MUON_TC_SPLIT"] = "0"
-    try:
-        return pkg.MuonHandle(0)
-    finally:
-        if old is None:
-            del os.environ["MUON_TC_SPLIT"]
-        else:
-            os.environ["MUON_TC_SPLIT"] = old
-
-
-@pytest.mark.parametrize("shape", [(1408, 2048), (2048, 1408), (1450, 1700), (2176, 2400), (1344, 1600)])
-@pytest.mark.parametrize("method", ["orthogonalize", "step"])
-def test_split_ragged_update_matches_unsplit_and_oracle(handles, unsplit_handle, shape, method):
-    """Ragged m (m mod 256 != 0): the default handle's UPDATE / FINAL run the
-    rows below the last multiple of 256 on CTA pairs and the one or two
-    remaining 128-row blocks on one SM (m = 1450 leaves 170 rows: two tail
-    blocks, the last ragged).  Against the oracle and the unsplit kernels."""
-    pkg, pair, _ = handles
-    X = wl.lowrank_grad(73, shape[0], shape[1], 64)
-    if method == "orthogonalize":
-        t = torch.tensor(X).to(torch.bfloat16).cuda()
-        ref = oracle.newton_schulz(t.double().cpu().numpy())
-        a, b = t.clone(), t.clone()
-        pkg.muon_orthogonalize(a, handle=pair)
-        pkg.muon_orthogonalize(b, handle=unsplit_handle)
-        torch.cuda.synchronize()
-        assert pair.check() == 0 and unsplit_handle.check() == 0
-        ga, gb = a.double().cpu().numpy(), b.double().cpu().numpy()
-        assert _rel(ga, ref) < TOL_BF16
-        assert _rel(ga, gb) < TOL_BF16
-    else:
-        # through FINAL into fp32 parameters (dW observed directly) with bf16 NS
-        W0 = wl.weight(74, shape).astype(np.float64)
-        G = torch.tensor(X).to(torch.bfloat16).cuda()
-        outs = []
-        for h in (pair, unsplit_handle):
-            W = torch.tensor(W0, dtype=torch.float32).cuda()
-            M = torch.zeros(shape, device="cuda")
-            pkg.muon_step([W], [G], [M], lr=0.02, wd=0.1, ns_dtype=torch.bfloat16, handle=h)
-            assert h.check() == 0
-            outs.append(W.double().cpu().numpy())
-        w_ref, _ = oracle.muon_step(torch.tensor(W0, dtype=torch.float32).double().numpy(), G.double().cpu().numpy(),
-                                    np.zeros(shape), lr=0.02, wd=0.1)
-        base = torch.tensor(W0, dtype=torch.float32).double().numpy() * (1 - 0.02 * 0.1)
-        for w in outs:
-            assert _rel(w - base, w_ref - base) < TOL_BF16

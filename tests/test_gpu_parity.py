@@ -539,3 +539,54 @@ def test_workspace_size_matches_the_allocation_of_a_step():
     # the workspace plus a descriptor buffer of at most a few MiB
     assert rounded <= used <= rounded + (16 << 20), (need, rounded, used)
     assert pkg.workspace_size([], handle=h) == 0
+
+
+# ------------------------------------------- fp32 path: tensor cores vs CUDA cores
+
+@pytest.fixture(scope="module")
+def cuda_core_handle(pkg):
+    """A handle whose fp32 path runs on the CUDA cores (MUON_F32_TC=0)."""
+    import os
+    old = os.environ.get("MUON_F32_TC")
+    os.environ["MUON_F32_TC"] = "0"
+    try:
+        return pkg.MuonHandle(0)
+    finally:
+        if old is None:
+            del os.environ["MUON_F32_TC"]
+        else:
+            os.environ["MUON_F32_TC"] = old
+
+
+F32_TC_SHAPES = ORTHO_SHAPES + [(768, 3072), (3072, 768), (768, 768), (130, 4100)]
+
+
+@pytest.mark.parametrize("shape", F32_TC_SHAPES)
+def test_fp32_tensor_core_path_matches_oracle_and_cuda_cores(pkg, cuda_core_handle, shape):
+    # fp32 inputs: the default handle runs the standard method on the tensor
+    # cores with three-plane bf16 operands (six MMAs per product); both it and
+    # the CUDA-core path are held to the fp32 bar against the oracle
+    X = wl.lowrank_grad(17, shape[0], shape[1], 32)
+    ref = oracle.newton_schulz(X.astype(np.float64))
+    a, b = to_dev(X, torch.float32), to_dev(X, torch.float32)
+    pkg.muon_orthogonalize(a)
+    pkg.muon_orthogonalize(b, handle=cuda_core_handle)
+    torch.cuda.synchronize()
+    assert pkg.default_handle().check() == 0 and cuda_core_handle.check() == 0
+    e_tc = record(f"fp32 tensor-core path {shape}", rel(host64(a), ref), TOL_F32)
+    e_cc = record(f"fp32 CUDA-core path {shape}", rel(host64(b), ref), TOL_F32)
+    assert e_tc < TOL_F32 and e_cc < TOL_F32
+
+
+def test_fp32_tensor_core_step_gpt2_layer_three_steps(pkg):
+    # one GPT-2-small layer in fp32 parameters and gradients, three steps on
+    # the tensor-core fp32 path; the oracle takes each step from the GPU's
+    # parameter, dW held to the fp32 bar
+    specs = wl.gpt2_small(layers=1).muon
+    per_step, moms = run_step_per_step(pkg, specs, torch.float32, steps=3)
+    for k, row in enumerate(per_step):
+        for i, (w_gpu, w_ref, base) in enumerate(row):
+            err = record(f"fp32 tensor-core step {k} {specs[i].name} dW", delta_err(w_gpu, w_ref, base), TOL_F32)
+            assert err < TOL_F32
+    for m_gpu, m_ref in moms:
+        assert rel(m_gpu, m_ref) < TOL_EXACT
