@@ -37,6 +37,7 @@ UNIT = "TFLOP/s"
 LR, WD, MU = 0.02, 0.1, 0.95
 NS_STEPS = 5
 E2E_SLICE_BYTES = 2 << 30      # parameters per muon_step call of the pipelined e2e loop
+F32_TC_MAX_M = int(os.environ.get("MUON_F32_TC_MAX_M", "1024"))   # the library's fp32 tensor-core rule
 
 
 def parse_args(argv=None):
@@ -462,7 +463,7 @@ def run_ours(args):
         if method == "gram" and not fp32:
             # tensor-core work: bf16x3 m x m products, two-plane final product
             row["mma_tflops"] = row["tflops"] * flops.kernel_mma_factor_gram()[k]
-        elif fp32 and method == "standard":
+        elif fp32 and method == "standard" and m <= F32_TC_MAX_M:
             # three-plane operands: six bf16 MMAs per product
             row["mma_tflops"] = row["tflops"] * 6.0
         group_rows.append(row)
@@ -483,8 +484,11 @@ def run_ours(args):
             except Exception:
                 traffic = None
         m_top = int(top["group"].split("x")[0])
-        kname = "ns_gemm_pair_kernel" if (not fp32 and uses_pairs(m_top, top["kernel"], method)) else (
-            "ns_gemm_tc_kernel" if not fp32 or method == "standard" else "ns_gemm_simt_kernel")
+        if fp32:
+            # the fp32 path's standard method runs on the tensor cores up to m = 1024
+            kname = "ns_gemm_tc_kernel" if (method == "standard" and m_top <= F32_TC_MAX_M) else "ns_gemm_simt_kernel"
+        else:
+            kname = "ns_gemm_pair_kernel" if uses_pairs(m_top, top["kernel"], method) else "ns_gemm_tc_kernel"
         roofline = {"bound": "tensor", "kernel": f"{kname}<{top['mode']}> on the {top['group']} group "
                                                   f"({top['matrices']} matrices)",
                     "achieved": top["tflops"], "peak": peak, "unit": "TFLOP/s", "frac": top["tflops"] / peak,

@@ -84,6 +84,14 @@ struct muon_handle_s {
   bool final_tma = true;        // FINAL into bf16 destinations through tensor maps (MUON_FINAL_TMA=0 disables)
   bool f32_tc = true;           // fp32 standard method on the tensor cores, three bf16 planes (MUON_F32_TC=0:
                                 // CUDA cores)
+  int f32_tc_max_m = 1024;      // ... for groups up to this m (MUON_F32_TC_MAX_M); the products' fp32
+                                // accumulation error grows with K = m (4096 x 4096: 1.5e-4 against the
+                                // 1e-4 bar, 1024 x 4096: 5.1e-5)
+  // standard bf16 method: the next unit's preparation on a side stream while
+  // the current unit's products run (MUON_OVERLAP=1)
+  bool overlap = false;
+  cudaStream_t side = nullptr;
+  std::vector<cudaEvent_t> ovl_ev;
 };
 
 namespace {
@@ -161,6 +169,25 @@ muon_status_t ensure_ws(muon_handle_t h, size_t bytes) {
     return fail(h, MUON_ERR_WORKSPACE, "workspace allocation of " + std::to_string(cap) + " bytes failed");
   }
   h->ws_cap = cap;
+  return MUON_OK;
+}
+
+// The side stream and at least n events of the overlapped standard path,
+// created on first use.
+muon_status_t ensure_overlap_events(muon_handle_t h, size_t n) {
+  if (h->side == nullptr && cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    h->side = nullptr;
+    return fail(h, MUON_ERR_CUDA, "side stream creation failed");
+  }
+  while (h->ovl_ev.size() < n) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, MUON_ERR_CUDA, "event creation failed");
+    }
+    h->ovl_ev.push_back(e);
+  }
   return MUON_OK;
 }
 
@@ -638,8 +665,13 @@ muon_status_t run_f32tc_group(muon_handle_t h, const GroupPlan& g, const Regions
 // Strides, tile widths and the chunk (matrices per launch) of one same-shape
 // group under the handle's workspace limit; returns the workspace bytes the
 // group's chunk needs.
-size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps) {
-  const bool f32tc = !tc && !gram && h->f32_tc;
+// The fp32 path's standard method runs on the tensor cores for this group.
+bool f32tc_group(muon_handle_t h, const GroupPlan& g, bool tc, bool gram) {
+  return !tc && !gram && h->f32_tc && g.m <= h->f32_tc_max_m;
+}
+
+size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps, size_t limit) {
+  const bool f32tc = f32tc_group(h, g, tc, gram);
   g.ldx = static_cast<long long>(align_up(g.n, 8));
   g.ldm = static_cast<long long>(align_up(g.m, 8));
   g.prep_tiles = static_cast<int>(ceil_div(g.m, 64) * ceil_div(g.n, 64));
@@ -649,7 +681,7 @@ size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps) 
   const size_t per2 = regions(g, 2, tc, gram, steps, f32tc).total;
   g.per_mat = per2 > per1 ? per2 - per1 : per1;
   const size_t fixed = per1 > g.per_mat ? per1 - g.per_mat : 0;
-  size_t fit = h->ws_limit > fixed ? (h->ws_limit - fixed) / std::max<size_t>(g.per_mat, 1) : 1;
+  size_t fit = limit > fixed ? (limit - fixed) / std::max<size_t>(g.per_mat, 1) : 1;
   fit = std::max<size_t>(fit, 1);
   fit = std::min<size_t>(fit, g.members.size());
   fit = std::min<size_t>(fit, 65535);
@@ -666,7 +698,9 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                          const float* coeffs, int coeff_stride, int ns_method, bool tc, cudaStream_t stream) {
   if (blocks.empty()) return MUON_OK;
   const bool gram = (ns_method == MUON_NS_GRAM);
-  const bool f32tc = !tc && !gram && h->f32_tc;
+  // unit preparation overlapped with the products (standard bf16 method):
+  // two workspace halves, each planned under half the limit
+  const bool overlap = h->overlap && tc && !gram && steps > 0;
 
   std::map<std::pair<int, int>, GroupPlan> groups;
   for (size_t i = 0; i < blocks.size(); ++i) {
@@ -680,8 +714,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   size_t ws_need = 0;
   for (auto& kv : groups) {
     GroupPlan& g = kv.second;
-    ws_need = std::max(ws_need, plan_group(h, g, tc, gram, steps));
-    if (f32tc) {
+    ws_need = std::max(ws_need, plan_group(h, g, tc, gram, steps, overlap ? h->ws_limit / 2 : h->ws_limit));
+    if (f32tc_group(h, g, tc, gram)) {
       std::vector<int2> t128 = sym_tiles(g.m, 128);
       g.tri128_count = static_cast<int>(t128.size());
       g.tri128_off = arena_push(arena, t128.data(), t128.size());
@@ -723,7 +757,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     }
   }
 
-  muon_status_t st = ensure_ws(h, ws_need);
+  const size_t half_bytes = align_up(ws_need, 256);
+  muon_status_t st = ensure_ws(h, overlap ? 2 * half_bytes : ws_need);
   if (st != MUON_OK) return st;
   void* dev = nullptr;
   st = upload(h, arena, stream, &dev);
@@ -731,188 +766,279 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   uint8_t* dbase = static_cast<uint8_t*>(dev);
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
 
-  int group_index = 0;
-  for (auto& kv : groups) {
-    GroupPlan& g = kv.second;
-    h->prof_tag = group_index++;
-    const Regions R = regions(g, g.chunk, tc, gram, steps, f32tc);
-    if (f32tc) {
-      muon_status_t fst = run_f32tc_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, mu, nesterov, stream);
-      if (fst != MUON_OK) return fst;
-      continue;
-    }
-    if (gram) {
-      muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, tc, mu, nesterov, stream);
-      if (gst != MUON_OK) return gst;
-      continue;
-    }
-    float* xf = reinterpret_cast<float*>(ws + R.xf);
-    float* xf2 = tc ? nullptr : reinterpret_cast<float*>(ws + R.xf2);
-    __nv_bfloat16* xb[2] = {tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb0) : nullptr,
-                            tc ? reinterpret_cast<__nv_bfloat16*>(ws + R.xb1) : nullptr};
-    void* symA = ws + R.symA;
-    void* symB = ws + R.symB;
-    float* pdiag = tc ? reinterpret_cast<float*>(ws + R.pdiag) : nullptr;
-    float* partials = reinterpret_cast<float*>(ws + R.partials);
-    float* scale = reinterpret_cast<float*>(ws + R.scale);
-
-    __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(ws + R.xlo) : nullptr;
+  // The standard method's workspace regions of one same-shape group at
+  // `base` (the workspace, or one of its halves when unit preparation
+  // overlaps the products), and the tensor maps over them.
+  struct StdSet {
+    float *xf, *xf2, *pdiag, *partials, *scale;
+    __nv_bfloat16 *xb[2], *xlo;
+    void *symA, *symB;
+    bool n128;
     CUtensorMap map_x[2], map_xmn[2], map_A, map_A64, map_B, map_xh[2], map_xl, map_sa, map_sb;
+  };
+  auto make_set = [&](const GroupPlan& g, uint8_t* base, StdSet& S) -> muon_status_t {
+    const Regions R = regions(g, g.chunk, tc, gram, steps, false);
     // pair symmetric products of a ragged m whose last 256-column block has
     // at most 128 valid columns: those tiles run N = 128 (64-row B boxes)
-    const bool n128 = tc && g.pair && g.m % 256 != 0 && g.m % 256 <= 128;
+    S.n128 = tc && g.pair && g.m % 256 != 0 && g.m % 256 <= 128;
+    S.xf = reinterpret_cast<float*>(base + R.xf);
+    S.xf2 = tc ? nullptr : reinterpret_cast<float*>(base + R.xf2);
+    S.xb[0] = tc ? reinterpret_cast<__nv_bfloat16*>(base + R.xb0) : nullptr;
+    S.xb[1] = tc ? reinterpret_cast<__nv_bfloat16*>(base + R.xb1) : nullptr;
+    S.symA = base + R.symA;
+    S.symB = base + R.symB;
+    S.pdiag = tc ? reinterpret_cast<float*>(base + R.pdiag) : nullptr;
+    S.partials = reinterpret_cast<float*>(base + R.partials);
+    S.scale = reinterpret_cast<float*>(base + R.scale);
+    S.xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(base + R.xlo) : nullptr;
     if (tc && steps > 0) {
-      if (!encode_map(h, &map_x[0], xb[0], g.n, g.m, g.chunk, g.ldx) ||
-          !encode_map(h, &map_x[1], xb[1], g.n, g.m, g.chunk, g.ldx) ||
-          !encode_map(h, &map_xmn[0], xb[0], g.n, g.m, g.chunk, g.ldx, 64) ||
-          !encode_map(h, &map_xmn[1], xb[1], g.n, g.m, g.chunk, g.ldx, 64) ||
-          !encode_map(h, &map_A, symA, g.m, g.m, g.chunk, g.ldm) ||
-          !encode_map(h, &map_A64, symA, g.m, g.m, g.chunk, g.ldm, 64) ||
-          !encode_map(h, &map_B, symB, g.m, g.m, g.chunk, g.ldm) ||
-          !encode_box32(h->encode, &map_xh[0], xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
-          !encode_box32(h->encode, &map_xh[1], xb[1], false, g.n, g.m, g.chunk, g.ldx) ||
-          !encode_box32(h->encode, &map_xl, xlo, false, g.n, g.m, g.chunk, g.ldx) ||
-          !encode_box32(h->encode, &map_sa, symA, false, g.m, g.m, g.chunk, g.ldm) ||
-          !encode_box32(h->encode, &map_sb, symB, false, g.m, g.m, g.chunk, g.ldm))
+      if (!encode_map(h, &S.map_x[0], S.xb[0], g.n, g.m, g.chunk, g.ldx) ||
+          !encode_map(h, &S.map_x[1], S.xb[1], g.n, g.m, g.chunk, g.ldx) ||
+          !encode_map(h, &S.map_xmn[0], S.xb[0], g.n, g.m, g.chunk, g.ldx, 64) ||
+          !encode_map(h, &S.map_xmn[1], S.xb[1], g.n, g.m, g.chunk, g.ldx, 64) ||
+          !encode_map(h, &S.map_A, S.symA, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_map(h, &S.map_A64, S.symA, g.m, g.m, g.chunk, g.ldm, 64) ||
+          !encode_map(h, &S.map_B, S.symB, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_box32(h->encode, &S.map_xh[0], S.xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_box32(h->encode, &S.map_xh[1], S.xb[1], false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_box32(h->encode, &S.map_xl, S.xlo, false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_box32(h->encode, &S.map_sa, S.symA, false, g.m, g.m, g.chunk, g.ldm) ||
+          !encode_box32(h->encode, &S.map_sb, S.symB, false, g.m, g.m, g.chunk, g.ldm))
         return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
+    return MUON_OK;
+  };
+  // chunk c: momentum, U, norm (and, with no NS step, the parameter write)
+  auto prep = [&](const GroupPlan& g, StdSet& S, size_t c, cudaStream_t stream) -> muon_status_t {
+    const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
+    const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
+    const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+    PrepParams pp{};
+    pp.src = src_d;
+    pp.mu = mu;
+    pp.nesterov = nesterov;
+    pp.m = g.m;
+    pp.ldx = g.ldx;
+    pp.xf = (tc && steps > 0) ? nullptr : S.xf;
+    pp.xb = S.xb[0];
+    pp.xlo = S.xlo;
+    pp.partials = S.partials;
+    pp.tiles_per_mat = g.prep_tiles;
+    MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");
+    MUON_LAUNCH(MUON_K_NORM, launch_norm_finalize(S.partials, g.prep_tiles, cnt, kNormEps, S.scale, h->err, stream),
+                "norm launch");
+
+    if (steps == 0) {
+      ApplyParams ap{out_d, S.scale, S.xf, g.ldx, g.m, g.n};
+      MUON_LAUNCH(MUON_K_APPLY, launch_apply(ap, cnt, stream), "apply launch");
+    }
+    return MUON_OK;
+  };
+  // chunk c: the NS products, the last one writing the destinations
+  auto products = [&](const GroupPlan& g, StdSet& S, size_t c, cudaStream_t stream) -> muon_status_t {
+    if (steps == 0) return MUON_OK;
     const int mi = static_cast<int>(ceil_div(g.m, 128));
     const int nj = static_cast<int>(ceil_div(g.n, g.bn_upd));
-
-    for (size_t c = 0; c < g.chunk_off.size(); ++c) {
-      const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
-      const SrcEntry* src_d = reinterpret_cast<const SrcEntry*>(dbase + g.chunk_off[c].first);
-      const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
-      const CUtensorMap* wmap_d =
-          g.chunk_wmap[c] == kNoMaps ? nullptr : reinterpret_cast<const CUtensorMap*>(dbase + g.chunk_wmap[c]);
-      // the last UPDATE writes the destinations: through their tensor maps
-      // when the chunk has them
-      const int final_mode = wmap_d != nullptr ? MODE_FINAL_T : MODE_FINAL;
-
-      PrepParams pp{};
-      pp.src = src_d;
-      pp.mu = mu;
-      pp.nesterov = nesterov;
-      pp.m = g.m;
-      pp.ldx = g.ldx;
-      pp.xf = (tc && steps > 0) ? nullptr : xf;
-      pp.xb = xb[0];
-      pp.xlo = xlo;
-      pp.partials = partials;
-      pp.tiles_per_mat = g.prep_tiles;
-      MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");
-      MUON_LAUNCH(MUON_K_NORM, launch_norm_finalize(partials, g.prep_tiles, cnt, kNormEps, scale, h->err, stream),
-                  "norm launch");
-
-      if (steps == 0) {
-        ApplyParams ap{out_d, scale, xf, g.ldx, g.m, g.n};
-        MUON_LAUNCH(MUON_K_APPLY, launch_apply(ap, cnt, stream), "apply launch");
-        continue;
-      }
-      for (int it = 0; it < steps; ++it) {
-        const bool last = (it == steps - 1);
-        NsGemmParams p{};
-        p.m = g.m;
-        p.n = g.n;
-        p.batch = cnt;
-        p.scale = it == 0 ? scale : nullptr;
-        p.ca = coeffs[it * coeff_stride];        // this iteration's (a, b, c)
-        p.cb = coeffs[it * coeff_stride + 1];
-        p.cc = coeffs[it * coeff_stride + 2];
-        p.ldm = g.ldm;
-        p.ldx = g.ldx;
-        p.out = out_d;
-        p.wmap = wmap_d;
-        p.err = h->err;
-        p.timeout_ns = h->timeout_ns;
-        p.pdiag = pdiag;
-        if (tc && g.pair) {
-          // SYRK, POLY and (pair_upd) UPDATE / FINAL on CTA pairs, 256 x 256
-          // tiles
-          NsGemmParams q = p;
-          q.tiles_per_mat = g.tri256_count;
-          q.num_tiles = cnt * g.tri256_count;
-          q.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
-          q.sym_out = symA;
-          const int pairs = std::min(q.num_tiles, h->max_pairs);
-          MUON_LAUNCH(MUON_K_SYRK,
-                      launch_ns_gemm_pair(MODE_SYRK, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, pairs, stream,
-                                          n128 ? &map_xmn[it & 1] : nullptr),
-                      "syrk launch");
-          q.scale = nullptr;
-          q.sym_in = symA;
-          q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY,
-                      launch_ns_gemm_pair(MODE_POLY, map_A, map_A, map_sb, map_sb, q, pairs, stream, n128 ? &map_A64 : nullptr),
-                      "poly launch");
-          NsGemmParams u = p;
-          if (g.pair_upd) {
-            const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
-            u.mi = mi2;
-            u.tiles_per_mat = mi2 * nj2;
-            u.num_tiles = cnt * mi2 * nj2;
-            const int upairs = std::min(u.num_tiles, h->max_pairs);
-            MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                        launch_ns_gemm_pair_update(last ? final_mode : MODE_UPDATE, map_B, map_xmn[it & 1],
-                                                   map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, upairs, stream,
-                                                   g.m <= kShortK ? 2 : 0),
-                        "update launch");
-          } else {
-            u.mi = mi;
-            u.tiles_per_mat = mi * nj;
-            u.num_tiles = cnt * mi * nj;
-            const int grid = std::min(u.num_tiles, h->num_sms);
-            MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                        launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
-                                                 map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
-                        "update launch");
-          }
-        } else if (tc) {
-          // SYRK: A = s^2 X X^T
-          NsGemmParams q = p;
-          q.tiles_per_mat = g.tri_count;
-          q.num_tiles = cnt * g.tri_count;
-          q.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
-          q.sym_out = symA;
-          int grid = std::min(q.num_tiles, h->num_sms);
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, grid,
-                                                         stream),
-                      "syrk launch");
-          // POLY: P = a I + b A + c A A
-          q.scale = nullptr;
-          q.sym_in = symA;
-          q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, map_A, map_A, map_sb, map_sb, q, grid, stream), "poly launch");
-          // UPDATE / FINAL: X = s (P^ X^ + P_rr X - P^_rr X^)
-          NsGemmParams u = p;
+    const int cnt = static_cast<int>(std::min<size_t>(g.chunk, g.members.size() - c * g.chunk));
+    const OutEntry* out_d = reinterpret_cast<const OutEntry*>(dbase + g.chunk_off[c].second);
+    const CUtensorMap* wmap_d =
+        g.chunk_wmap[c] == kNoMaps ? nullptr : reinterpret_cast<const CUtensorMap*>(dbase + g.chunk_wmap[c]);
+    // the last UPDATE writes the destinations: through their tensor maps
+    // when the chunk has them
+    const int final_mode = wmap_d != nullptr ? MODE_FINAL_T : MODE_FINAL;
+    for (int it = 0; it < steps; ++it) {
+      const bool last = (it == steps - 1);
+      NsGemmParams p{};
+      p.m = g.m;
+      p.n = g.n;
+      p.batch = cnt;
+      p.scale = it == 0 ? S.scale : nullptr;
+      p.ca = coeffs[it * coeff_stride];        // this iteration's (a, b, c)
+      p.cb = coeffs[it * coeff_stride + 1];
+      p.cc = coeffs[it * coeff_stride + 2];
+      p.ldm = g.ldm;
+      p.ldx = g.ldx;
+      p.out = out_d;
+      p.wmap = wmap_d;
+      p.err = h->err;
+      p.timeout_ns = h->timeout_ns;
+      p.pdiag = S.pdiag;
+      if (tc && g.pair) {
+        // SYRK, POLY and (pair_upd) UPDATE / FINAL on CTA pairs, 256 x 256
+        // tiles
+        NsGemmParams q = p;
+        q.tiles_per_mat = g.tri256_count;
+        q.num_tiles = cnt * g.tri256_count;
+        q.tri = reinterpret_cast<const int2*>(dbase + g.tri256_off);
+        q.sym_out = S.symA;
+        const int pairs = std::min(q.num_tiles, h->max_pairs);
+        MUON_LAUNCH(MUON_K_SYRK,
+                    launch_ns_gemm_pair(MODE_SYRK, S.map_x[it & 1], S.map_x[it & 1], S.map_sa, S.map_sa, q, pairs, stream,
+                                        S.n128 ? &S.map_xmn[it & 1] : nullptr),
+                    "syrk launch");
+        q.scale = nullptr;
+        q.sym_in = S.symA;
+        q.sym_out = S.symB;
+        MUON_LAUNCH(MUON_K_POLY,
+                    launch_ns_gemm_pair(MODE_POLY, S.map_A, S.map_A, S.map_sb, S.map_sb, q, pairs, stream, S.n128 ? &S.map_A64 : nullptr),
+                    "poly launch");
+        NsGemmParams u = p;
+        if (g.pair_upd) {
+          const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
+          u.mi = mi2;
+          u.tiles_per_mat = mi2 * nj2;
+          u.num_tiles = cnt * mi2 * nj2;
+          const int upairs = std::min(u.num_tiles, h->max_pairs);
+          MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                      launch_ns_gemm_pair_update(last ? final_mode : MODE_UPDATE, S.map_B, S.map_xmn[it & 1],
+                                                 S.map_xh[it & 1], S.map_xl, S.map_xh[(it + 1) & 1], u, upairs, stream,
+                                                 g.m <= kShortK ? 2 : 0),
+                      "update launch");
+        } else {
           u.mi = mi;
           u.tiles_per_mat = mi * nj;
           u.num_tiles = cnt * mi * nj;
-          grid = std::min(u.num_tiles, h->num_sms);
+          const int grid = std::min(u.num_tiles, h->num_sms);
           MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
-                      launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, map_B, map_xmn[it & 1],
-                                               map_xh[it & 1], map_xl, map_xh[(it + 1) & 1], u, grid, stream),
-                      "update launch");
-        } else {
-          float* xin = (it & 1) ? xf2 : xf;
-          float* xout = (it & 1) ? xf : xf2;
-          NsGemmParams q = p;
-          q.xf_in = xin;
-          q.sym_out = symA;
-          MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_SYRK, q, stream), "syrk launch");
-          q.scale = nullptr;
-          q.sym_in = symA;
-          q.sym_out = symB;
-          MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_simt(MODE_POLY, q, stream), "poly launch");
-          NsGemmParams u = p;
-          u.sym_in = symB;
-          u.xf_in = xin;
-          u.xf_out = xout;
-          MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE, launch_ns_gemm_simt(last ? MODE_FINAL : MODE_UPDATE, u, stream),
+                      launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, S.map_B, S.map_xmn[it & 1],
+                                               S.map_xh[it & 1], S.map_xl, S.map_xh[(it + 1) & 1], u, grid, stream),
                       "update launch");
         }
+      } else if (tc) {
+        // SYRK: A = s^2 X X^T
+        NsGemmParams q = p;
+        q.tiles_per_mat = g.tri_count;
+        q.num_tiles = cnt * g.tri_count;
+        q.tri = reinterpret_cast<const int2*>(dbase + g.tri_off);
+        q.sym_out = S.symA;
+        int grid = std::min(q.num_tiles, h->num_sms);
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, S.map_x[it & 1], S.map_x[it & 1], S.map_sa, S.map_sa, q, grid,
+                                                       stream),
+                    "syrk launch");
+        // POLY: P = a I + b A + c A A
+        q.scale = nullptr;
+        q.sym_in = S.symA;
+        q.sym_out = S.symB;
+        MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, S.map_A, S.map_A, S.map_sb, S.map_sb, q, grid, stream), "poly launch");
+        // UPDATE / FINAL: X = s (P^ X^ + P_rr X - P^_rr X^)
+        NsGemmParams u = p;
+        u.mi = mi;
+        u.tiles_per_mat = mi * nj;
+        u.num_tiles = cnt * mi * nj;
+        grid = std::min(u.num_tiles, h->num_sms);
+        MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE,
+                    launch_ns_gemm_tc_update(last ? final_mode : MODE_UPDATE, g.bn_upd, S.map_B, S.map_xmn[it & 1],
+                                             S.map_xh[it & 1], S.map_xl, S.map_xh[(it + 1) & 1], u, grid, stream),
+                    "update launch");
+      } else {
+        float* xin = (it & 1) ? S.xf2 : S.xf;
+        float* xout = (it & 1) ? S.xf : S.xf2;
+        NsGemmParams q = p;
+        q.xf_in = xin;
+        q.sym_out = S.symA;
+        MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_simt(MODE_SYRK, q, stream), "syrk launch");
+        q.scale = nullptr;
+        q.sym_in = S.symA;
+        q.sym_out = S.symB;
+        MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_simt(MODE_POLY, q, stream), "poly launch");
+        NsGemmParams u = p;
+        u.sym_in = S.symB;
+        u.xf_in = xin;
+        u.xf_out = xout;
+        MUON_LAUNCH(last ? MUON_K_FINAL : MUON_K_UPDATE, launch_ns_gemm_simt(last ? MODE_FINAL : MODE_UPDATE, u, stream),
+                    "update launch");
       }
     }
+    return MUON_OK;
+  };
+
+  std::vector<GroupPlan*> order;              // ascending (m, n)
+  for (auto& kv : groups) order.push_back(&kv.second);
+  if (!overlap) {
+    for (size_t gi = 0; gi < order.size(); ++gi) {
+      GroupPlan& g = *order[gi];
+      h->prof_tag = static_cast<int>(gi);
+      const bool f32tc = f32tc_group(h, g, tc, gram);
+      const Regions R = regions(g, g.chunk, tc, gram, steps, f32tc);
+      if (f32tc) {
+        muon_status_t fst = run_f32tc_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, mu, nesterov, stream);
+        if (fst != MUON_OK) return fst;
+        continue;
+      }
+      if (gram) {
+        muon_status_t gst = run_gram_group(h, g, R, ws, dbase, steps, coeffs, coeff_stride, tc, mu, nesterov, stream);
+        if (gst != MUON_OK) return gst;
+        continue;
+      }
+      StdSet S;
+      muon_status_t sst = make_set(g, ws, S);
+      if (sst != MUON_OK) return sst;
+      for (size_t c = 0; c < g.chunk_off.size(); ++c) {
+        sst = prep(g, S, c, stream);
+        if (sst != MUON_OK) return sst;
+        sst = products(g, S, c, stream);
+        if (sst != MUON_OK) return sst;
+      }
+    }
+    return MUON_OK;
+  }
+
+  // Overlapped: units (group, chunk) in launch order use the two workspace
+  // halves in turn; unit u+1's preparation (an HBM-bound pass) runs on the
+  // handle's side stream while unit u's products run on the caller's stream.
+  // Events order it: the side stream starts after everything enqueued
+  // before this call, prepares unit u+1 once unit u-1 (the last user of that
+  // half) has finished, and the caller's stream waits for a unit's
+  // preparation before its products, so every side-stream launch is joined
+  // before the call's last products.
+  struct Unit {
+    int group;
+    size_t chunk;
+  };
+  std::vector<Unit> units;
+  for (size_t gi = 0; gi < order.size(); ++gi)
+    for (size_t c = 0; c < order[gi]->chunk_off.size(); ++c) units.push_back(Unit{static_cast<int>(gi), c});
+  std::vector<StdSet> sets(2 * order.size());
+  std::vector<char> made(2 * order.size(), 0);
+  auto set_of = [&](const Unit& u, int half, StdSet** out) -> muon_status_t {
+    const size_t k = 2 * static_cast<size_t>(u.group) + static_cast<size_t>(half);
+    if (!made[k]) {
+      muon_status_t r = make_set(*order[u.group], ws + static_cast<size_t>(half) * half_bytes, sets[k]);
+      if (r != MUON_OK) return r;
+      made[k] = 1;
+    }
+    *out = &sets[k];
+    return MUON_OK;
+  };
+  muon_status_t ost = ensure_overlap_events(h, 2 * units.size() + 1);
+  if (ost != MUON_OK) return ost;
+  cudaEvent_t ev_start = h->ovl_ev[0];
+  auto ev_ready = [&](size_t u) { return h->ovl_ev[1 + 2 * u]; };
+  auto ev_freed = [&](size_t u) { return h->ovl_ev[2 + 2 * u]; };
+  MUON_CUDA_TRY(cudaEventRecord(ev_start, stream), "overlap start event");
+  MUON_CUDA_TRY(cudaStreamWaitEvent(h->side, ev_start, 0), "side stream wait");
+  {
+    StdSet* S0 = nullptr;
+    if ((ost = set_of(units[0], 0, &S0)) != MUON_OK) return ost;
+    h->prof_tag = units[0].group;
+    if ((ost = prep(*order[units[0].group], *S0, units[0].chunk, stream)) != MUON_OK) return ost;
+  }
+  for (size_t u = 0; u < units.size(); ++u) {
+    if (u + 1 < units.size()) {
+      const Unit& nx = units[u + 1];
+      StdSet* Sn = nullptr;
+      if ((ost = set_of(nx, static_cast<int>((u + 1) & 1), &Sn)) != MUON_OK) return ost;
+      if (u >= 1) MUON_CUDA_TRY(cudaStreamWaitEvent(h->side, ev_freed(u - 1), 0), "side stream wait");
+      h->prof_tag = nx.group;
+      if ((ost = prep(*order[nx.group], *Sn, nx.chunk, h->side)) != MUON_OK) return ost;
+      MUON_CUDA_TRY(cudaEventRecord(ev_ready(u + 1), h->side), "overlap ready event");
+    }
+    if (u >= 1) MUON_CUDA_TRY(cudaStreamWaitEvent(stream, ev_ready(u), 0), "stream wait");
+    StdSet* S = nullptr;
+    if ((ost = set_of(units[u], static_cast<int>(u & 1), &S)) != MUON_OK) return ost;
+    h->prof_tag = units[u].group;
+    if ((ost = products(*order[units[u].group], *S, units[u].chunk, stream)) != MUON_OK) return ost;
+    MUON_CUDA_TRY(cudaEventRecord(ev_freed(u), stream), "overlap freed event");
   }
   return MUON_OK;
 }
@@ -1021,6 +1147,11 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
   h->max_pairs = h->use_pair ? ns_gemm_pair_max_pairs() : 0;
   if (const char* ft = std::getenv("MUON_FINAL_TMA")) h->final_tma = ft[0] != '0';
   if (const char* ft = std::getenv("MUON_F32_TC")) h->f32_tc = ft[0] != '0';
+  if (const char* fm = std::getenv("MUON_F32_TC_MAX_M")) {
+    const long v = std::strtol(fm, nullptr, 10);
+    if (v >= 1 && v <= (1L << 30)) h->f32_tc_max_m = static_cast<int>(v);
+  }
+  if (const char* ov = std::getenv("MUON_OVERLAP")) h->overlap = ov[0] == '1';
   bool ok = cudaMalloc(&h->err, sizeof(unsigned)) == cudaSuccess && cudaMemset(h->err, 0, sizeof(unsigned)) == cudaSuccess;
   for (int k = 0; ok && k < muon_handle_s::kStages; ++k)
     ok = cudaEventCreateWithFlags(&h->stage_ev[k], cudaEventDisableTiming) == cudaSuccess;
@@ -1047,6 +1178,8 @@ muon_status_t muon_handle_destroy(muon_handle_t h) {
     if (h->stage_ev[k]) cudaEventDestroy(h->stage_ev[k]);
   }
   if (h->err) cudaFree(h->err);
+  for (cudaEvent_t e : h->ovl_ev) cudaEventDestroy(e);
+  if (h->side) cudaStreamDestroy(h->side);
   for (auto& r : h->prof) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -1132,10 +1265,12 @@ muon_status_t muon_workspace_size(muon_handle_t h, const muon_param_t* params, i
     g.n = blocks[i].n;
     g.members.push_back(static_cast<int>(i));
   }
+  const bool tc = ns_dtype == MUON_BF16, gram = ns_method == MUON_NS_GRAM;
+  const bool overlap = h->overlap && tc && !gram && ns_steps > 0;
   size_t need = 0;
   for (auto& kv : groups)
-    need = std::max(need, plan_group(h, kv.second, ns_dtype == MUON_BF16, ns_method == MUON_NS_GRAM, ns_steps));
-  *bytes = need;
+    need = std::max(need, plan_group(h, kv.second, tc, gram, ns_steps, overlap ? h->ws_limit / 2 : h->ws_limit));
+  *bytes = (overlap && need > 0) ? 2 * align_up(need, 256) : need;
   return MUON_OK;
 }
 

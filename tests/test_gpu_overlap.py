@@ -1,0 +1,55 @@
+"""The overlapped schedule (MUON_OVERLAP=1): each unit's preparation
+(momentum, Nesterov, norm partials, bf16 planes) runs on the handle's side
+stream while the previous unit's products run, the two units using the two
+halves of the workspace.  The arithmetic is the serial schedule's, so the
+parameters and momenta must agree with a default handle bit for bit; the
+cases force several chunks per group (a small workspace limit) and several
+groups, and run two steps so that a unit's half is reused."""
+import os
+
+import pytest
+import torch
+
+from newton_schulz_orthogonalized_muon_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _handle(pkg, **env):
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
+    try:
+        return pkg.MuonHandle(0)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                del os.environ[k]
+            else:
+                os.environ[k] = v
+
+
+@pytest.mark.parametrize("limit_mb", [8, 64, 4096])
+def test_overlapped_schedule_matches_serial_bitwise(limit_mb):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    torch.cuda.set_device(0)
+    serial, ovl = pkg.MuonHandle(0), _handle(pkg, MUON_OVERLAP="1")
+    specs = [wl.ParamSpec("a", (512, 1536)), wl.ParamSpec("b", (1536, 512)), wl.ParamSpec("c", (256, 768)),
+             wl.ParamSpec("d", (1408, 2048)), wl.ParamSpec("q", (512, 512), split_heads=4),
+             wl.ParamSpec("e", (512, 1536)), wl.ParamSpec("f", (96, 200))]
+    W0 = [torch.tensor(wl.weight(600 + i, s.shape)).to(torch.bfloat16) for i, s in enumerate(specs)]
+    G = [[torch.tensor(wl.lowrank_grad(700 + 10 * k + i, s.shape[0], s.shape[1], 32)).to(torch.bfloat16).cuda()
+          for i, s in enumerate(specs)] for k in range(2)]
+    outs = []
+    for h in (serial, ovl):
+        h.set_workspace_limit(limit_mb << 20)
+        W = [w.clone().cuda() for w in W0]
+        M = [torch.zeros(s.shape, device="cuda") for s in specs]
+        for k in range(2):
+            pkg.muon_step(W, G[k], M, lr=0.02, wd=0.1, split_heads=[s.split_heads for s in specs], handle=h)
+        torch.cuda.synchronize()
+        assert h.check() == 0
+        outs.append(([w.cpu() for w in W], [m.cpu() for m in M]))
+    for a, b in zip(outs[0][0] + outs[0][1], outs[1][0] + outs[1][1]):
+        assert torch.equal(a, b)
