@@ -13,6 +13,12 @@ Prints one JSON line.  `value` is the Newton-Schulz throughput in TFLOP/s
 copies of the set are dealt to the ranks by size-sorted ping-pong ownership
 (weak scaling, no collective inside the step).
 
+After the headline's timed regions, the default run also times the other
+configurations compactly and reports them under "other_configs" (one GPU,
+--workload llama3-8b only; --no-other-configs skips them): the Gram method
+on the same Llama inputs, GPT-2-small in bf16 and in fp32, the single fp32
+256x512 matrix, and the Moonlight-like MoE set, each with its own clocks.
+
 --impl reference times the fp64 CPU oracle (the reference arm) on a bounded
 sample of the same workload.
 """
@@ -59,6 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the compact timing of the other configurations after the headline")
     ap.add_argument("--cpu-baseline-plan", action="store_true",
                     help="time the fp64 oracle over all five configurations on the host cores and exit")
     return ap.parse_args(argv)
@@ -519,6 +527,17 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(specs, method)
 
+    # ---- the other configurations, after the headline's timed regions (one
+    # GPU, default workload only): the Gram method on the same inputs, then
+    # the small sets and the MoE set on fresh inputs
+    others = None
+    if world == 1 and not args.no_other_configs and args.workload == "llama3-8b" and args.layers is None \
+            and method == "standard" and not fp32:
+        others = {"llama3-8b gram": time_config(h, W, G, M, specs, "gram", args, peaks)}
+        del W, G, M
+        torch.cuda.empty_cache()
+        others.update(other_configs(args, h, dev, peaks))
+
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -538,11 +557,88 @@ def run_ours(args):
                "ns_tflops_standard_equivalent": alg_std_all / (ms_max / 1e3) / 1e12,
                "ns_frac_of_peak": value / peak, "roofline": roofline, "roofline_hbm": hbm,
                "kernels": kernel_rows, "kernel_groups": group_rows, "gpu_launches": launches, "clocks": clk, "e2e": e2e, "adamw": adamw,
-               "cpu_baseline": cpu}
+               "cpu_baseline": cpu, "other_configs": others}
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def time_config(h, W, G, M, specs, method, args, peaks, steps=3, warmup=3):
+    """Compact timing of one configuration on given device tensors: warm-up,
+    then `steps` steps bracketed by CUDA events (no per-launch events), then
+    the same number of steps with per-launch events for the per-class rates.
+    Returns step ms, the method's algorithmic NS TFLOP/s, its fraction of the
+    measured sustained peak, per-class ms and TFLOP/s, and the clocks."""
+    import torch
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+    split = [s_.split_heads for s_ in specs]
+    fp32 = W[0].dtype == torch.float32
+
+    def step():
+        pkg.muon_step(W, G, M, lr=LR, wd=WD, mu=MU, nesterov=True, ns_method=method, ns_steps=NS_STEPS,
+                      split_heads=split, handle=h)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h.set_profiling(True)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    prof = h.profile()
+    h.set_profiling(False)
+    clk = clocks.stop()
+    if h.check() != 0:
+        raise RuntimeError(f"device error while timing the {method} configuration")
+    alg, _ = flops.set_flops(specs, NS_STEPS, method)
+    classes = {}
+    per_class = {k: 0.0 for k in ("syrk", "poly", "update", "final")}
+    it = flops.kernel_launches(method, NS_STEPS)
+    for s_ in specs:
+        m, n = flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads)
+        kf = flops.kernel_flops(method, m, n)
+        for k in per_class:
+            per_class[k] += s_.split_heads * it[k] * kf[k]
+    for k, (kms, cnt) in prof.items():
+        if cnt:
+            row = {"ms_per_step": kms / steps}
+            if k in per_class and kms > 0:
+                row["tflops"] = per_class[k] / (kms / steps / 1e3) / 1e12
+            classes[k] = row
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    value = alg / (ms / 1e3) / 1e12
+    return {"ms_per_step": ms, "value": value, "unit": UNIT, "ns_frac_of_sustained_peak": value / peak,
+            "ns_method": method, "dtype": "f32" if fp32 else "bf16", "steps": steps, "warmup": warmup,
+            "kernels": classes, "clocks": clk}
+
+
+def other_configs(args, h, dev, peaks):
+    """The small sets (GPT-2-small in bf16 and fp32, the single fp32 256x512
+    matrix) and the Moonlight-like MoE set, each on fresh seeded inputs,
+    timed compactly after the headline."""
+    import torch
+    out = {}
+    for name, wname, dtype in (("gpt2-small", "gpt2-small", torch.bfloat16),
+                               ("gpt2-small fp32", "gpt2-small", torch.float32),
+                               ("single fp32 256x512", "single-fp32", torch.float32),
+                               ("moonlight-moe", "moonlight-moe", torch.bfloat16)):
+        ws = weight_set(wname)
+        specs = list(ws.muon)
+        W, G, M = make_inputs(specs, dev, args.seed, dtype=dtype, rank=ws.grad_rank)
+        out[name] = time_config(h, W, G, M, specs, "standard", args, peaks, steps=3 if wname == "moonlight-moe" else 10)
+        del W, G, M
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_adamw(args, ws, dev, stream, h, peaks):
