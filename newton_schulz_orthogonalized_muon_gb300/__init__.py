@@ -13,10 +13,16 @@ _BINDING_NAMES = ("MuonHandle", "MuonError", "muon_orthogonalize", "muon_orthogo
                   "QUINTIC", "EXPORTS")
 
 
+_OPTIM_NAMES = ("Muon", "split_params", "takes_muon")
+
+
 def __getattr__(name):
     if name in _BINDING_NAMES:
         from . import _binding
         return getattr(_binding, name)
+    if name in _OPTIM_NAMES:
+        from . import optim
+        return getattr(optim, name)
     raise AttributeError(name)
 
 
