@@ -83,7 +83,7 @@ struct Cfg {
   // shared memory: [stages][epilogue buffers][barriers], + 1024 alignment slack
   static constexpr int STAGES_FIT = (MAX_DYN_SMEM - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT < 8 ? STAGES_FIT : 8;
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int TMEM_COLS = 2 * BN * AccParts<MODE>::v;   // two tiles in flight, each of AccParts parts
   static constexpr size_t SMEM = static_cast<size_t>(STAGES) * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
   static_assert(STAGES >= 2, "pipeline needs two stages");
   static_assert(SMEM <= MAX_DYN_SMEM, "shared memory");
@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+        constexpr int kParts = AccParts<MODE>::v;
+        const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * BN * kParts);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_bounded(&full[s], ph, abort, p.timeout_ns)) {
             raise_timeout(abort, p.err);
@@ -228,12 +229,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + s * C::STAGE_BYTES);
           const uint32_t sb = sa + AP * C::A_BYTES;
+          // with two accumulator parts, even K steps go to the first, odd to the second
+          const uint32_t d = dt + static_cast<uint32_t>((kParts == 2 && (kb & 1)) ? BN : 0);
+          const int kfirst = kParts == 2 ? (kb >> 1) : kb;   // 0: the part's first K step
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t a0 = sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint32_t boff = kUpd ? kk * 2048 : kk * 32;
             const uint64_t b0 = kUpd ? sdesc_sw128(sb + boff, BOX_BYTES, 1024) : sdesc_sw128(sb + boff, 16, 1024);
-            umma_bf16(d, a0, b0, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d, a0, b0, idesc, (kfirst | kk) != 0 ? 1u : 0u);
             // plane q of A / B in this stage
             auto adesc = [&](int q) { return sdesc_sw128(sa + q * C::A_BYTES + kk * 32, 16, 1024); };
             auto bdesc = [&](int q) {

@@ -51,6 +51,31 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
   }
 }
 
+// The fp32 tensor-core modes accumulate the even and the odd K steps of a
+// tile in two TMEM accumulators, BN columns apart, and the epilogue adds
+// them in fp32: the tensor core's fp32 accumulation loses accuracy along K
+// (the fp32 path's error grew with K = m), and each half accumulates half
+// the steps.  Every other mode keeps one accumulator per tile.
+template <int MODE>
+struct AccParts {
+  static constexpr int v = ModeTraits<MODE>::kF32 ? 2 : 1;
+};
+
+// 16 columns of a tile's accumulator at `taddr`: the sum of its parts
+// (`two`: the K loop had at least two steps, so the second part was written).
+template <int MODE, int BN>
+__device__ __forceinline__ void acc_ld16(uint32_t taddr, float* v, bool two) {
+  tmem_ld16(taddr, v);
+  if constexpr (AccParts<MODE>::v == 2) {
+    if (two) {
+      float w[16];
+      tmem_ld16(taddr + static_cast<uint32_t>(BN), w);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] += w[e];
+    }
+  }
+}
+
 __device__ __forceinline__ void raise_timeout(volatile int* abort, unsigned* err) {
   *abort = 1;
   atomicOr(err, ERRBIT_TIMEOUT);
@@ -256,6 +281,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
   const int quad = warp & 3;
   const int cbeg = ((warp - 2) >> 2) * (BN / 2);
   const uint32_t wsm = smem_u32(wbuf);
+  const bool two_parts = ((ModeTraits<MODE>::kKn ? p.n : p.m) + BK - 1) / BK >= 2;
 
   // ---- input prefetch, in this warp's block order, at most SLOTS blocks ahead
   int pf_t = et.t0, pf_blk = 0;
@@ -338,7 +364,8 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
     }
     OutEntry oe{};
     if (MODE != MODE_UPDATE && MODE != MODE_F_UPDATE) oe = p.out[b];
-    const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + cbeg);
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                        static_cast<uint32_t>(acc * BN * AccParts<MODE>::v + cbeg);
     const int g0 = j * BN + cbeg;
     const int nb = g0 >= p.n ? 0 : min(NB, (p.n - g0 + 31) >> 5);
 #pragma unroll 1
@@ -355,7 +382,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
 #pragma unroll
         for (int h = 0; h < 32; h += 16) {
           float v[16];
-          tmem_ld16(tb + static_cast<uint32_t>(32 * k + h), v);
+          acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k + h), v, two_parts);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint4* ph = reinterpret_cast<uint4*>(sbuf + sw64_off(lane, (h >> 3) + q));
@@ -394,8 +421,8 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         // X' = s * acc as three bf16 planes p0 + p1 + p2, stored by TMA:
         // p0 and p1 through the slot's two halves, then p2 through the first
         float v[32];
-        tmem_ld16(tb + static_cast<uint32_t>(32 * k), v);
-        tmem_ld16(tb + static_cast<uint32_t>(32 * k + 16), v + 16);
+        acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k), v, two_parts);
+        acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k + 16), v + 16, two_parts);
         uint32_t w0[16], w1[16], w2[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -461,7 +488,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
 #pragma unroll
         for (int h = 0; h < 32; h += 16) {
           float v[16];
-          tmem_ld16(tb + static_cast<uint32_t>(32 * k + h), v);
+          acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k + h), v, two_parts);
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = s * (v[e] + corr[h + e]);
           if (tr) {
@@ -523,7 +550,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
 #pragma unroll
         for (int h = 0; h < 32; h += 16) {
           float v[16];
-          tmem_ld16(tb + static_cast<uint32_t>(32 * k + h), v);
+          acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k + h), v, two_parts);
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = s * (v[e] + corr[h + e]);
           if (tr) {
@@ -639,6 +666,7 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
   const int quad = warp & 3;
   const int cbeg = ((warp - 2) >> 2) * (BN / 2);
   const int m = p.m;
+  const bool two_parts = ((ModeTraits<MODE>::kKn ? p.n : p.m) + BK - 1) / BK >= 2;
   const uint32_t out_s = smem_u32(wbuf), mir_s = out_s + 2048;
   bool pending = false;                                // a bulk store may still read the buffers
   int acc = 0;
@@ -679,14 +707,15 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
       s = p.scale[b];
       s = s * s;                                       // SYRK / G_R0 of the first iteration: s^2 X X^T
     }
-    const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN + cbeg);
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                        static_cast<uint32_t>(acc * BN * AccParts<MODE>::v + cbeg);
 #pragma unroll 1
     for (int k = k0; k < NB; ++k) {
       const int gcb = g0 + 32 * k;
       if (gcb >= m) break;
       float v[32];
-      tmem_ld16(tb + static_cast<uint32_t>(32 * k), v);
-      tmem_ld16(tb + static_cast<uint32_t>(32 * k + 16), v + 16);
+      acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k), v, two_parts);
+      acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k + 16), v + 16, two_parts);
       const bool diag = (gcb == row0);
       if (MODE == MODE_SYRK || MODE == MODE_G_R0 || MODE == MODE_F_SYRK) {
 #pragma unroll
