@@ -43,6 +43,7 @@ UNIT = "TFLOP/s"
 LR, WD, MU = 0.02, 0.1, 0.95
 NS_STEPS = 5
 E2E_SLICE_BYTES = 2 << 30      # parameters per muon_step call of the pipelined e2e loop
+E2E_LAST_SLICE_BYTES = 256 << 20   # ... and in its last call, whose read-back is not overlapped
 F32_TC_MAX_M = int(os.environ.get("MUON_F32_TC_MAX_M", "1024"))   # the library's fp32 tensor-core rule
 
 
@@ -675,27 +676,44 @@ def run_adamw(args, ws, dev, stream, h, peaks):
     return out
 
 
-def e2e_slices(specs, param_bytes, limit=None):
+def e2e_slices(specs, param_bytes, limit=None, last_limit=None):
     """The muon_step calls of one pipelined e2e step: parameter indices grouped
     by the library's same-shape groups (NS dims after the transpose and
     Muon-Split rules, in ascending (m, n) order, the library's own order),
     each group cut into consecutive slices of at most `limit` bytes of
-    parameters (at least one matrix per slice)."""
+    parameters (at least one matrix per slice).  The step's read-back of the
+    last slice is the one copy not overlapped with compute, so the last
+    group ends with a slice of at most `last_limit` bytes."""
     from newton_schulz_orthogonalized_muon_gb300 import flops
     limit = E2E_SLICE_BYTES if limit is None else limit
+    last_limit = E2E_LAST_SLICE_BYTES if last_limit is None else last_limit
     by_group = {}
     for i, s_ in enumerate(specs):
         by_group.setdefault(flops.ns_dims(s_.shape[0], s_.shape[1], s_.split_heads), []).append(i)
     order = []
-    for key in sorted(by_group):
+    keys = sorted(by_group)
+    for key in keys:
+        members = by_group[key]
+        tail = []
+        if key == keys[-1] and sum(param_bytes[i] for i in members) > last_limit:
+            # the final slice: matrices from the group's end, up to last_limit bytes (at least one)
+            nbytes = 0
+            while members and (not tail or nbytes + param_bytes[members[-1]] <= last_limit) \
+                    and len(tail) < len(by_group[key]) - 1:
+                nbytes += param_bytes[members[-1]]
+                tail.insert(0, members[-1])
+                members = members[:-1]
         cur, nbytes = [], 0
-        for i in by_group[key]:
+        for i in members:
             if cur and nbytes + param_bytes[i] > limit:
                 order.append(cur)
                 cur, nbytes = [], 0
             cur.append(i)
             nbytes += param_bytes[i]
-        order.append(cur)
+        if cur:
+            order.append(cur)
+        if tail:
+            order.append(tail)
     return order
 
 

@@ -84,3 +84,17 @@ def test_gram_flops_are_below_standard_only_for_wide_matrices():
     # n / m is large enough
     assert flops.ns_flops("gram", 256, 16384) < 0.3 * flops.ns_flops("standard", 256, 16384)
     assert flops.ns_flops("gram", 4096, 4096) > flops.ns_flops("standard", 4096, 4096)
+
+
+def test_e2e_last_slice_is_small():
+    # the step's last read-back is not overlapped: the last group ends with a
+    # slice of at most E2E_LAST_SLICE_BYTES (two 117 MB Llama matrices)
+    specs = bench.weight_set("llama3-8b", None).muon
+    nb = _bytes(specs)
+    order = bench.e2e_slices(specs, nb)
+    assert sum(nb[i] for i in order[-1]) <= bench.E2E_LAST_SLICE_BYTES
+    assert len(order[-1]) >= 1
+    assert sorted(i for sl in order for i in sl) == list(range(len(specs)))
+    # a last group smaller than the limit is not cut
+    small = [wl.ParamSpec(f"p{i}", (64, 128)) for i in range(10)]
+    assert bench.e2e_slices(small, _bytes(small)) == [list(range(10))]
