@@ -44,7 +44,7 @@ LR, WD, MU = 0.02, 0.1, 0.95
 NS_STEPS = 5
 E2E_SLICE_BYTES = 2 << 30      # parameters per muon_step call of the pipelined e2e loop
 E2E_LAST_SLICE_BYTES = 256 << 20   # ... and in its last call, whose read-back is not overlapped
-F32_TC_MAX_M = int(os.environ.get("MUON_F32_TC_MAX_M", "1024"))   # the library's fp32 tensor-core rule
+F32_TC_MAX_M = int(os.environ.get("MUON_F32_TC_MAX_M", "2048"))   # the library's fp32 tensor-core rule
 
 
 def parse_args(argv=None):
@@ -494,7 +494,7 @@ def run_ours(args):
                 traffic = None
         m_top = int(top["group"].split("x")[0])
         if fp32:
-            # the fp32 path's standard method runs on the tensor cores up to m = 1024
+            # the fp32 path's standard method runs on the tensor cores up to m = 2048
             kname = "ns_gemm_tc_kernel" if (method == "standard" and m_top <= F32_TC_MAX_M) else "ns_gemm_simt_kernel"
         else:
             kname = "ns_gemm_pair_kernel" if uses_pairs(m_top, top["kernel"], method) else "ns_gemm_tc_kernel"

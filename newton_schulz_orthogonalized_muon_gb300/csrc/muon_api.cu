@@ -84,9 +84,10 @@ struct muon_handle_s {
   bool final_tma = true;        // FINAL into bf16 destinations through tensor maps (MUON_FINAL_TMA=0 disables)
   bool f32_tc = true;           // fp32 standard method on the tensor cores, three bf16 planes (MUON_F32_TC=0:
                                 // CUDA cores)
-  int f32_tc_max_m = 1024;      // ... for groups up to this m (MUON_F32_TC_MAX_M); the products' fp32
-                                // accumulation error grows with K = m (4096 x 4096: 1.5e-4 against the
-                                // 1e-4 bar, 1024 x 4096: 5.1e-5)
+  int f32_tc_max_m = 2048;      // ... for groups up to this m (MUON_F32_TC_MAX_M); the products' fp32
+                                // accumulation error grows with K = m (with two accumulators per tile:
+                                // 2048 x 8192 5.7e-5, 4096 x 4096 7.5e-5, 4096 x 14336 1.0e-4 against
+                                // the 1e-4 bar)
   // standard bf16 method: the next unit's preparation on a side stream while
   // the current unit's products run (MUON_OVERLAP=1)
   bool overlap = false;

@@ -592,11 +592,12 @@ def test_fp32_tensor_core_step_gpt2_layer_three_steps(pkg):
         assert rel(m_gpu, m_ref) < TOL_EXACT
 
 
-@pytest.mark.parametrize("shape", [(2048, 8192), (4096, 4096)])
+@pytest.mark.parametrize("shape", [(2048, 8192), (2048, 2048), (4096, 4096)])
 def test_fp32_large_m_runs_within_the_bar(pkg, shape):
-    # above m = 1024 the fp32 path's products stay on the CUDA cores: the
-    # three-plane tensor-core products' fp32 accumulation error grows with
-    # K = m (1.5e-4 at 4096 x 4096), the CUDA cores' does not
+    # up to m = 2048 the fp32 path runs on the tensor cores (three-plane
+    # products, two accumulators per tile); above, the products' fp32
+    # accumulation error, which grows with K = m, would near the bar
+    # (7.5e-5 at 4096 x 4096) and they stay on the CUDA cores
     X = wl.lowrank_grad(18, shape[0], shape[1], 64)
     t = to_dev(X, torch.float32)
     pkg.muon_orthogonalize(t)
