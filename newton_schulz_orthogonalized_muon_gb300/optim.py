@@ -103,9 +103,19 @@ class Muon:
         self.exp_avg_sq = [torch.zeros_like(p, dtype=torch.float32) for p in self.adamw_params]
         self.adamw_steps = [0] * len(self.adamw_params)
 
-    @torch.no_grad()
-    def step(self):
-        """One step over every parameter whose ``.grad`` is set."""
+    def step(self, closure=None):
+        """One step over every parameter whose ``.grad`` is set; ``closure``
+        (optional) re-evaluates the model with gradients enabled first, and
+        its loss is returned."""
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        with torch.no_grad():
+            self._step()
+        return loss
+
+    def _step(self):
         idx = [i for i, e in enumerate(self.muon) if e.param.grad is not None]
         if idx:
             params = [self.muon[i].param.view(self.muon[i].rows, self.muon[i].cols) for i in idx]
@@ -128,6 +138,37 @@ class Muon:
                                 [self.exp_avg[j] for j in jdx], [self.exp_avg_sq[j] for j in jdx],
                                 step=count, lr=self.adamw_lr, beta1=self.betas[0], beta2=self.betas[1],
                                 eps=self.eps, wd=self.adamw_wd, handle=self.handle)
+
+    def state_dict(self):
+        """The optimizer state (momenta, AdamW moments and step counts, by
+        parameter name, as copies on the host) and its hyper-parameters."""
+        return {"muon": {e.name: self.momenta[i].detach().cpu().clone() for i, e in enumerate(self.muon)},
+                "adamw": {n: {"exp_avg": self.exp_avg[j].detach().cpu().clone(),
+                              "exp_avg_sq": self.exp_avg_sq[j].detach().cpu().clone(),
+                              "step": self.adamw_steps[j]} for j, n in enumerate(self.adamw_names)},
+                "hparams": {"lr": self.lr, "wd": self.wd, "momentum": self.momentum, "nesterov": self.nesterov,
+                            "ns_steps": self.ns_steps, "ns_method": self.ns_method, "update_rms": self.update_rms,
+                            "adamw_lr": self.adamw_lr, "adamw_betas": self.betas, "adamw_eps": self.eps,
+                            "adamw_wd": self.adamw_wd}}
+
+    def load_state_dict(self, state):
+        """Restore a ``state_dict``: the same parameter names are required;
+        the hyper-parameters are taken from it."""
+        names = [e.name for e in self.muon]
+        if sorted(state["muon"]) != sorted(names) or sorted(state["adamw"]) != sorted(self.adamw_names):
+            raise ValueError("the state holds other parameters than this optimizer")
+        for i, n in enumerate(names):
+            self.momenta[i].copy_(state["muon"][n])
+        for j, n in enumerate(self.adamw_names):
+            st = state["adamw"][n]
+            self.exp_avg[j].copy_(st["exp_avg"])
+            self.exp_avg_sq[j].copy_(st["exp_avg_sq"])
+            self.adamw_steps[j] = int(st["step"])
+        hp = state["hparams"]
+        self.lr, self.wd, self.momentum, self.nesterov = hp["lr"], hp["wd"], hp["momentum"], hp["nesterov"]
+        self.ns_steps, self.ns_method, self.update_rms = hp["ns_steps"], hp["ns_method"], hp["update_rms"]
+        self.adamw_lr, self.betas, self.eps, self.adamw_wd = (hp["adamw_lr"], tuple(hp["adamw_betas"]),
+                                                              hp["adamw_eps"], hp["adamw_wd"])
 
     def zero_grad(self, set_to_none: bool = True):
         for p in [e.param for e in self.muon] + self.adamw_params:

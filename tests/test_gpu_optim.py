@@ -70,3 +70,36 @@ def test_muon_optimizer_three_steps_against_the_oracle():
     # the optimizer's momenta equal the oracle's
     for i, n in enumerate(muon_names):
         assert np.linalg.norm(opt.momenta[i].double().cpu().numpy() - mom[n]) <= TOL_EXACT * np.linalg.norm(mom[n])
+
+
+def test_muon_optimizer_state_dict_resumes_bit_for_bit():
+    # two steps, save, a fresh optimizer loads the state, one more step:
+    # parameters equal three uninterrupted steps bit for bit
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    torch.cuda.set_device(0)
+
+    def grads(params, k):
+        for i, (n, p) in enumerate(params.items()):
+            g = wl.gaussian(1000 + 10 * k + i, p.shape, 1e-2)
+            p.grad = torch.tensor(g).to(torch.bfloat16).cuda()
+
+    runs = []
+    for resume in (False, True):
+        params = _model()
+        kw = dict(lr=0.02, wd=0.1, adamw_lr=3e-4, higher_rank=True, split_heads={"attn.qkv.weight": 3})
+        opt = pkg.Muon(params.items(), **kw)
+        for k in range(3):
+            if resume and k == 2:
+                state = opt.state_dict()
+                opt = pkg.Muon(params.items(), **dict(kw, lr=1.0))   # hyper-parameters come from the state
+                opt.load_state_dict(state)
+            grads(params, k)
+            loss = opt.step(closure=lambda: torch.zeros(()))
+            assert float(loss) == 0.0
+            opt.zero_grad()
+        torch.cuda.synchronize()
+        runs.append({n: p.detach().cpu() for n, p in params.items()})
+    for n in runs[0]:
+        assert torch.equal(runs[0][n], runs[1][n]), n
