@@ -115,8 +115,10 @@ muon_status_t muon_handle_check(muon_handle_t h, void* stream);
  * Iteration; "DeepSpeed 集成 Muon 优化器实战", §核心算子).
  *   X       device, [batch][m][n] row-major, dtype; overwritten by O
  *   dtype   MUON_BF16: bf16 tensor-core path (bf16 operands, fp32
- *           accumulation, master X kept as bf16 hi + lo planes, about 16
- *           mantissa bits); MUON_F32: fp32 CUDA-core path
+ *           accumulation, master X kept as a bf16 plane hi plus one byte
+ *           with its next 8 bits, about 16 significant bits); MUON_F32:
+ *           fp32 path (tensor cores with three bf16 planes per operand up
+ *           to m = 2048, CUDA cores above)
  *   steps   >= 0 (0 returns the normalised input)
  *   coeffs  host pointer to (a, b, c); NULL = (3.4445, -4.7750, 2.0315)
  *   ns_method  muon_ns_method_t

@@ -52,6 +52,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
+// ------------------------------------------------ lo plane as signed bytes
+// The tensor-core path holds the master X as hi + lo.  x is kept to 24 bits
+// (its fp32 pattern rounded at bit 8); hi = bf16(x), rounded to nearest, is
+// the MMA operand, and the signed byte q = (bits(x) + 128 - (bits(hi) << 16))
+// >> 8 carries the next 8 bits: (bits(hi) << 16) + (q << 8) is x's rounded
+// pattern again, in integer arithmetic on the patterns (x and hi share
+// their sign).  -128 <= q <= 128; q = 128 (x's 24-bit rounding falls on the
+// midpoint between two bf16 values, about one value in 512) is stored as
+// 127, one step short.  hi + lo keeps about 16 significant bits, as a bf16
+// lo plane would, at 3 bytes per element.
+// hi32 = bits(hi) << 16 (hi's fp32 pattern).
+__device__ __forceinline__ int lo8_code(uint32_t xbits, uint32_t hi32) {
+  const int d = static_cast<int>(xbits + 0x80u - hi32) >> 8;
+  return d < 127 ? d : 127;
+}
+// byte k of w sign-extended and shifted left by 8 (prmt: byte 0 zero, byte
+// 1 = byte k, bytes 2 and 3 replicate its sign)
+__device__ __forceinline__ uint32_t lo8_shifted(uint32_t w, int k) {
+  const uint32_t sel = 0x4u | (static_cast<uint32_t>(k) << 4) | ((static_cast<uint32_t>(k) | 8u) << 8) |
+                       ((static_cast<uint32_t>(k) | 8u) << 12);
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(w), "r"(0u), "r"(sel));
+  return d;
+}
+// x from hi's fp32 pattern and byte k of a word of codes
+__device__ __forceinline__ float lo8_join(uint32_t hi32, uint32_t w, int k) {
+  return __uint_as_float(hi32 + lo8_shifted(w, k));
+}
+// the low bytes of four codes into one word, code k in byte k
+__device__ __forceinline__ uint32_t pack_lo8x4(int q0, int q1, int q2, int q3) {
+  uint32_t t01, t23, w;
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(t01) : "r"(q0), "r"(q1));
+  asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(t23) : "r"(q2), "r"(q3));
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(t01), "r"(t23));
+  return w;
+}
+
 __device__ __forceinline__ float load_as_f32(const void* base, long long idx, int dtype) {
   return dtype == DT_BF16 ? bf2f(reinterpret_cast<const __nv_bfloat16*>(base)[idx])
                           : reinterpret_cast<const float*>(base)[idx];

@@ -47,7 +47,8 @@ struct PrepParams {
   long long ldx;           // row stride of the NS workspace (elements)
   float* xf;               // fp32 copy [batch][m][ldx] or nullptr
   __nv_bfloat16* xb;       // bf16 operand copy = hi plane of the master, or nullptr (fp32 path)
-  __nv_bfloat16* xlo;      // lo plane of the master, bf16(U - bf16(U)), or nullptr
+  __nv_bfloat16* xlo;      // second bf16 plane bf16(U - bf16(U)) (fp32 tensor-core path), or nullptr
+  int8_t* xlo8;            // lo plane of the bf16 path's master as signed-byte codes (lo8_code), or nullptr
   __nv_bfloat16* xlo2;     // third plane bf16(U - hi - lo) (fp32 tensor-core path), or nullptr
   float* partials;         // [batch][tiles_per_mat]
   int tiles_per_mat;
@@ -220,7 +221,7 @@ cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStrea
 // 3-D map {cols, rows, batch} (row stride ld elements, matrices rows * ld
 // apart) with a 32 x 32 box: fp32 with 128-byte swizzle (32 floats = one
 // 128-byte row) or bf16 with 64-byte swizzle: the epilogue's blocks of the
-// master X planes.
+// master X's hi plane and of the destinations.
 inline bool encode_box32(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, bool f32,
                          uint64_t cols, uint64_t rows, uint64_t batch, uint64_t ld) {
   const uint64_t es = f32 ? 4 : 2;
@@ -231,6 +232,19 @@ inline bool encode_box32(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map
   return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same 3-D map over the master X's lo plane of signed-byte codes (row
+// stride ld bytes, a multiple of 16): 32 x 32 box, 32-byte swizzle.
+inline bool encode_lo8_box32(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, uint64_t cols,
+                             uint64_t rows, uint64_t batch, uint64_t ld) {
+  cuuint64_t dims[3] = {cols, rows, batch};
+  cuuint64_t strides[2] = {ld, rows * ld};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // fp32 SIMT path (CUDA cores).  wide = 0: fp32 m x m matrices; wide = 1:

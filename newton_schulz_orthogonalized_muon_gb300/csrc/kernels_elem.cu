@@ -3,10 +3,10 @@
 //  * muon_prepare_kernel: momentum M <- mu*M + G, Nesterov U = G + mu*M
 //    (else U = M), per-tile partial sums of U^2 for the Frobenius norm, and
 //    the NS working copy of U (fp32 for the fp32 CUDA-core path; for the
-//    tensor-core path the bf16 MMA operand hi = bf16(U) and the lo plane
-//    bf16(U - hi), and for the fp32 tensor-core path a third plane
-//    bf16(U - hi - lo)), transposed through shared memory when the block has
-//    rows > cols.
+//    bf16 tensor-core path the MMA operand hi = bf16(U) and the lo plane as
+//    signed-byte codes of U - hi; for the fp32 tensor-core path three bf16
+//    planes hi, bf16(U - hi), bf16(U - hi - lo)), transposed through shared
+//    memory when the block has rows > cols.
 //    ("迎接DeepSeek开源周…Muon优化器" (coreui.cn), §代码, Muon step;
 //     "Muon Optimizer and the Distributed Implementation", §Newton-Schulz
 //     Iteration, normalisation by the Frobenius norm.)
@@ -42,6 +42,14 @@ __device__ __forceinline__ void split_hi_lo(const float* u, uint32_t* hw, uint32
       l2w[k] = pack_bf16x2(r0 - lf.x, r1 - lf.y);
     }
   }
+}
+
+// the lo code of one value, and a word of the codes of four
+__device__ __forceinline__ int lo8_of(float u) {
+  return lo8_code(__float_as_uint(u), __float_as_uint(bf2f(f2bf(u))));
+}
+__device__ __forceinline__ uint32_t lo8_word(const float* u) {
+  return pack_lo8x4(lo8_of(u[0]), lo8_of(u[1]), lo8_of(u[2]), lo8_of(u[3]));
 }
 
 // the third plane of one value
@@ -143,6 +151,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
             uint32_t hw[4], lw[4], l2w[4];
             split_hi_lo(u, hw, lw, 4, l2w);
             *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (p.xlo8 != nullptr) *reinterpret_cast<uint2*>(p.xlo8 + xo) = make_uint2(lo8_word(u), lo8_word(u + 4));
             if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             if (p.xlo2 != nullptr) *reinterpret_cast<uint4*>(p.xlo2 + xo) = make_uint4(l2w[0], l2w[1], l2w[2], l2w[3]);
           }
@@ -152,6 +161,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
             if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
             if (p.xlo2 != nullptr) p.xlo2[xo + k] = third_plane(u[k]);
+            if (p.xlo8 != nullptr) p.xlo8[xo + k] = static_cast<int8_t>(lo8_of(u[k]));
           }
         }
       }
@@ -181,6 +191,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
             uint32_t hw[2], lw[2], l2w[2];
             split_hi_lo(u, hw, lw, 2, l2w);
             *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(hw[0], hw[1]);
+            if (p.xlo8 != nullptr) *reinterpret_cast<uint32_t*>(p.xlo8 + xo) = lo8_word(u);
             if (p.xlo != nullptr) *reinterpret_cast<uint2*>(p.xlo + xo) = make_uint2(lw[0], lw[1]);
             if (p.xlo2 != nullptr) *reinterpret_cast<uint2*>(p.xlo2 + xo) = make_uint2(l2w[0], l2w[1]);
           }
@@ -190,6 +201,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
             if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
             if (p.xlo2 != nullptr) p.xlo2[xo + k] = third_plane(u[k]);
+            if (p.xlo8 != nullptr) p.xlo8[xo + k] = static_cast<int8_t>(lo8_of(u[k]));
           }
         }
       }

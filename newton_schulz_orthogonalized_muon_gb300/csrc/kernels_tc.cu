@@ -65,9 +65,9 @@ using namespace tc;
 
 
 // UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
-// 4 KB slot, which leaves room for a fourth main-loop stage at BN = 256;
-// FINAL keeps two, FINAL_T one (6 KB), G_FINAL_T two 2 KB slots (free: the
-// stage count is the same with one).
+// 3 KB slot, which leaves room for a fourth main-loop stage at BN = 256;
+// FINAL keeps two 4 KB slots, FINAL_T one (5 KB), G_FINAL_T two 2 KB slots
+// (free: the stage count is the same with one).
 template <int MODE>
 struct OneSlots {
   static constexpr int v = (MODE == MODE_FINAL || MODE == MODE_G_FINAL_T) ? 2 : 1;

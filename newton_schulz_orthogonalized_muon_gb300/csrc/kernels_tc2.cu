@@ -30,7 +30,7 @@ using namespace tc;
 constexpr int PBM = 256;       // rows of the pair's tile (128 per CTA)
 constexpr int PBN = 256;       // columns of the tile = N of the pair MMA (128 loaded per CTA)
 // UPDATE / FINAL input blocks in flight per epilogue warp: UPDATE takes one
-// 4 KB slot (two measured no faster on long K); FINAL keeps two, as one slot
+// 3 KB slot (two measured no faster on long K); FINAL keeps two, as one slot
 // costs it register spills.  XS overrides the default: UPDATE with two slots
 // serves short K (m <= 1024), where the epilogue's input latency, not the
 // main loop, bounds a tile; the five-stage ring leaves room for it.

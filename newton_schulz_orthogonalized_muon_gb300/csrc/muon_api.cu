@@ -364,9 +364,10 @@ Regions regions(const GroupPlan& g, int cap, bool tc, bool gram, int steps, bool
   } else if (!gram) {
     if (tc) {
       // master X = hi + lo: hi is the operand copy (xb0 / xb1 ping-pong), lo
-      // in place; the fp32 copy only when no NS step runs
+      // (one signed-byte code per element) in place; the fp32 copy only when
+      // no NS step runs
       r.xf = (steps == 0) ? take(xe * 4) : 0;
-      r.xlo = (steps == 0) ? 0 : take(xe * 2);
+      r.xlo = (steps == 0) ? 0 : take(xe);
       r.xb0 = take(xe * 2);
       r.xb1 = take(xe * 2);
       r.symA = take(se * 2);
@@ -673,7 +674,7 @@ bool f32tc_group(muon_handle_t h, const GroupPlan& g, bool tc, bool gram) {
 
 size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps, size_t limit) {
   const bool f32tc = f32tc_group(h, g, tc, gram);
-  g.ldx = static_cast<long long>(align_up(g.n, 8));
+  g.ldx = static_cast<long long>(align_up(g.n, 16));   // 16: the lo plane's byte rows stay 16-byte aligned
   g.ldm = static_cast<long long>(align_up(g.m, 8));
   g.prep_tiles = static_cast<int>(ceil_div(g.m, 64) * ceil_div(g.n, 64));
   g.bn_sym = g.m <= 128 ? 128 : 256;
@@ -772,7 +773,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
   // overlaps the products), and the tensor maps over them.
   struct StdSet {
     float *xf, *xf2, *pdiag, *partials, *scale;
-    __nv_bfloat16 *xb[2], *xlo;
+    __nv_bfloat16* xb[2];
+    int8_t* xlo;
     void *symA, *symB;
     bool n128;
     CUtensorMap map_x[2], map_xmn[2], map_A, map_A64, map_B, map_xh[2], map_xl, map_sa, map_sb;
@@ -791,7 +793,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     S.pdiag = tc ? reinterpret_cast<float*>(base + R.pdiag) : nullptr;
     S.partials = reinterpret_cast<float*>(base + R.partials);
     S.scale = reinterpret_cast<float*>(base + R.scale);
-    S.xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(base + R.xlo) : nullptr;
+    S.xlo = (tc && steps > 0) ? reinterpret_cast<int8_t*>(base + R.xlo) : nullptr;
     if (tc && steps > 0) {
       if (!encode_map(h, &S.map_x[0], S.xb[0], g.n, g.m, g.chunk, g.ldx) ||
           !encode_map(h, &S.map_x[1], S.xb[1], g.n, g.m, g.chunk, g.ldx) ||
@@ -802,7 +804,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
           !encode_map(h, &S.map_B, S.symB, g.m, g.m, g.chunk, g.ldm) ||
           !encode_box32(h->encode, &S.map_xh[0], S.xb[0], false, g.n, g.m, g.chunk, g.ldx) ||
           !encode_box32(h->encode, &S.map_xh[1], S.xb[1], false, g.n, g.m, g.chunk, g.ldx) ||
-          !encode_box32(h->encode, &S.map_xl, S.xlo, false, g.n, g.m, g.chunk, g.ldx) ||
+          !encode_lo8_box32(h->encode, &S.map_xl, S.xlo, g.n, g.m, g.chunk, g.ldx) ||
           !encode_box32(h->encode, &S.map_sa, S.symA, false, g.m, g.m, g.chunk, g.ldm) ||
           !encode_box32(h->encode, &S.map_sb, S.symB, false, g.m, g.m, g.chunk, g.ldm))
         return fail(h, MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed");
@@ -822,7 +824,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     pp.ldx = g.ldx;
     pp.xf = (tc && steps > 0) ? nullptr : S.xf;
     pp.xb = S.xb[0];
-    pp.xlo = S.xlo;
+    pp.xlo8 = S.xlo;
     pp.partials = S.partials;
     pp.tiles_per_mat = g.prep_tiles;
     MUON_LAUNCH(MUON_K_PREPARE, launch_prepare(pp, cnt, g.prep_tiles, stream), "prepare launch");

@@ -129,7 +129,7 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
   const bool tc = (dtype == MUON_BF16);
   const float ca = coeffs ? coeffs[0] : 3.4445f, cb = coeffs ? coeffs[1] : -4.7750f, cc = coeffs ? coeffs[2] : 2.0315f;
   const int M = static_cast<int>(mm), N = static_cast<int>(nn);
-  const long long ldx = (N + 7) / 8 * 8, ldm = (M + 7) / 8 * 8;
+  const long long ldx = (N + 15) / 16 * 16, ldm = (M + 7) / 8 * 8;
   const int prep_tiles = ((M + 63) / 64) * ((N + 63) / 64);
   const int bn_sym = M <= 128 ? 128 : 256, bn_upd = N <= 128 ? 128 : 256;
 
@@ -148,9 +148,9 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
   int2* tri_d = reinterpret_cast<int2*>(take(sizeof(int2) * kMaxTri));
   const size_t xe = static_cast<size_t>(M) * ldx, se = static_cast<size_t>(M) * ldm;
   // fp32 copy of X0 (fp32 path, or no NS step); the tensor-core path's lo
-  // plane of the master X = hi + lo shares its space
+  // plane of the master X = hi + lo (signed-byte codes) shares its space
   float* xf = reinterpret_cast<float*>(take(xe * 4));
-  __nv_bfloat16* xlo = (tc && steps > 0) ? reinterpret_cast<__nv_bfloat16*>(xf) : nullptr;
+  int8_t* xlo = (tc && steps > 0) ? reinterpret_cast<int8_t*>(xf) : nullptr;
   float* xf2 = tc ? nullptr : reinterpret_cast<float*>(take(xe * 4));
   __nv_bfloat16* xb0 = tc ? reinterpret_cast<__nv_bfloat16*>(take(xe * 2)) : nullptr;
   __nv_bfloat16* xb1 = tc ? reinterpret_cast<__nv_bfloat16*>(take(xe * 2)) : nullptr;
@@ -185,7 +185,7 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
   pp.ldx = ldx;
   pp.xf = (tc && steps > 0) ? nullptr : xf;
   pp.xb = xb0;
-  pp.xlo = xlo;
+  pp.xlo8 = xlo;
   pp.partials = partials;
   pp.tiles_per_mat = prep_tiles;
   if (launch_prepare(pp, 1, prep_tiles, stream) != cudaSuccess) return MUON_ERR_CUDA;
@@ -201,7 +201,7 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
               encode_map(S->encode, &map_A, symA, M, M, ldm) && encode_map(S->encode, &map_B, symB, M, M, ldm) &&
               encode_box32(S->encode, &map_xh[0], xb0, false, N, M, 1, ldx) &&
               encode_box32(S->encode, &map_xh[1], xb1, false, N, M, 1, ldx) &&
-              encode_box32(S->encode, &map_xl, xlo, false, N, M, 1, ldx) &&
+              encode_lo8_box32(S->encode, &map_xl, xlo, N, M, 1, ldx) &&
               encode_box32(S->encode, &map_sa, symA, false, M, M, 1, ldm) &&
               encode_box32(S->encode, &map_sb, symB, false, M, M, 1, ldm)))
     return MUON_ERR_CUDA;

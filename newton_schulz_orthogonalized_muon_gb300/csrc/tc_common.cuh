@@ -96,22 +96,24 @@ __device__ __forceinline__ void decode_tile(const NsGemmParams& p, int t, int& b
 }
 
 // ------------------------------------------- UPDATE / FINAL / G_FINAL epilogue
-// The master X of the tensor-core path is held as two bf16 planes, X = hi +
-// lo: hi = bf16(X) is the MMA operand copy itself, lo = bf16(X - hi) keeps
-// about 16 mantissa bits in all.  Each epilogue warp owns 32 rows (its TMEM
+// The master X of the tensor-core path is held as two planes, X = hi + lo:
+// hi = bf16(X) is the MMA operand copy itself, lo a signed byte with the
+// next 8 bits of X's pattern (lo8_code), about 16 significant bits in all at
+// 3 bytes per element.  Each epilogue warp owns 32 rows (its TMEM
 // lane quadrant) and half of the tile's columns, which it walks in 32 x 32
-// blocks.  Per warp, in shared memory, SLOTS slots of 4 KB:
-//   UPDATE / FINAL: [hi 32 x 32 bf16 | lo 32 x 32 bf16], 64-byte rows with
-//   64-byte swizzle, loaded by TMA up to SLOTS blocks ahead (across tile
-//   boundaries) so the loads overlap the main loop.  UPDATE writes the new
-//   hi and lo back in place and stores both with TMA (hi to the other
-//   operand buffer, lo in place).
+// blocks.  Per warp, in shared memory, SLOTS slots (3 KB for UPDATE, 4 KB
+// for FINAL):
+//   UPDATE / FINAL: [hi 32 x 32 bf16, 64-byte rows with 64-byte swizzle |
+//   lo 32 x 32 codes, 32-byte rows with 32-byte swizzle], loaded by TMA up
+//   to SLOTS blocks ahead (across tile boundaries) so the loads overlap the
+//   main loop.  UPDATE writes the new hi and lo back in place and stores
+//   both with TMA (hi to the other operand buffer, lo in place).
 //   FINAL / G_FINAL: after the block's inputs are in registers the slot is
 //   reused as 32 x 32 fp32 (128-byte rows, 128-byte swizzle) holding the
 //   result in destination orientation (transposed when the destination is
 //   out[c][r]), then written out as 16-byte row segments, eight lanes per
 //   destination row.
-//   FINAL_T (bf16 destinations with tensor maps): [hi | lo | W], W the
+//   FINAL_T (bf16 destinations with tensor maps): [hi | lo | W] (5 KB), W the
 //   destination's 32 x 32 block in destination orientation, loaded by TMA
 //   with hi and lo, updated in place and stored back by TMA; G_FINAL_T: [W].
 //   F_UPDATE (fp32 tensor-core path): no inputs; the result's three bf16
@@ -125,9 +127,11 @@ struct EpiLayout {
   static constexpr bool kLoadX = (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_FINAL_T);
   static constexpr bool kFill = kLoadX || ModeTraits<MODE>::kTmaOut;   // slots filled by TMA
   static constexpr int SLOTS = kFill ? XSLOTS : 1;         // input blocks in flight per warp
-  static constexpr int SLOT_BYTES = MODE == MODE_FINAL_T ? 6144 : MODE == MODE_G_FINAL_T ? 2048 : 4096;
-  static constexpr int LO_OFF = 2048;                 // lo plane within a slot
-  static constexpr int W_OFF = MODE == MODE_G_FINAL_T ? 0 : 4096;   // destination block within a slot
+  static constexpr int X_BYTES = 3072;                // a block of the master: hi (2 KB) + lo codes (1 KB)
+  static constexpr int SLOT_BYTES =
+      MODE == MODE_FINAL_T ? 5120 : MODE == MODE_G_FINAL_T ? 2048 : MODE == MODE_UPDATE ? X_BYTES : 4096;
+  static constexpr int LO_OFF = 2048;                 // lo codes (F_UPDATE: second plane) within a slot
+  static constexpr int W_OFF = MODE == MODE_G_FINAL_T ? 0 : X_BYTES;   // destination block within a slot
   static constexpr int WARP_BYTES = SLOTS * SLOT_BYTES;   // a multiple of 1024
   static constexpr int BYTES = kMN ? EPI_WARPS * WARP_BYTES : 0;
 };
@@ -139,6 +143,27 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int q) {
 // byte offset of 16-byte chunk q of row r: 64-byte rows, 64-byte swizzle
 __device__ __forceinline__ uint32_t sw64_off(int r, int q) {
   return static_cast<uint32_t>(r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+}
+// byte offset of 16-byte chunk q of row r: 32-byte rows, 32-byte swizzle
+__device__ __forceinline__ uint32_t sw32_off(int r, int q) {
+  return static_cast<uint32_t>(r * 32 + ((q ^ ((r >> 2) & 1)) << 4));
+}
+// hi patterns (fp32 bits) of 8 bf16 values, and the 8 values x = hi + lo
+// joined with their codes, the elements 8 * (g & 1) .. + 7 of a 16-code chunk
+__device__ __forceinline__ void lo8_unpack8(const uint4& hraw, const uint4& codes, int g, uint32_t* hi32, float* x) {
+  const uint32_t hw[4] = {hraw.x, hraw.y, hraw.z, hraw.w};
+  const uint32_t w0 = (g & 1) ? codes.z : codes.x;
+  const uint32_t w1 = (g & 1) ? codes.w : codes.y;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    hi32[2 * e] = hw[e] << 16;
+    hi32[2 * e + 1] = hw[e] & 0xFFFF0000u;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[e] = lo8_join(hi32[e], w0, e);
+    x[4 + e] = lo8_join(hi32[4 + e], w1, e);
+  }
 }
 // byte offset of bf16 element (r, c) of a 32 x 32 block, 64-byte rows, 64-byte swizzle
 __device__ __forceinline__ uint32_t sw64_elem(int r, int c) { return sw64_off(r, c >> 3) + 2u * (c & 7); }
@@ -316,7 +341,7 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
               tma_load_3d(dst + L::W_OFF, &p.wmap[b], &xfull[slot], tr ? y : x, tr ? x : y, 0);
             }
           } else {
-            mbar_arrive_expect_tx(&xfull[slot], L::SLOT_BYTES);
+            mbar_arrive_expect_tx(&xfull[slot], L::X_BYTES);
             tma_load_3d(dst, map_xh, &xfull[slot], x, y, b);
             tma_load_3d(dst + L::LO_OFF, map_xl, &xfull[slot], x, y, b);
           }
@@ -383,29 +408,34 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         for (int h = 0; h < 32; h += 16) {
           float v[16];
           acc_ld16<MODE, BN>(tb + static_cast<uint32_t>(32 * k + h), v, two_parts);
+          uint4* pl = reinterpret_cast<uint4*>(sbuf + L::LO_OFF + sw32_off(lane, h >> 4));
+          const uint4 codes = *pl;
+          uint32_t nc[4];
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             uint4* ph = reinterpret_cast<uint4*>(sbuf + sw64_off(lane, (h >> 3) + q));
-            uint4* pl = reinterpret_cast<uint4*>(sbuf + L::LO_OFF + sw64_off(lane, (h >> 3) + q));
-            float hi[8], lo[8], o[8];
-            unpack8(*ph, hi);
-            unpack8(*pl, lo);
+            uint32_t hi32[8];
+            float x[8], o[8];
+            lo8_unpack8(*ph, codes, q, hi32, x);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              o[e] = s * fmaf(pd, hi[e] + lo[e], fmaf(-pdb, hi[e], v[8 * q + e]));
-            uint4 nh, nl;
+              o[e] = s * fmaf(pd, x[e], fmaf(-pdb, __uint_as_float(hi32[e]), v[8 * q + e]));
+            uint4 nh;
             uint32_t* wh = reinterpret_cast<uint32_t*>(&nh);
-            uint32_t* wl = reinterpret_cast<uint32_t*>(&nl);
+            int qc[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
-              const float2 hf = __bfloat1622float2(h2);
-              wh[e] = *reinterpret_cast<const uint32_t*>(&h2);
-              wl[e] = pack_bf16x2(o[2 * e] - hf.x, o[2 * e + 1] - hf.y);
+              const uint32_t hw = *reinterpret_cast<const uint32_t*>(&h2);
+              wh[e] = hw;
+              qc[2 * e] = lo8_code(__float_as_uint(o[2 * e]), hw << 16);
+              qc[2 * e + 1] = lo8_code(__float_as_uint(o[2 * e + 1]), hw & 0xFFFF0000u);
             }
+            nc[2 * q] = pack_lo8x4(qc[0], qc[1], qc[2], qc[3]);
+            nc[2 * q + 1] = pack_lo8x4(qc[4], qc[5], qc[6], qc[7]);
             *ph = nh;
-            *pl = nl;
           }
+          *pl = make_uint4(nc[0], nc[1], nc[2], nc[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -472,11 +502,12 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         if constexpr (L::kLoadX) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float hi[8], lo[8];
-            unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)), hi);
-            unpack8(*reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)), lo);
+            uint32_t hi32[8];
+            float x[8];
+            lo8_unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)),
+                        *reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw32_off(lane, q >> 1)), q, hi32, x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd - pdb, hi[e], pd * lo[e]);
+            for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd, x[e], -pdb * __uint_as_float(hi32[e]));
           }
         } else {
 #pragma unroll
@@ -535,11 +566,12 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
         if (MODE == MODE_FINAL) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float hi[8], lo[8];
-            unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)), hi);
-            unpack8(*reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw64_off(lane, q)), lo);
+            uint32_t hi32[8];
+            float x[8];
+            lo8_unpack8(*reinterpret_cast<const uint4*>(sbuf + sw64_off(lane, q)),
+                        *reinterpret_cast<const uint4*>(sbuf + L::LO_OFF + sw32_off(lane, q >> 1)), q, hi32, x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd - pdb, hi[e], pd * lo[e]);
+            for (int e = 0; e < 8; ++e) corr[8 * q + e] = fmaf(pd, x[e], -pdb * __uint_as_float(hi32[e]));
           }
           __syncwarp();                  // every lane holds its row: the slot may be overwritten
         } else {

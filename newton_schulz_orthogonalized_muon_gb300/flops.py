@@ -85,9 +85,10 @@ def set_flops(specs, steps: int = 5, method: str = "standard"):
 
 def prepare_bytes(numel: int, grad_bytes: int = 2) -> float:
     """HBM bytes of the momentum/Nesterov/norm/cast pass of the tensor-core
-    path: read G, read and write M (fp32), write the two bf16 planes of the
-    master X (hi = the MMA operand copy, lo = the residual)."""
-    return float(numel) * (grad_bytes + 4 + 4 + 2 + 2)
+    path: read G, read and write M (fp32), write the master X's two planes
+    (hi = the bf16 MMA operand copy, lo = one signed byte with the next
+    8 bits)."""
+    return float(numel) * (grad_bytes + 4 + 4 + 2 + 1)
 
 
 def adamw_bytes(numel: int, param_bytes: int = 2, grad_bytes: int = 2) -> float:
