@@ -140,7 +140,9 @@ struct NsGemmParams {
   int num_tiles;                // batch * tiles_per_mat
   int mi;                       // row blocks of the output (UPDATE/FINAL)
   const int2* tri;              // (i, j) tile table of the symmetric modes
-  const float* scale;           // per-matrix 1/||U||_F applied this iteration, or nullptr
+  const float* scale;           // per-matrix s = 1/||U||_F in the first iteration, or nullptr:
+                                // SYRK writes s^2 X X^T, the bf16 path's POLY s P (its
+                                // UPDATE / FINAL then apply none), the other updates s P X
   float ca, cb, cc;             // quintic coefficients
   // symmetric outputs (A or B matrix), row stride ldm
   void* sym_out;                // bf16 (tensor-core path) or fp32 (fp32 path)

@@ -879,7 +879,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
                     launch_ns_gemm_pair(MODE_SYRK, S.map_x[it & 1], S.map_x[it & 1], S.map_sa, S.map_sa, q, pairs, stream,
                                         S.n128 ? &S.map_xmn[it & 1] : nullptr),
                     "syrk launch");
-        q.scale = nullptr;
+        q.scale = p.scale;                     // P' = s P in the first iteration
         q.sym_in = S.symA;
         q.sym_out = S.symB;
         MUON_LAUNCH(MUON_K_POLY,
@@ -918,12 +918,12 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
         MUON_LAUNCH(MUON_K_SYRK, launch_ns_gemm_tc(MODE_SYRK, g.bn_sym, S.map_x[it & 1], S.map_x[it & 1], S.map_sa, S.map_sa, q, grid,
                                                        stream),
                     "syrk launch");
-        // POLY: P = a I + b A + c A A
-        q.scale = nullptr;
+        // POLY: P = a I + b A + c A A, times s in the first iteration
+        q.scale = p.scale;
         q.sym_in = S.symA;
         q.sym_out = S.symB;
         MUON_LAUNCH(MUON_K_POLY, launch_ns_gemm_tc(MODE_POLY, g.bn_sym, S.map_A, S.map_A, S.map_sb, S.map_sb, q, grid, stream), "poly launch");
-        // UPDATE / FINAL: X = s (P^ X^ + P_rr X - P^_rr X^)
+        // UPDATE / FINAL: X = P^ X^ + P_rr X - P^_rr X^ (s inside P)
         NsGemmParams u = p;
         u.mi = mi;
         u.tiles_per_mat = mi * nj;

@@ -232,7 +232,7 @@ extern "C" muon_status_t muon_orthogonalize_noalloc(void* X, int32_t dtype, int6
       const int gs = q.num_tiles < S->num_sms ? q.num_tiles : S->num_sms;
       e = launch_ns_gemm_tc(MODE_SYRK, bn_sym, map_x[it & 1], map_x[it & 1], map_sa, map_sa, q, gs, stream);
       if (e != cudaSuccess) return MUON_ERR_CUDA;
-      q.scale = nullptr;
+      // POLY keeps the scale: P' = s P in the first iteration
       q.sym_in = symA;
       q.sym_out = symB;
       e = launch_ns_gemm_tc(MODE_POLY, bn_sym, map_A, map_A, map_sb, map_sb, q, gs, stream);

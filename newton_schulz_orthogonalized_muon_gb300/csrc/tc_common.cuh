@@ -379,7 +379,10 @@ __device__ __forceinline__ void mn_epilogue(const NsGemmParams& p, const CUtenso
     tc_fence_after();
     const int row0 = i * TROWS + et.row_off + quad * 32;
     const int gr = row0 + lane;
-    const float s = p.scale != nullptr ? p.scale[b] : 1.f;
+    // the first iteration's 1 / ||U||_F: UPDATE / FINAL / FINAL_T take it
+    // folded into P (POLY wrote s P), the other modes apply it here
+    constexpr bool kFolded = (MODE == MODE_UPDATE || MODE == MODE_FINAL || MODE == MODE_FINAL_T);
+    const float s = (!kFolded && p.scale != nullptr) ? p.scale[b] : 1.f;
     // exact diagonal term: acc + P_rr x - P^_rr hi, hi being the operand copy
     // whose product with the rounded diagonal P^_rr the accumulator holds
     float pd = 0.f, pdb = 0.f;
@@ -734,10 +737,10 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
       break;
     }
     tc_fence_after();
-    float s = 1.f;
+    float s = 1.f, s1 = 1.f;
     if (p.scale != nullptr) {
-      s = p.scale[b];
-      s = s * s;                                       // SYRK / G_R0 of the first iteration: s^2 X X^T
+      s1 = p.scale[b];
+      s = s1 * s1;                                     // SYRK / G_R0 of the first iteration: s^2 X X^T
     }
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                         static_cast<uint32_t>(acc * BN * AccParts<MODE>::v + cbeg);
@@ -782,10 +785,19 @@ __device__ __forceinline__ void sym_epilogue(const NsGemmParams& p, const CUtens
         if (diag && gr < m) {
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (c == lane) {
-              v[c] += p.ca;
-              if (MODE == MODE_POLY) p.pdiag[static_cast<size_t>(b) * m + gr] = v[c];
-            }
+            if (c == lane) v[c] += p.ca;
+        }
+        if (MODE == MODE_POLY) {
+          // the first iteration's s folded into P: the update reads s P
+          if (p.scale != nullptr) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] *= s1;
+          }
+          if (diag && gr < m) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c == lane) p.pdiag[static_cast<size_t>(b) * m + gr] = v[c];
+          }
         }
       }
 #pragma unroll 1
