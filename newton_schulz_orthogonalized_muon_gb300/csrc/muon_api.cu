@@ -93,6 +93,13 @@ struct muon_handle_s {
   bool overlap = false;
   cudaStream_t side = nullptr;
   std::vector<cudaEvent_t> ovl_ev;
+  // standard bf16 method on small sets: every same-shape group's chain on a
+  // stream of its own, so small launches of different groups share the SMs
+  // (MUON_CONCURRENT: 0 off, 1 whenever the groups fit the workspace limit
+  // together; default: also only for sets of at most kConcMaxElements)
+  int concurrent = -1;
+  std::vector<cudaStream_t> conc;
+  std::vector<cudaEvent_t> conc_ev;
 };
 
 namespace {
@@ -188,6 +195,28 @@ muon_status_t ensure_overlap_events(muon_handle_t h, size_t n) {
       return fail(h, MUON_ERR_CUDA, "event creation failed");
     }
     h->ovl_ev.push_back(e);
+  }
+  return MUON_OK;
+}
+
+// At least n streams and n + 1 events for concurrent groups, created on
+// first use.
+muon_status_t ensure_concurrent(muon_handle_t h, size_t n) {
+  while (h->conc.size() < n) {
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, MUON_ERR_CUDA, "stream creation failed");
+    }
+    h->conc.push_back(cs);
+  }
+  while (h->conc_ev.size() < n + 1) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, MUON_ERR_CUDA, "event creation failed");
+    }
+    h->conc_ev.push_back(e);
   }
   return MUON_OK;
 }
@@ -694,6 +723,29 @@ size_t plan_group(muon_handle_t h, GroupPlan& g, bool tc, bool gram, int steps, 
   return regions(g, g.chunk, tc, gram, steps, f32tc).total;
 }
 
+constexpr size_t kConcMaxElements = size_t(1) << 28;
+
+// Workspace bytes of the concurrent-groups layout (every group's regions
+// side by side), or 0 when the call runs its groups one after another.
+// Concurrent: the standard bf16 method, two or more groups each in a single
+// chunk, their regions within the workspace limit together, and (unless
+// forced by MUON_CONCURRENT=1) at most kConcMaxElements NS elements in all:
+// large groups fill the GPU with each launch on their own.
+size_t concurrent_need(muon_handle_t h, const std::map<std::pair<int, int>, GroupPlan>& groups, bool tc, bool gram,
+                       int steps, bool overlap) {
+  if (!tc || gram || steps == 0 || overlap || h->concurrent == 0 || groups.size() < 2) return 0;
+  size_t sum = 0, elems = 0;
+  for (const auto& kv : groups) {
+    const GroupPlan& g = kv.second;
+    if (static_cast<size_t>(g.chunk) < g.members.size()) return 0;
+    sum += align_up(regions(g, g.chunk, tc, gram, steps, false).total, 256);
+    elems += g.members.size() * static_cast<size_t>(g.m) * static_cast<size_t>(g.n);
+  }
+  if (sum > h->ws_limit) return 0;
+  if (h->concurrent < 0 && elems > kConcMaxElements) return 0;
+  return sum;
+}
+
 // coeffs: (a, b, c) of step k at coeffs[k * coeff_stride] (stride 0: one
 // triple for every step, 3: a schedule of `steps` triples).
 muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, float mu, int nesterov, int steps,
@@ -759,6 +811,8 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     }
   }
 
+  const size_t conc_need = concurrent_need(h, groups, tc, gram, steps, overlap);
+  if (conc_need > 0) ws_need = conc_need;
   const size_t half_bytes = align_up(ws_need, 256);
   muon_status_t st = ensure_ws(h, overlap ? 2 * half_bytes : ws_need);
   if (st != MUON_OK) return st;
@@ -957,6 +1011,44 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
 
   std::vector<GroupPlan*> order;              // ascending (m, n)
   for (auto& kv : groups) order.push_back(&kv.second);
+  if (conc_need > 0) {
+    // Concurrent groups: the group with the most work on the caller's
+    // stream, every other on a stream of its own that first waits for
+    // everything enqueued before (the descriptor upload included); the
+    // caller's stream waits for each of them before the call returns.
+    std::vector<GroupPlan*> by_work(order);
+    std::stable_sort(by_work.begin(), by_work.end(), [](const GroupPlan* a, const GroupPlan* b) {
+      const double wa = static_cast<double>(a->members.size()) * a->m * a->m * a->n;
+      const double wb = static_cast<double>(b->members.size()) * b->m * b->m * b->n;
+      return wa > wb;
+    });
+    std::map<const GroupPlan*, size_t> offset;   // the regions side by side, in (m, n) order
+    size_t off = 0;
+    for (GroupPlan* g : order) {
+      offset[g] = off;
+      off += align_up(regions(*g, g->chunk, tc, gram, steps, false).total, 256);
+    }
+    const size_t nside = by_work.size() - 1;
+    muon_status_t cst = ensure_concurrent(h, nside);
+    if (cst != MUON_OK) return cst;
+    MUON_CUDA_TRY(cudaEventRecord(h->conc_ev[0], stream), "concurrent start event");
+    for (size_t k = 0; k < nside; ++k)
+      MUON_CUDA_TRY(cudaStreamWaitEvent(h->conc[k], h->conc_ev[0], 0), "concurrent stream wait");
+    for (size_t k = 0; k < by_work.size(); ++k) {
+      GroupPlan& g = *by_work[k];
+      cudaStream_t gs = k == 0 ? stream : h->conc[k - 1];
+      h->prof_tag = static_cast<int>(std::find(order.begin(), order.end(), by_work[k]) - order.begin());
+      StdSet S;
+      if ((cst = make_set(g, ws + offset[&g], S)) != MUON_OK) return cst;
+      if ((cst = prep(g, S, 0, gs)) != MUON_OK) return cst;
+      if ((cst = products(g, S, 0, gs)) != MUON_OK) return cst;
+    }
+    for (size_t k = 0; k < nside; ++k) {
+      MUON_CUDA_TRY(cudaEventRecord(h->conc_ev[1 + k], h->conc[k]), "concurrent done event");
+      MUON_CUDA_TRY(cudaStreamWaitEvent(stream, h->conc_ev[1 + k], 0), "concurrent join");
+    }
+    return MUON_OK;
+  }
   if (!overlap) {
     for (size_t gi = 0; gi < order.size(); ++gi) {
       GroupPlan& g = *order[gi];
@@ -1155,6 +1247,7 @@ muon_status_t muon_handle_create(muon_handle_t* out, int device) {
     if (v >= 1 && v <= (1L << 30)) h->f32_tc_max_m = static_cast<int>(v);
   }
   if (const char* ov = std::getenv("MUON_OVERLAP")) h->overlap = ov[0] == '1';
+  if (const char* cc = std::getenv("MUON_CONCURRENT")) h->concurrent = cc[0] == '0' ? 0 : cc[0] == '1' ? 1 : -1;
   bool ok = cudaMalloc(&h->err, sizeof(unsigned)) == cudaSuccess && cudaMemset(h->err, 0, sizeof(unsigned)) == cudaSuccess;
   for (int k = 0; ok && k < muon_handle_s::kStages; ++k)
     ok = cudaEventCreateWithFlags(&h->stage_ev[k], cudaEventDisableTiming) == cudaSuccess;
@@ -1183,6 +1276,8 @@ muon_status_t muon_handle_destroy(muon_handle_t h) {
   if (h->err) cudaFree(h->err);
   for (cudaEvent_t e : h->ovl_ev) cudaEventDestroy(e);
   if (h->side) cudaStreamDestroy(h->side);
+  for (cudaEvent_t e : h->conc_ev) cudaEventDestroy(e);
+  for (cudaStream_t cs : h->conc) cudaStreamDestroy(cs);
   for (auto& r : h->prof) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -1273,6 +1368,8 @@ muon_status_t muon_workspace_size(muon_handle_t h, const muon_param_t* params, i
   size_t need = 0;
   for (auto& kv : groups)
     need = std::max(need, plan_group(h, kv.second, tc, gram, ns_steps, overlap ? h->ws_limit / 2 : h->ws_limit));
+  const size_t conc_need = concurrent_need(h, groups, tc, gram, ns_steps, overlap);
+  if (conc_need > 0) need = conc_need;
   *bytes = (overlap && need > 0) ? 2 * align_up(need, 256) : need;
   return MUON_OK;
 }
