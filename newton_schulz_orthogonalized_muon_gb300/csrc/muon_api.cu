@@ -727,18 +727,21 @@ constexpr size_t kConcMaxElements = size_t(1) << 28;
 
 // Workspace bytes of the concurrent-groups layout (every group's regions
 // side by side), or 0 when the call runs its groups one after another.
-// Concurrent: the standard bf16 method, two or more groups each in a single
+// Concurrent: the standard method on the bf16 path or the fp32 tensor-core
+// path, two or more groups each in a single
 // chunk, their regions within the workspace limit together, and (unless
 // forced by MUON_CONCURRENT=1) at most kConcMaxElements NS elements in all:
 // large groups fill the GPU with each launch on their own.
 size_t concurrent_need(muon_handle_t h, const std::map<std::pair<int, int>, GroupPlan>& groups, bool tc, bool gram,
                        int steps, bool overlap) {
-  if (!tc || gram || steps == 0 || overlap || h->concurrent == 0 || groups.size() < 2) return 0;
+  if (gram || steps == 0 || overlap || h->concurrent == 0 || groups.size() < 2) return 0;
   size_t sum = 0, elems = 0;
   for (const auto& kv : groups) {
     const GroupPlan& g = kv.second;
+    const bool f32tc = f32tc_group(h, g, tc, gram);
+    if (!tc && !f32tc) return 0;                 // the fp32 CUDA-core path runs its groups in turn
     if (static_cast<size_t>(g.chunk) < g.members.size()) return 0;
-    sum += align_up(regions(g, g.chunk, tc, gram, steps, false).total, 256);
+    sum += align_up(regions(g, g.chunk, tc, gram, steps, f32tc).total, 256);
     elems += g.members.size() * static_cast<size_t>(g.m) * static_cast<size_t>(g.n);
   }
   if (sum > h->ws_limit) return 0;
@@ -1026,7 +1029,7 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
     size_t off = 0;
     for (GroupPlan* g : order) {
       offset[g] = off;
-      off += align_up(regions(*g, g->chunk, tc, gram, steps, false).total, 256);
+      off += align_up(regions(*g, g->chunk, tc, gram, steps, f32tc_group(h, *g, tc, gram)).total, 256);
     }
     const size_t nside = by_work.size() - 1;
     muon_status_t cst = ensure_concurrent(h, nside);
@@ -1038,6 +1041,13 @@ muon_status_t run_blocks(muon_handle_t h, const std::vector<Block>& blocks, floa
       GroupPlan& g = *by_work[k];
       cudaStream_t gs = k == 0 ? stream : h->conc[k - 1];
       h->prof_tag = static_cast<int>(std::find(order.begin(), order.end(), by_work[k]) - order.begin());
+      if (f32tc_group(h, g, tc, gram)) {
+        const Regions R = regions(g, g.chunk, tc, gram, steps, true);
+        if ((cst = run_f32tc_group(h, g, R, ws + offset[&g], dbase, steps, coeffs, coeff_stride, mu, nesterov, gs)) !=
+            MUON_OK)
+          return cst;
+        continue;
+      }
       StdSet S;
       if ((cst = make_set(g, ws + offset[&g], S)) != MUON_OK) return cst;
       if ((cst = prep(g, S, 0, gs)) != MUON_OK) return cst;
