@@ -717,6 +717,48 @@ def e2e_slices(specs, param_bytes, limit=None, last_limit=None):
     return order
 
 
+def host_link(dev, stream):
+    """This machine's host link as the e2e loop meets it: one 1 GiB copy each
+    way between a pinned buffer and the device (best of three), and where the
+    GPU sits (its PCI address, NUMA node and local CPUs from sysfs) against
+    the CPUs this process may run on.  Host-to-device rates measured 33 GB/s
+    on some machines and 210 GB/s on others for the same program."""
+    import subprocess
+    import torch
+    out = {}
+    n = 1 << 29
+    hb = torch.ones(n, dtype=torch.bfloat16, pin_memory=True)
+    db = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    for name, fn in (("h2d_gbs_1gib", lambda: db.copy_(hb, non_blocking=True)),
+                     ("d2h_gbs_1gib", lambda: hb.copy_(db, non_blocking=True))):
+        best = 0.0
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            best = max(best, 2 * n / (a.elapsed_time(b) / 1e3) / 1e9)
+        out[name] = best
+    del hb, db
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={dev.index or 0}", "--query-gpu=pci.bus_id",
+                              "--format=csv,noheader"], capture_output=True, text=True, timeout=20).stdout.strip()
+        out["gpu_pci"] = bus
+        sysdir = "/sys/bus/pci/devices/" + bus.lower()[-12:]
+        for key, fname in (("gpu_numa_node", "numa_node"), ("gpu_local_cpus", "local_cpulist")):
+            if os.path.exists(os.path.join(sysdir, fname)):
+                out[key] = open(os.path.join(sysdir, fname)).read().strip()
+    except Exception:
+        pass
+    try:
+        out["process_cpus"] = len(os.sched_getaffinity(0))
+    except Exception:
+        pass
+    return out
+
+
 def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     """Same step through the public API with host buffers: every step copies
     its gradients host->device from pinned memory and reads the updated
@@ -745,6 +787,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             views.append(flat[off:off + t.numel()].view(t.shape))
             off += t.numel()
         return views
+    link = host_link(dev, stream)
     Gh = pinned_views(G)
     for gh, gd in zip(Gh, G):
         gh.copy_(gd)
@@ -856,7 +899,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             "mode": f"pipelined (copies overlapped with compute; {len(order)} calls per step, one per slice of at most "
                     f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
-            "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs}
+            "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_link": link}
 
 
 def param_dtype(args):
