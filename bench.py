@@ -513,6 +513,20 @@ def run_ours(args):
         gbs = nb / (kernel_rows["prepare"]["ms_per_step"] / 1e3) / 1e9
         hbm = {"bound": "hbm", "kernel": "muon_prepare_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"],
                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": nb}
+        # per same-shape group (the transposed parameters' groups write X through shared memory)
+        pg = {}
+        for k, tag, kms in records:
+            if k == "prepare" and 0 <= tag < len(group_list):
+                pg[tag] = pg.get(tag, 0.0) + kms
+        rows = []
+        for tag, kms in sorted(pg.items()):
+            (m, n), count = group_list[tag]
+            gb = flops.prepare_bytes(count * m * n)
+            g_gbs = gb / (kms / args.steps / 1e3) / 1e9
+            rows.append({"group": f"{m}x{n}", "matrices": count, "ms_per_step": kms / args.steps, "achieved": g_gbs,
+                         "frac": g_gbs / peaks["hbm_gbs"]})
+        if rows:
+            hbm["groups"] = rows
 
     # ---- AdamW fallback over the set's AdamW parameters (embeddings, norms)
     adamw = None
