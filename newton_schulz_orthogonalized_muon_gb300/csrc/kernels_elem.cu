@@ -59,9 +59,24 @@ __device__ __forceinline__ __nv_bfloat16 third_plane(float u) {
 }
 constexpr int PREP_THREADS = 256;
 
+// 16-byte asynchronous copy global -> shared (bypassing L1), and the waits
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
   __shared__ float tile[PT][PT + 1];
   __shared__ float red[PREP_THREADS / 32];
+  // the block's bf16 G and fp32 M tiles, staged by cp.async: every load of
+  // the block is in flight at once without holding registers (the kernel
+  // waits on memory latency; with registers as the load targets its warps
+  // kept the HBM ~70% busy)
+  __shared__ __align__(16) __nv_bfloat16 gst[PT * PT];
+  __shared__ __align__(16) float mst[PT * PT];
   // the workspace it writes is read by the previous group's kernels
   pdl_wait();
   pdl_launch_dependents();
@@ -79,6 +94,29 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
                    (e.mom == nullptr || (reinterpret_cast<uintptr_t>(e.mom) & 15) == 0);
   const long long xbase = static_cast<long long>(b) * p.m * p.ldx;
   float ss = 0.f;
+  const bool gstage = vec && e.gdtype == DT_BF16;
+  const bool mstage = vec && e.mom != nullptr;
+  if (gstage || mstage) {
+    // chunks of 8 bf16 (G) and 4 fp32 (M) values; cols % 8 == 0 on this
+    // path, so a chunk that starts inside the matrix ends inside it
+    if (gstage) {
+      for (int q = threadIdx.x; q < PT * 8; q += PREP_THREADS) {
+        const int rl = q >> 3, c = c0 + (q & 7) * 8;
+        if (r0 + rl < e.rows && c < e.cols)
+          cp_async16(gst + rl * PT + (q & 7) * 8,
+                     reinterpret_cast<const __nv_bfloat16*>(e.g) + static_cast<long long>(r0 + rl) * e.ld + c);
+      }
+    }
+    if (mstage) {
+      for (int q = threadIdx.x; q < PT * 16; q += PREP_THREADS) {
+        const int rl = q >> 4, c = c0 + (q & 15) * 4;
+        if (r0 + rl < e.rows && c < e.cols)
+          cp_async16(mst + rl * PT + (q & 15) * 4, e.mom + static_cast<long long>(r0 + rl) * e.ld + c);
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+  }
 
 #pragma unroll
   for (int pass = 0; pass < PT / 32; ++pass) {
@@ -93,7 +131,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
       if (vec && c + 7 < e.cols) {
         float g[8];
         if (e.gdtype == DT_BF16) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.g) + off);
+          const uint4 raw = *reinterpret_cast<const uint4*>(gst + rl * PT + tx * 8);
           const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -107,8 +145,8 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
           g[0] = f0.x; g[1] = f0.y; g[2] = f0.z; g[3] = f0.w; g[4] = f1.x; g[5] = f1.y; g[6] = f1.z; g[7] = f1.w;
         }
         if (e.mom != nullptr) {
-          const float4 m0 = *reinterpret_cast<const float4*>(e.mom + off);
-          const float4 m1 = *reinterpret_cast<const float4*>(e.mom + off + 4);
+          const float4 m0 = *reinterpret_cast<const float4*>(mst + rl * PT + tx * 8);
+          const float4 m1 = *reinterpret_cast<const float4*>(mst + rl * PT + tx * 8 + 4);
           const float mo[8] = {fmaf(mu, m0.x, g[0]), fmaf(mu, m0.y, g[1]), fmaf(mu, m0.z, g[2]), fmaf(mu, m0.w, g[3]),
                                fmaf(mu, m1.x, g[4]), fmaf(mu, m1.y, g[5]), fmaf(mu, m1.z, g[6]), fmaf(mu, m1.w, g[7])};
           *reinterpret_cast<float4*>(e.mom + off) = make_float4(mo[0], mo[1], mo[2], mo[3]);
@@ -173,30 +211,34 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
 
   if (e.transposed) {
     __syncthreads();
-    // X[c][r] = U[r][c]: thread (wx, wy) writes X rows c0+wy+16*pass, 4 consecutive r.
-    const int wx = threadIdx.x & 15, wy = threadIdx.x >> 4;
+    // X[c][r] = U[r][c]: thread (wx, wy) writes X rows c0+wy+32*pass, 8 consecutive r
+    // (16-byte hi stores; the column reads of the padded tile are free of bank conflicts)
+    const int wx = threadIdx.x & 7, wy = threadIdx.x >> 3;
 #pragma unroll
-    for (int pass = 0; pass < PT / 16; ++pass) {
-      const int cl = wy + 16 * pass;
+    for (int pass = 0; pass < PT / 32; ++pass) {
+      const int cl = wy + 32 * pass;
       const int c = c0 + cl;
-      const int r = r0 + wx * 4;
+      const int r = r0 + wx * 8;
       if (c < e.cols) {
-        float u[4];
+        float u[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) u[k] = tile[wx * 4 + k][cl];
+        for (int k = 0; k < 8; ++k) u[k] = tile[wx * 8 + k][cl];
         const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
-        if (r + 3 < e.rows) {
-          if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+        if (r + 7 < e.rows) {
+          if (p.xf != nullptr) {
+            *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+            *reinterpret_cast<float4*>(p.xf + xo + 4) = make_float4(u[4], u[5], u[6], u[7]);
+          }
           if (p.xb != nullptr) {
-            uint32_t hw[2], lw[2], l2w[2];
-            split_hi_lo(u, hw, lw, 2, l2w);
-            *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(hw[0], hw[1]);
-            if (p.xlo8 != nullptr) *reinterpret_cast<uint32_t*>(p.xlo8 + xo) = lo8_word(u);
-            if (p.xlo != nullptr) *reinterpret_cast<uint2*>(p.xlo + xo) = make_uint2(lw[0], lw[1]);
-            if (p.xlo2 != nullptr) *reinterpret_cast<uint2*>(p.xlo2 + xo) = make_uint2(l2w[0], l2w[1]);
+            uint32_t hw[4], lw[4], l2w[4];
+            split_hi_lo(u, hw, lw, 4, l2w);
+            *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            if (p.xlo8 != nullptr) *reinterpret_cast<uint2*>(p.xlo8 + xo) = make_uint2(lo8_word(u), lo8_word(u + 4));
+            if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            if (p.xlo2 != nullptr) *reinterpret_cast<uint4*>(p.xlo2 + xo) = make_uint4(l2w[0], l2w[1], l2w[2], l2w[3]);
           }
         } else {
-          for (int k = 0; k < 4 && r + k < e.rows; ++k) {
+          for (int k = 0; k < 8 && r + k < e.rows; ++k) {
             if (p.xf != nullptr) p.xf[xo + k] = u[k];
             if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
             if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
