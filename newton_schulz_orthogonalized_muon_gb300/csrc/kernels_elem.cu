@@ -68,6 +68,50 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// The NS working copy of 8 consecutive values u (16-byte aligned at xo)
+// and of one value.  kHiLo8: the bf16 tensor-core path's hi plane and lo
+// codes only (the planes of the other paths are neither computed nor
+// stored there); otherwise every plane the parameters name.
+template <bool kHiLo8>
+__device__ __forceinline__ void write_x8(const PrepParams& p, long long xo, const float* u) {
+  if constexpr (kHiLo8) {
+    uint32_t hw[4];
+    int q[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+      hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
+      q[2 * k] = lo8_code(__float_as_uint(u[2 * k]), hw[k] << 16);
+      q[2 * k + 1] = lo8_code(__float_as_uint(u[2 * k + 1]), hw[k] & 0xFFFF0000u);
+    }
+    *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint2*>(p.xlo8 + xo) =
+        make_uint2(pack_lo8x4(q[0], q[1], q[2], q[3]), pack_lo8x4(q[4], q[5], q[6], q[7]));
+  } else {
+    if (p.xf != nullptr) {
+      *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+      *reinterpret_cast<float4*>(p.xf + xo + 4) = make_float4(u[4], u[5], u[6], u[7]);
+    }
+    if (p.xb != nullptr) {
+      uint32_t hw[4], lw[4], l2w[4];
+      split_hi_lo(u, hw, lw, 4, l2w);
+      *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      if (p.xlo8 != nullptr) *reinterpret_cast<uint2*>(p.xlo8 + xo) = make_uint2(lo8_word(u), lo8_word(u + 4));
+      if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      if (p.xlo2 != nullptr) *reinterpret_cast<uint4*>(p.xlo2 + xo) = make_uint4(l2w[0], l2w[1], l2w[2], l2w[3]);
+    }
+  }
+}
+template <bool kHiLo8>
+__device__ __forceinline__ void write_x1(const PrepParams& p, long long xo, float u) {
+  if (!kHiLo8 && p.xf != nullptr) p.xf[xo] = u;
+  if (kHiLo8 || p.xb != nullptr) p.xb[xo] = f2bf(u);
+  if (!kHiLo8 && p.xlo != nullptr) p.xlo[xo] = f2bf(u - bf2f(f2bf(u)));
+  if (!kHiLo8 && p.xlo2 != nullptr) p.xlo2[xo] = third_plane(u);
+  if (kHiLo8 || p.xlo8 != nullptr) p.xlo8[xo] = static_cast<int8_t>(lo8_of(u));
+}
+
+template <bool kHiLo8>
 __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
   __shared__ float tile[PT][PT + 1];
   __shared__ float red[PREP_THREADS / 32];
@@ -181,26 +225,9 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
       if (r < e.rows) {
         const long long xo = xbase + static_cast<long long>(r) * p.ldx + c;
         if (c + 7 < e.cols) {
-          if (p.xf != nullptr) {
-            *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
-            *reinterpret_cast<float4*>(p.xf + xo + 4) = make_float4(u[4], u[5], u[6], u[7]);
-          }
-          if (p.xb != nullptr) {
-            uint32_t hw[4], lw[4], l2w[4];
-            split_hi_lo(u, hw, lw, 4, l2w);
-            *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            if (p.xlo8 != nullptr) *reinterpret_cast<uint2*>(p.xlo8 + xo) = make_uint2(lo8_word(u), lo8_word(u + 4));
-            if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            if (p.xlo2 != nullptr) *reinterpret_cast<uint4*>(p.xlo2 + xo) = make_uint4(l2w[0], l2w[1], l2w[2], l2w[3]);
-          }
+          write_x8<kHiLo8>(p, xo, u);
         } else {
-          for (int k = 0; k < 8 && c + k < e.cols; ++k) {
-            if (p.xf != nullptr) p.xf[xo + k] = u[k];
-            if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
-            if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
-            if (p.xlo2 != nullptr) p.xlo2[xo + k] = third_plane(u[k]);
-            if (p.xlo8 != nullptr) p.xlo8[xo + k] = static_cast<int8_t>(lo8_of(u[k]));
-          }
+          for (int k = 0; k < 8 && c + k < e.cols; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
         }
       }
     } else {
@@ -225,26 +252,9 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
         for (int k = 0; k < 8; ++k) u[k] = tile[wx * 8 + k][cl];
         const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
         if (r + 7 < e.rows) {
-          if (p.xf != nullptr) {
-            *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
-            *reinterpret_cast<float4*>(p.xf + xo + 4) = make_float4(u[4], u[5], u[6], u[7]);
-          }
-          if (p.xb != nullptr) {
-            uint32_t hw[4], lw[4], l2w[4];
-            split_hi_lo(u, hw, lw, 4, l2w);
-            *reinterpret_cast<uint4*>(p.xb + xo) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            if (p.xlo8 != nullptr) *reinterpret_cast<uint2*>(p.xlo8 + xo) = make_uint2(lo8_word(u), lo8_word(u + 4));
-            if (p.xlo != nullptr) *reinterpret_cast<uint4*>(p.xlo + xo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            if (p.xlo2 != nullptr) *reinterpret_cast<uint4*>(p.xlo2 + xo) = make_uint4(l2w[0], l2w[1], l2w[2], l2w[3]);
-          }
+          write_x8<kHiLo8>(p, xo, u);
         } else {
-          for (int k = 0; k < 8 && r + k < e.rows; ++k) {
-            if (p.xf != nullptr) p.xf[xo + k] = u[k];
-            if (p.xb != nullptr) p.xb[xo + k] = f2bf(u[k]);
-            if (p.xlo != nullptr) p.xlo[xo + k] = f2bf(u[k] - bf2f(f2bf(u[k])));
-            if (p.xlo2 != nullptr) p.xlo2[xo + k] = third_plane(u[k]);
-            if (p.xlo8 != nullptr) p.xlo8[xo + k] = static_cast<int8_t>(lo8_of(u[k]));
-          }
+          for (int k = 0; k < 8 && r + k < e.rows; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
         }
       }
     }
@@ -417,7 +427,9 @@ cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStrea
 cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s) {
   if (batch == 0 || tiles_per_mat == 0) return cudaSuccess;
   dim3 grid(tiles_per_mat, batch);
-  return launch_k(pdl_level() >= 2, muon_prepare_kernel, grid, dim3(PREP_THREADS), 0, s, p);
+  const bool hilo8 = p.xb != nullptr && p.xlo8 != nullptr && p.xf == nullptr && p.xlo == nullptr && p.xlo2 == nullptr;
+  if (hilo8) return launch_k(pdl_level() >= 2, muon_prepare_kernel<true>, grid, dim3(PREP_THREADS), 0, s, p);
+  return launch_k(pdl_level() >= 2, muon_prepare_kernel<false>, grid, dim3(PREP_THREADS), 0, s, p);
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
