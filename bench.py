@@ -802,14 +802,42 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             off += t.numel()
         return views
     link = host_link(dev, stream)
-    Gh = pinned_views(G)
-    for gh, gd in zip(Gh, G):
-        gh.copy_(gd)
+    # the gradients: one pinned host buffer and two device buffers, each laid
+    # out in the calls' slice order, so that a step's host-to-device transfer
+    # is one copy (per-tensor copies of the same bytes ran at 33-43 GB/s on
+    # machines whose link moved a 1 GiB buffer at 211 GB/s)
+    order = e2e_slices(specs, [w.numel() * w.element_size() for w in W])
+    seq = [i for idx in order for i in idx]
+    total = sum(G[i].numel() for i in seq)
+    gh_flat = torch.empty(total, dtype=G[0].dtype, pin_memory=True)
+    gd_flat = [torch.empty(total, dtype=G[0].dtype, device=dev) for _ in range(2)]
+    Gh, Gd = [None] * len(G), [[None] * len(G), [None] * len(G)]
+    off = 0
+    for i in seq:
+        n = G[i].numel()
+        Gh[i] = gh_flat[off:off + n].view(G[i].shape)
+        for q in range(2):
+            Gd[q][i] = gd_flat[q][off:off + n].view(G[i].shape)
+        off += n
+    for i in seq:
+        Gh[i].copy_(G[i])
     Wh = pinned_views(W)
     torch.cuda.synchronize()
     h2d = sum(g.numel() * g.element_size() for g in G)
     d2h = sum(w.numel() * w.element_size() for w in W)
     steps = max(1, args.steps)
+
+    def copy_in(q):
+        gd_flat[q].copy_(gh_flat, non_blocking=True)
+
+    # diagnostic: the same bytes as one copy per tensor, once, outside the timed loops
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_.record(stream)
+    for i in seq:
+        Gd[1][i].copy_(Gh[i], non_blocking=True)
+    b_.record(stream)
+    torch.cuda.synchronize()
+    link["h2d_gbs_per_tensor_copies"] = h2d / (a_.elapsed_time(b_) / 1e3) / 1e9
 
     def step(grads):
         pkg.muon_step(W, grads, M, lr=LR, wd=WD, mu=MU, nesterov=True, ns_method=args.ns_method, ns_steps=NS_STEPS,
@@ -823,11 +851,10 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     def serial_one(marks=None):
         if marks:
             marks[0].record(stream)
-        for gd, gh in zip(G, Gh):
-            gd.copy_(gh, non_blocking=True)
+        copy_in(0)
         if marks:
             marks[1].record(stream)
-        step(G)
+        step(Gd[0])
         if marks:
             marks[2].record(stream)
         for wh, wd in zip(Wh, W):
@@ -848,9 +875,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     d2h_ms = sum(m[2].elapsed_time(m[3]) for m in ev) / steps
 
     # pipelined: two device gradient buffers; calls per slice of a same-shape group
-    order = e2e_slices(specs, [w.numel() * w.element_size() for w in W])
-    G2 = [torch.empty_like(g) for g in G]
-    gbuf = [G, G2]
+    gbuf = Gd
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     in_done = [torch.cuda.Event(), torch.cuda.Event()]
     group_done = [torch.cuda.Event() for _ in order]
@@ -862,18 +887,15 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     s_in.wait_stream(stream)
     s_out.wait_stream(stream)
     with torch.cuda.stream(s_in):
-        for gd, gh in zip(gbuf[0], Gh):
-            gd.copy_(gh, non_blocking=True)
+        copy_in(0)
         in_done[0].record(s_in)
     for k in range(steps):
         cur = gbuf[k % 2]
         if k + 1 < steps:                               # next step's gradients, overlapped
-            nxt = gbuf[(k + 1) % 2]
             with torch.cuda.stream(s_in):
                 if k >= 1:
                     s_in.wait_event(step_done_prev)     # the buffer was read by step k-1
-                for gd, gh in zip(nxt, Gh):
-                    gd.copy_(gh, non_blocking=True)
+                copy_in((k + 1) % 2)
                 in_done[(k + 1) % 2].record(s_in)
         stream.wait_event(in_done[k % 2])
         for gi, idx in enumerate(order):
@@ -906,12 +928,13 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
         nbytes = torch.tensor([h2d, d2h], device=dev, dtype=torch.float64)
         dist.all_reduce(nbytes, op=dist.ReduceOp.SUM)
         h2d, d2h = int(nbytes[0]), int(nbytes[1])
-    del G2
+    del gd_flat, Gd, gbuf
     torch.cuda.empty_cache()
     return {"value": alg_all / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "mode": f"pipelined (copies overlapped with compute; {len(order)} calls per step, one per slice of at most "
-                    f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group)",
+                    f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group; the gradients in one "
+                    f"host-to-device copy, the parameters read back per tensor)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
             "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_link": link}
 
