@@ -781,8 +781,9 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     "pipelined" (the reported value): the step is issued as several
     muon_step calls, one per slice of at most E2E_SLICE_BYTES of parameters
     within a same-shape group, groups in the library's order (ascending
-    (m, n)); the gradients of step k+1 are copied in on one side stream while
-    step k computes, and each slice's parameters are read back on another
+    (m, n)); the gradients of step k+1 are copied in on one side stream, one
+    copy per slice, while step k computes (a call waits for its own slice's
+    gradients only), and each slice's parameters are read back on another
     side stream as soon as that slice's call has finished, while the later
     slices compute.  Step k+1's call for a slice waits for the read-back of
     the same slice from step k (it overwrites those parameters), so no device
@@ -827,8 +828,19 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     d2h = sum(w.numel() * w.element_size() for w in W)
     steps = max(1, args.steps)
 
-    def copy_in(q):
-        gd_flat[q].copy_(gh_flat, non_blocking=True)
+    # element range of each slice in the flat layout
+    bounds, off = [], 0
+    for idx in order:
+        n = sum(G[i].numel() for i in idx)
+        bounds.append((off, off + n))
+        off += n
+
+    def copy_in(q, gi=None):
+        if gi is None:
+            gd_flat[q].copy_(gh_flat, non_blocking=True)
+        else:
+            a, b = bounds[gi]
+            gd_flat[q][a:b].copy_(gh_flat[a:b], non_blocking=True)
 
     # diagnostic: the same bytes as one copy per tensor, once, outside the timed loops
     a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -877,7 +889,9 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     # pipelined: two device gradient buffers; calls per slice of a same-shape group
     gbuf = Gd
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    in_done = [torch.cuda.Event(), torch.cuda.Event()]
+    # per buffer and slice: that slice's gradients have arrived, so a step's
+    # first call waits for its own slice only
+    in_done = [[torch.cuda.Event() for _ in order] for _ in range(2)]
     group_done = [torch.cuda.Event() for _ in order]
     out_done = [torch.cuda.Event() for _ in order]
     torch.cuda.synchronize()
@@ -887,18 +901,20 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     s_in.wait_stream(stream)
     s_out.wait_stream(stream)
     with torch.cuda.stream(s_in):
-        copy_in(0)
-        in_done[0].record(s_in)
+        for gi in range(len(order)):
+            copy_in(0, gi)
+            in_done[0][gi].record(s_in)
     for k in range(steps):
         cur = gbuf[k % 2]
         if k + 1 < steps:                               # next step's gradients, overlapped
             with torch.cuda.stream(s_in):
                 if k >= 1:
                     s_in.wait_event(step_done_prev)     # the buffer was read by step k-1
-                copy_in((k + 1) % 2)
-                in_done[(k + 1) % 2].record(s_in)
-        stream.wait_event(in_done[k % 2])
+                for gi in range(len(order)):
+                    copy_in((k + 1) % 2, gi)
+                    in_done[(k + 1) % 2][gi].record(s_in)
         for gi, idx in enumerate(order):
+            stream.wait_event(in_done[k % 2][gi])       # this slice's gradients are in
             if k >= 1:
                 stream.wait_event(out_done[gi])         # step k-1's parameters of this group are read back
             pkg.muon_step([W[i] for i in idx], [cur[i] for i in idx], [M[i] for i in idx], lr=LR, wd=WD, mu=MU,
@@ -934,7 +950,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
             "d2h_bytes_per_step": d2h, "steps": steps,
             "mode": f"pipelined (copies overlapped with compute; {len(order)} calls per step, one per slice of at most "
                     f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group; the gradients in one "
-                    f"host-to-device copy, the parameters read back per tensor)",
+                    f"host-to-device copy per slice, the parameters read back per tensor)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
             "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_link": link}
 
