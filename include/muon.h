@@ -62,8 +62,12 @@ typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype_t;
 
 /* Newton-Schulz method: "standard" iterates on X; "gram" iterates on the
  * small square R = XX^T and applies the accumulated polynomial to X0 once
- * (DeepSpeed's NS_METHODS {standard, gram}). */
-typedef enum { MUON_NS_STANDARD = 0, MUON_NS_GRAM = 1 } muon_ns_method_t;
+ * (DeepSpeed's NS_METHODS {standard, gram}).  MUON_NS_AUTO (no counterpart
+ * on the pages) chooses per same-shape group, after the rows <= cols rule:
+ * gram on the bf16 path when n >= 4m, where it measured faster on this GPU,
+ * standard otherwise and on the fp32 paths; a call with both kinds of
+ * group runs as two calls in turn on the same stream. */
+typedef enum { MUON_NS_STANDARD = 0, MUON_NS_GRAM = 1, MUON_NS_AUTO = 2 } muon_ns_method_t;
 
 typedef struct muon_handle_s* muon_handle_t;
 

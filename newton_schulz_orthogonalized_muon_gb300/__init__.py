@@ -10,6 +10,7 @@ __version__ = "1.0.0"
 _BINDING_NAMES = ("MuonHandle", "MuonError", "muon_orthogonalize", "muon_orthogonalize_noalloc", "noalloc_check", "muon_step", "adamw_step",
                   "workspace_size", "default_handle", "MUON_SCALE_RMS", "MUON_SCALE_MUP",
                   "load_library", "selftest_timeout", "MUON_F32", "MUON_BF16", "MUON_NS_STANDARD", "MUON_NS_GRAM",
+                  "MUON_NS_AUTO",
                   "QUINTIC", "EXPORTS")
 
 

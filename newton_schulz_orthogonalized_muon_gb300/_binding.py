@@ -17,7 +17,7 @@ import torch
 from ._build import LIB_PATH
 
 MUON_F32, MUON_BF16 = 0, 1
-MUON_NS_STANDARD, MUON_NS_GRAM = 0, 1
+MUON_NS_STANDARD, MUON_NS_GRAM, MUON_NS_AUTO = 0, 1, 2
 MUON_SCALE_RMS, MUON_SCALE_MUP = 0, 1
 QUINTIC = (3.4445, -4.7750, 2.0315)
 
@@ -138,6 +138,8 @@ def _method(ns_method) -> int:
         return MUON_NS_STANDARD
     if ns_method in ("gram", MUON_NS_GRAM):
         return MUON_NS_GRAM
+    if ns_method in ("auto", MUON_NS_AUTO):
+        return MUON_NS_AUTO
     raise ValueError(f"unknown ns_method {ns_method!r}")
 
 

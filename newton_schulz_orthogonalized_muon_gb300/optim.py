@@ -69,7 +69,7 @@ class Muon:
     ``named_params``: ``model.named_parameters()`` (or any ``(name, tensor)``
     pairs of contiguous CUDA tensors, fp32 or bf16).  Muon hyper-parameters
     follow ``muon_step``: ``lr``, ``wd`` (decoupled), ``momentum``,
-    ``nesterov``, ``ns_steps``, ``ns_method`` ("standard" | "gram"),
+    ``nesterov``, ``ns_steps``, ``ns_method`` ("standard" | "gram" | "auto"),
     ``update_rms`` (0.2: the update RMS matched to AdamW's); ``split_heads``
     maps a parameter name to its Muon-Split head count; ``higher_rank`` sends
     parameters with more than two dimensions to the Muon step (see the

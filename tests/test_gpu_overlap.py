@@ -100,3 +100,41 @@ def test_concurrent_groups_match_serial_bitwise(dtype, limit_mb):
     if limit_mb == 4096:                 # regions side by side
         assert need > pkg.workspace_size(shapes, split_heads=split, ns_dtype=dtype, handle=serial)
 
+
+
+@pytest.mark.parametrize("limit_mb", [2, 4096])
+def test_auto_method_matches_the_two_methods_bitwise(limit_mb):
+    # ns_method="auto": the wide groups (n >= 4m) take the Gram method and
+    # the others the standard one; each must equal a call with that method
+    # alone bit for bit, and the workspace planned for auto covers both
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import newton_schulz_orthogonalized_muon_gb300 as pkg
+    torch.cuda.set_device(0)
+    h = pkg.MuonHandle(0)
+    h.set_workspace_limit(limit_mb << 20)
+    wide = [wl.ParamSpec("w1", (256, 1024)), wl.ParamSpec("w2", (1536, 384)), wl.ParamSpec("w3", (128, 1024))]
+    square = [wl.ParamSpec("s1", (512, 1024)), wl.ParamSpec("s2", (384, 384)), wl.ParamSpec("s3", (700, 1400))]
+    specs = wide + square
+    W0 = [torch.tensor(wl.weight(1200 + i, s.shape)).to(torch.bfloat16) for i, s in enumerate(specs)]
+    G = [torch.tensor(wl.lowrank_grad(1300 + i, s.shape[0], s.shape[1], 16)).to(torch.bfloat16).cuda()
+         for i, s in enumerate(specs)]
+
+    def run(idx, method):
+        W = [W0[i].clone().cuda() for i in idx]
+        M = [torch.zeros(specs[i].shape, device="cuda") for i in idx]
+        pkg.muon_step(W, [G[i] for i in idx], M, lr=0.02, wd=0.1, ns_method=method, handle=h)
+        torch.cuda.synchronize()
+        assert h.check() == 0
+        return [w.cpu() for w in W], [m.cpu() for m in M]
+
+    n_w = len(wide)
+    w_all, m_all = run(list(range(len(specs))), "auto")
+    w_g, m_g = run(list(range(n_w)), "gram")
+    w_s, m_s = run(list(range(n_w, len(specs))), "standard")
+    for a, b in zip(w_all + m_all, w_g + w_s + m_g + m_s):
+        assert torch.equal(a, b)
+    shapes = [s.shape for s in specs]
+    need = pkg.workspace_size(shapes, ns_method="auto", handle=h)
+    assert need == max(pkg.workspace_size([s.shape for s in wide], ns_method="gram", handle=h),
+                       pkg.workspace_size([s.shape for s in square], ns_method="standard", handle=h))
