@@ -895,6 +895,8 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     group_done = [torch.cuda.Event() for _ in order]
     out_done = [torch.cuda.Event() for _ in order]
     torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -932,6 +934,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
     stream.wait_stream(s_in)
     t1.record(stream)
     torch.cuda.synchronize()
+    e2e_clk = clocks.stop()
     ms = t0.elapsed_time(t1) / steps
     if world > 1:
         import torch.distributed as dist
@@ -952,7 +955,7 @@ def run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
                     f"{E2E_SLICE_BYTES >> 30} GiB of parameters of one same-shape group; the gradients in one "
                     f"host-to-device copy per slice, the parameters read back per tensor)",
             "serial_ms_per_step": serial_ms, "serial_value": alg_all / (serial_ms / 1e3) / 1e12,
-            "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_link": link}
+            "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "host_link": link, "clocks": e2e_clk}
 
 
 def param_dtype(args):
