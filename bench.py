@@ -976,24 +976,26 @@ def kernel_mode(method, kernel_class, fp32=False):
 
 def uses_pairs(m, kernel_class, method="standard"):
     """The library's rule for which products run on the CTA-pair kernels.
-    Standard method: symmetric products when m is a multiple of 256 or
-    m >= MUON_TC_PAIR_MIN_M (1024 by default); UPDATE / FINAL when m is a
-    multiple of 256 or m >= 2048.  Gram method: its symmetric products
-    (R0, P, the m x m products) by the same rule; O = Q X0 always on one
+    A group uses pairs when m >= MUON_TC_PAIR_MIN_M (1024 by default) or
+    m = 256.  Standard method: its symmetric products then; UPDATE / FINAL
+    when, in addition, m is a multiple of 256 or m >= 2048.  Gram method: its
+    symmetric products (R0, P, the m x m products); O = Q X0 always on one
     SM.  None with MUON_TC_PAIR=0, symmetric products only with
     MUON_TC_PAIR=sym."""
     env = os.environ.get("MUON_TC_PAIR")
     if env == "0" or m < 256:
         return False
-    if method == "gram" and kernel_class == "final":
-        return False
-    if method == "standard" and kernel_class in ("update", "final"):
-        return env != "sym" and (m % 256 == 0 or m >= 2048)
     try:
         min_m = int(os.environ.get("MUON_TC_PAIR_MIN_M", "1024"))
     except ValueError:
         min_m = 1024
-    return m % 256 == 0 or m >= min_m
+    if not (m >= min_m or m == 256):
+        return False
+    if method == "gram" and kernel_class == "final":
+        return False
+    if method == "standard" and kernel_class in ("update", "final"):
+        return env != "sym" and (m % 256 == 0 or m >= 2048)
+    return True
 
 
 def kernel_source_hash():

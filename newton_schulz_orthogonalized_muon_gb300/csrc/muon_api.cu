@@ -310,7 +310,12 @@ std::vector<int2> sym_tiles(int m, int bn, int bm = 128) {
 
 // Groups whose m fills 256-row pair tiles well run on the CTA-pair kernels:
 // m a multiple of 256, or m >= pair_min_m (ragged last tile).
-bool pair_group(int m, int pair_min_m) { return m >= 256 && (m % 256 == 0 || m >= pair_min_m); }
+// CTA pairs from m = pair_min_m (1024 by default, MUON_TC_PAIR_MIN_M), and
+// for m = 256 (one 256-row block, whose pair tiles halve the per-SM traffic
+// of the wide X panels: 64 matrices 256 x 16384, 2.74 against 2.78 ms on
+// one SM).  Between them the one-SM kernels won: GPT-2-small (m = 768)
+// 1.515 -> 1.495 ms.
+bool pair_group(int m, int pair_min_m) { return m >= 256 && (m >= pair_min_m || m == 256); }
 
 struct GroupPlan {
   int m = 0, n = 0;

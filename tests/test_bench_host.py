@@ -47,8 +47,8 @@ def test_e2e_slices_keep_transposed_partners_in_their_group():
 
 @pytest.mark.parametrize("m,kernel,pair", [
     (4096, "update", True), (4096, "syrk", True), (1408, "syrk", True), (1408, "update", False),
-    (1408, "final", False), (2176, "update", True), (768, "update", True), (640, "syrk", False),
-    (128, "syrk", False)])
+    (1408, "final", False), (2176, "update", True), (768, "update", False), (768, "syrk", False),
+    (256, "update", True), (256, "syrk", True), (640, "syrk", False), (128, "syrk", False)])
 def test_pair_rule_matches_the_library(m, kernel, pair, monkeypatch):
     monkeypatch.delenv("MUON_TC_PAIR", raising=False)
     monkeypatch.delenv("MUON_TC_PAIR_MIN_M", raising=False)

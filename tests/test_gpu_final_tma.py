@@ -45,7 +45,8 @@ def handles():
     import newton_schulz_orthogonalized_muon_gb300 as pkg
     torch.cuda.set_device(0)
     return pkg, {
-        "pair": (_handle(pkg), _handle(pkg, MUON_FINAL_TMA="0")),
+        # pairs from m = 256, so that the 512-row group runs on them too
+        "pair": (_handle(pkg, MUON_TC_PAIR_MIN_M="256"), _handle(pkg, MUON_TC_PAIR_MIN_M="256", MUON_FINAL_TMA="0")),
         "single": (_handle(pkg, MUON_TC_PAIR="0"), _handle(pkg, MUON_TC_PAIR="0", MUON_FINAL_TMA="0")),
     }
 

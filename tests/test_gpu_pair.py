@@ -1,7 +1,9 @@
 """CTA-pair tensor-core kernels (tcgen05 cta_group::2, 256 x 256 tiles).
 
-Groups whose m is a multiple of 256 (or >= 2048) run on the pair kernels;
-a handle created with MUON_TC_PAIR=0 runs the one-CTA kernels.  Both are
+A handle created with MUON_TC_PAIR_MIN_M=256 runs every product of a group
+with m >= 256 on the pair kernels (UPDATE / FINAL when m is a multiple of
+256 or m >= 2048); a handle created with MUON_TC_PAIR=0 runs the one-CTA
+kernels.  Both are
 compared with the fp64 oracle, and with each other, on the same inputs,
 including ragged n, a ragged last 256-row tile (m = 2176), transposed
 matrices and batches.
@@ -30,7 +32,16 @@ def handles():
         pytest.skip("no CUDA device")
     import newton_schulz_orthogonalized_muon_gb300 as pkg
     torch.cuda.set_device(0)
-    pair = pkg.MuonHandle(0)
+    # pairs from m = 256 (the default starts them at m = 1024, and at 256)
+    old_min = os.environ.get("MUON_TC_PAIR_MIN_M")
+    os.environ["MUON_TC_PAIR_MIN_M"] = "256"
+    try:
+        pair = pkg.MuonHandle(0)
+    finally:
+        if old_min is None:
+            del os.environ["MUON_TC_PAIR_MIN_M"]
+        else:
+            os.environ["MUON_TC_PAIR_MIN_M"] = old_min
     old = os.environ.get("MUON_TC_PAIR")
     os.environ["MUON_TC_PAIR"] = "0"
     try:
