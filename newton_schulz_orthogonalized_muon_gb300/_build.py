@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmuon_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["muon_api.cu", "kernels_tc.cu", "kernels_tc2.cu", "kernels_elem.cu", "kernels_simt.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "internal.h", "tc_common.cuh"]
+HEADERS = ["common.cuh", "internal.h", "tc_common.cuh", "launch_opts.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE]
 

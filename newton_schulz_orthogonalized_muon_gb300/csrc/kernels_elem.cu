@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch_opts.h"
 
 namespace muon {
 
@@ -416,20 +417,29 @@ int pdl_level() {
   return level;
 }
 
+namespace {
+thread_local bool g_elem_pdl = false;
+}
+void set_elementwise_pdl(bool on) { g_elem_pdl = on; }
+bool elementwise_pdl() { return g_elem_pdl; }
+// the element-wise kernels' launches: with PDL at level 2, or at level 1
+// when the calling thread's current call asked for it
+static bool elem_pdl() { return pdl_level() >= 2 || (pdl_level() == 1 && g_elem_pdl); }
+
 cudaError_t launch_desc_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
   const size_t n16 = bytes / 16;
   if (n16 == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<size_t>((n16 + threads - 1) / threads, 1024));
-  return launch_k(pdl_level() >= 2, desc_copy_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(dst),
+  return launch_k(elem_pdl(), desc_copy_kernel, dim3(blocks), dim3(threads), 0, s, static_cast<uint4*>(dst),
                   static_cast<const uint4*>(src), n16);
 }
 cudaError_t launch_prepare(const PrepParams& p, int batch, int tiles_per_mat, cudaStream_t s) {
   if (batch == 0 || tiles_per_mat == 0) return cudaSuccess;
   dim3 grid(tiles_per_mat, batch);
   const bool hilo8 = p.xb != nullptr && p.xlo8 != nullptr && p.xf == nullptr && p.xlo == nullptr && p.xlo2 == nullptr;
-  if (hilo8) return launch_k(pdl_level() >= 2, muon_prepare_kernel<true>, grid, dim3(PREP_THREADS), 0, s, p);
-  return launch_k(pdl_level() >= 2, muon_prepare_kernel<false>, grid, dim3(PREP_THREADS), 0, s, p);
+  if (hilo8) return launch_k(elem_pdl(), muon_prepare_kernel<true>, grid, dim3(PREP_THREADS), 0, s, p);
+  return launch_k(elem_pdl(), muon_prepare_kernel<false>, grid, dim3(PREP_THREADS), 0, s, p);
 }
 
 cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int batch, float eps, float* scale,
@@ -437,7 +447,7 @@ cudaError_t launch_norm_finalize(const float* partials, int tiles_per_mat, int b
   if (batch == 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = (batch * 32 + threads - 1) / threads;
-  return launch_k(pdl_level() >= 2, norm_finalize_kernel, dim3(blocks), dim3(threads), 0, s, partials, tiles_per_mat, batch, eps, scale,
+  return launch_k(elem_pdl(), norm_finalize_kernel, dim3(blocks), dim3(threads), 0, s, partials, tiles_per_mat, batch, eps, scale,
                   err);
 }
 
@@ -447,12 +457,12 @@ cudaError_t launch_apply(const ApplyParams& p, int batch, cudaStream_t s) {
   int bx = static_cast<int>((total + 255) / 256);
   if (bx > 1024) bx = 1024;
   if (bx < 1) bx = 1;
-  return launch_k(pdl_level() >= 2, apply_kernel, dim3(bx, batch), dim3(256), 0, s, p);
+  return launch_k(elem_pdl(), apply_kernel, dim3(bx, batch), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_adamw(const AdamParams& p, int n_chunks, cudaStream_t s) {
   if (n_chunks == 0) return cudaSuccess;
-  return launch_k(pdl_level() >= 2, adamw_kernel, dim3(n_chunks), dim3(256), 0, s, p);
+  return launch_k(elem_pdl(), adamw_kernel, dim3(n_chunks), dim3(256), 0, s, p);
 }
 
 cudaError_t launch_wait_selftest(unsigned long long timeout_ns, unsigned* err, cudaStream_t s) {
