@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   using C = Cfg<MODE, BN, AP, BP>;
   using L = EpiLayout<MODE, OneSlots<MODE>::v>;
   constexpr bool kUpd = ModeTraits<MODE>::kMN;
-  constexpr bool kSym = ModeTraits<MODE>::kSym;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;                 // 1024-aligned
