@@ -1026,9 +1026,9 @@ def uses_pairs(m, kernel_class, method="standard"):
     A group uses pairs when m >= MUON_TC_PAIR_MIN_M (1024 by default) or
     m = 256.  Standard method: its symmetric products then; UPDATE / FINAL
     when, in addition, m is a multiple of 256 or m >= 2048.  Gram method: its
-    symmetric products (R0, P, the m x m products); O = Q X0 always on one
-    SM.  None with MUON_TC_PAIR=0, symmetric products only with
-    MUON_TC_PAIR=sym."""
+    symmetric products (R0, P, the m x m products), and O = Q X0 into bf16
+    destinations by the UPDATE rule.  None with MUON_TC_PAIR=0, symmetric
+    products only with MUON_TC_PAIR=sym."""
     env = os.environ.get("MUON_TC_PAIR")
     if env == "0" or m < 256:
         return False
@@ -1038,9 +1038,7 @@ def uses_pairs(m, kernel_class, method="standard"):
         min_m = 1024
     if not (m >= min_m or m == 256):
         return False
-    if method == "gram" and kernel_class == "final":
-        return False
-    if method == "standard" and kernel_class in ("update", "final"):
+    if (method == "standard" and kernel_class in ("update", "final")) or (method == "gram" and kernel_class == "final"):
         return env != "sym" and (m % 256 == 0 or m >= 2048)
     return True
 

@@ -211,6 +211,11 @@ cudaError_t launch_ns_gemm_pair(int mode, const CUtensorMap& map_a, const CUtens
 cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                       const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
                                       const NsGemmParams& p, int pairs, cudaStream_t s, int slots = 0);
+// The Gram method's last product O = s Q X0 into bf16 destinations on CTA
+// pairs (MODE_G_FINAL_T): a0 / a1 Q's hi and lo planes (128-row boxes), b X0
+// read MN-major (64 x 64 boxes); 256 x 256 tiles as for UPDATE.
+cudaError_t launch_ns_gemm_pair_gram_final(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                                           const NsGemmParams& p, int pairs, cudaStream_t s);
 cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
                                       const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& so,
                                       const CUtensorMap& so_lo, const NsGemmParams& p, int pairs, cudaStream_t s);

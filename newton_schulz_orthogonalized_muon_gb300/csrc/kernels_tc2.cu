@@ -72,7 +72,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   // block with at most 128 valid columns runs N = 128, each CTA loading 64
   // rows of B through map_b1 (the same operand with 64-row boxes)
   constexpr bool kN128 = ModeTraits<MODE>::kSym && BP == 1;
-  static_assert(MODE != MODE_G_FINAL && MODE != MODE_G_FINAL_T, "G_FINAL runs on the one-CTA kernel");
+  static_assert(MODE != MODE_G_FINAL, "the element-wise G_FINAL runs on the one-CTA kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;                 // 1024-aligned
@@ -362,6 +362,12 @@ cudaError_t launch_ns_gemm_pair_update(int mode, const CUtensorMap& a, const CUt
     case MODE_FINAL_T: return launch_pair<MODE_FINAL_T, 1, 1>(a, a, b, b, xh, xl, xo, p, pairs, s);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ns_gemm_pair_gram_final(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                                           const NsGemmParams& p, int pairs, cudaStream_t s) {
+  if (p.num_tiles == 0) return cudaSuccess;
+  return launch_pair<MODE_G_FINAL_T, 2, 1>(a0, a1, b, b, b, b, b, p, pairs, s);
 }
 
 cudaError_t launch_ns_gemm_pair_planes(int mode, const CUtensorMap& a0, const CUtensorMap& a1,

@@ -579,7 +579,16 @@ muon_status_t run_gram_group(muon_handle_t h, const GroupPlan& g, const Regions&
     f.scale = scale;
     f.sym_in = hi[qcur];
     f.wmap = wmap_d;
-    if (tc) {
+    if (tc && wmap_d != nullptr && g.pair_upd) {
+      // on CTA pairs, 256 x 256 tiles, as the standard method's UPDATE
+      const int mi2 = static_cast<int>(ceil_div(g.m, 256)), nj2 = static_cast<int>(ceil_div(g.n, 256));
+      f.mi = mi2;
+      f.tiles_per_mat = mi2 * nj2;
+      f.num_tiles = cnt * mi2 * nj2;
+      const int pairs = std::min(f.num_tiles, h->max_pairs);
+      MUON_LAUNCH(MUON_K_FINAL, launch_ns_gemm_pair_gram_final(mhi[qcur], mlo[qcur], map_xmn, f, pairs, stream),
+                  "gram final");
+    } else if (tc) {
       f.mi = mi;
       f.tiles_per_mat = mi * nj;
       f.num_tiles = cnt * mi * nj;

@@ -56,11 +56,11 @@ def test_pair_rule_matches_the_library(m, kernel, pair, monkeypatch):
 
 
 @pytest.mark.parametrize("m,kernel,pair", [
-    (4096, "syrk", True), (4096, "poly", True), (4096, "update", True), (4096, "final", False),
-    (1408, "update", True), (640, "update", False)])
+    (4096, "syrk", True), (4096, "poly", True), (4096, "update", True), (4096, "final", True),
+    (1408, "update", True), (1408, "final", False), (640, "update", False)])
 def test_gram_pair_rule_matches_the_library(m, kernel, pair, monkeypatch):
     # the Gram method runs R0, P and its m x m products on pairs by the
-    # symmetric-product rule, and O = Q X0 on one SM
+    # symmetric-product rule, and O = Q X0 by the UPDATE rule
     monkeypatch.delenv("MUON_TC_PAIR", raising=False)
     monkeypatch.delenv("MUON_TC_PAIR_MIN_M", raising=False)
     assert bench.uses_pairs(m, kernel, "gram") is pair
