@@ -536,7 +536,7 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host grads in, params out
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world)
+        e2e = run_e2e_bounded(args, W, G, M, specs, split, h, dev, stream, alg_all, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -770,6 +770,57 @@ def host_link(dev, stream):
         out["process_cpus"] = len(os.sched_getaffinity(0))
     except Exception:
         pass
+    return out
+
+
+def host_memory_bytes():
+    """Physical memory of this machine (Linux), or None."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemTotal:"):
+                return int(line.split()[1]) * 1024
+    except Exception:
+        pass
+    return None
+
+
+def e2e_subset(specs, param_bytes, frac):
+    """Indices of the first ceil-down fraction `frac` (at least one) of each
+    same-shape group's matrices, in the library's group order."""
+    keep = []
+    for idx in e2e_slices(specs, param_bytes, limit=1 << 62, last_limit=1 << 62):
+        keep += idx[:max(1, int(len(idx) * frac))]
+    return sorted(keep)
+
+
+def run_e2e_bounded(args, W, G, M, specs, split, h, dev, stream, alg_all, world):
+    """run_e2e over the whole set when its host buffers (gradients in,
+    parameters out: twice the set's gradient bytes per rank) fit in half of
+    the machine's memory shared by the ranks on it; otherwise over the first
+    matrices of each same-shape group, the same fraction of every group, with
+    the flop count of that subset summed over the ranks, and the fraction in
+    the result (several ranks of a large set on one machine)."""
+    import torch
+    need = 2 * sum(g.numel() * g.element_size() for g in G) + (1 << 30)
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    mem = host_memory_bytes()
+    if mem is None or need <= 0.5 * mem / max(local, 1):
+        return run_e2e(args, W, G, M, specs, split, h, dev, stream, alg_all, world)
+    frac = 0.5 * mem / max(local, 1) / need
+    keep = e2e_subset(specs, [w.numel() * w.element_size() for w in W], frac)
+    from newton_schulz_orthogonalized_muon_gb300 import flops
+    sub = [specs[i] for i in keep]
+    alg, _ = flops.set_flops(sub, NS_STEPS, args.ns_method)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([alg], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        alg = float(t.item())
+    out = run_e2e(args, [W[i] for i in keep], [G[i] for i in keep], [M[i] for i in keep], sub,
+                  [split[i] for i in keep], h, dev, stream, alg, world)
+    out["subset"] = {"matrices_per_rank": len(keep), "of": len(specs), "reason":
+                     f"host memory: {need / 1e9:.0f} GB of buffers per rank against {mem / 1e9:.0f} GB shared by "
+                     f"{local} ranks"}
     return out
 
 

@@ -98,3 +98,15 @@ def test_e2e_last_slice_is_small():
     # a last group smaller than the limit is not cut
     small = [wl.ParamSpec(f"p{i}", (64, 128)) for i in range(10)]
     assert bench.e2e_slices(small, _bytes(small)) == [list(range(10))]
+
+
+def test_e2e_subset_takes_the_same_fraction_of_every_group():
+    # the bounded e2e keeps the first matrices of each same-shape group
+    specs = ([wl.ParamSpec(f"a{i}", (1024, 4096)) for i in range(8)] +
+             [wl.ParamSpec(f"b{i}", (4096, 1024)) for i in range(4)] +     # transposed: same group as a
+             [wl.ParamSpec(f"c{i}", (512, 512)) for i in range(10)])
+    keep = bench.e2e_subset(specs, _bytes(specs), 0.5)
+    assert keep == sorted([0, 1, 2, 3, 4, 5] + list(range(12, 17)))
+    assert bench.e2e_subset(specs, _bytes(specs), 0.01) == [0, 12]        # at least one per group
+    assert bench.e2e_subset(specs, _bytes(specs), 1.0) == list(range(len(specs)))
+
