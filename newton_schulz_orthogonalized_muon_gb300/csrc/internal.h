@@ -91,8 +91,9 @@ struct AdamParams {
 // ------------------------------------------------ Newton-Schulz GEMMs
 // Modes of the NS GEMM kernels (tensor-core path; P^ = bf16(P), X^ = bf16(X)):
 //   SYRK   A = s^2 * X^ X^^T                 (symmetric, upper tiles, mirrored)
-//   POLY   P = a*I + b*A + c*A A             (symmetric; fp32 diagonal kept aside)
-//   UPDATE X' = s*(P^ X^ + P_rr X - P^_rr X^)   (fp32 master + bf16 operand copy)
+//   POLY   P = s*(a*I + b*A + c*A A)         (symmetric; fp32 diagonal kept aside;
+//                                             s only in the first iteration)
+//   UPDATE X' = P^ X^ + P_rr X - P^_rr X^    (master X = hi + lo, hi the bf16 operand)
 //   FINAL  out = alpha*out + beta*X'         (parameter or caller matrix)
 // The fp32 path (CUDA cores) evaluates the same iteration as
 //   SYRK A = s^2 X X^T, POLY B = b*A + c*A A, UPDATE X' = s*(a*X + B X).
@@ -181,9 +182,10 @@ cudaError_t launch_ns_gemm_tc(int mode, int bn, const CUtensorMap& map_a, const 
                               const CUtensorMap& map_so, const CUtensorMap& map_so_lo, const NsGemmParams& p,
                               int grid, cudaStream_t s);
 // UPDATE / FINAL: the master X is hi + lo, hi being the bf16 operand copy.
-// map_xh: hi plane of this iteration (= the B operand), map_xl: lo plane
-// (updated in place), map_xo: hi plane of the next iteration (UPDATE); all
-// bf16 with 32 x 32 boxes from encode_box32.
+// map_xh: hi plane of this iteration (= the B operand), map_xl: lo plane of
+// signed-byte codes (updated in place), map_xo: hi plane of the next
+// iteration (UPDATE); 32 x 32 boxes from encode_box32 (bf16 planes) and
+// encode_lo8_box32 (the lo plane).
 cudaError_t launch_ns_gemm_tc_update(int mode, int bn, const CUtensorMap& map_a, const CUtensorMap& map_b,
                                      const CUtensorMap& map_xh, const CUtensorMap& map_xl, const CUtensorMap& map_xo,
                                      const NsGemmParams& p, int grid, cudaStream_t s);
