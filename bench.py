@@ -489,7 +489,9 @@ def run_ours(args):
             try:
                 entry = json.load(open(tpath)).get(ws.name, {}).get(f"{top['mode']}@{top['group']}")
                 if entry and entry.get("kernel_source_hash") == kernel_source_hash():
-                    traffic = entry.get("bytes_per_launch")
+                    # per-matrix traffic (each matrix's tiles touch only that
+                    # matrix) times this launch's matrices
+                    traffic = entry["bytes_per_launch"] * top["matrices"] / entry.get("matrices", top["matrices"])
             except Exception:
                 traffic = None
         m_top = int(top["group"].split("x")[0])
