@@ -1174,8 +1174,8 @@ bool valid_method(int32_t m) { return m == MUON_NS_STANDARD || m == MUON_NS_GRAM
 
 // MUON_NS_AUTO: the Gram method for a same-shape group whose n is at least
 // kAutoGramRatio times its m (bf16 path), where it measured faster than the
-// standard method (64 bf16 matrices each: 1024 x 4096 1.08x, 2048 x 16384
-// 1.46x, 256 x 4096 1.84x; 2048 x 4096 0.60x); the standard method otherwise.
+// standard method (64 bf16 matrices each: 1024 x 4096 1.02x, 2048 x 16384
+// 1.43x, 256 x 4096 1.77x; 2048 x 4096 0.60x); the standard method otherwise.
 constexpr int64_t kAutoGramRatio = 4;
 bool auto_gram(const Block& b, bool tc) { return tc && static_cast<int64_t>(b.n) >= kAutoGramRatio * b.m; }
 
