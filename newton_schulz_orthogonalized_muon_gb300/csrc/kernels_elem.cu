@@ -114,7 +114,18 @@ __device__ __forceinline__ void write_x1(const PrepParams& p, long long xo, floa
 
 template <bool kHiLo8>
 __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
-  __shared__ float tile[PT][PT + 1];
+  // transpose tile: fp32 U (padded rows) for the generic instance; for the
+  // bf16 path the encoded hi bits (64 x 64 bf16) and lo codes (64 x 64
+  // bytes), 12 KB, so six blocks fit on an SM.  Their rows are split into
+  // eight 8-column chunks whose order is XORed with the row's 8-row band:
+  // the row pass stores a chunk as one 16-byte (hi) and one 8-byte (codes)
+  // store, and the column pass's lanes, which read rows of eight bands at
+  // once, fall in distinct banks.
+  constexpr int TILE_BYTES = kHiLo8 ? PT * PT * 3 : PT * (PT + 1) * 4;
+  __shared__ __align__(16) uint8_t tbuf[TILE_BYTES];
+  float (*tile)[PT + 1] = reinterpret_cast<float (*)[PT + 1]>(tbuf);
+  uint32_t* const thi = reinterpret_cast<uint32_t*>(tbuf);          // [PT][PT / 2] words
+  uint8_t* const tlo = tbuf + PT * PT * 2;                           // [PT][PT] bytes
   __shared__ float red[PREP_THREADS / 32];
   // the block's bf16 G and fp32 M tiles, staged by cp.async: every load of
   // the block is in flight at once without holding registers (the kernel
@@ -231,6 +242,20 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
           for (int k = 0; k < 8 && c + k < e.cols; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
         }
       }
+    } else if constexpr (kHiLo8) {
+      uint32_t hw[4];
+      int q[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+        hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
+        q[2 * k] = lo8_code(__float_as_uint(u[2 * k]), hw[k] << 16);
+        q[2 * k + 1] = lo8_code(__float_as_uint(u[2 * k + 1]), hw[k] & 0xFFFF0000u);
+      }
+      const int ch = tx ^ (rl >> 3);
+      *reinterpret_cast<uint4*>(thi + rl * (PT / 2) + ch * 4) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint2*>(tlo + rl * PT + ch * 8) =
+          make_uint2(pack_lo8x4(q[0], q[1], q[2], q[3]), pack_lo8x4(q[4], q[5], q[6], q[7]));
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) tile[rl][tx * 8 + k] = u[k];
@@ -239,23 +264,62 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
 
   if (e.transposed) {
     __syncthreads();
-    // X[c][r] = U[r][c]: thread (wx, wy) writes X rows c0+wy+32*pass, 8 consecutive r
-    // (16-byte hi stores; the column reads of the padded tile are free of bank conflicts)
     const int wx = threadIdx.x & 7, wy = threadIdx.x >> 3;
+    if constexpr (kHiLo8) {
+      // X[c][r] = U[r][c]: warp w takes the tile's chunk w (columns 8w ..
+      // 8w+7); lane (wx, j) reads rows 8wx .. 8wx+7 of its column pair
+      // 8w+2j, 8w+2j+1 (one word of hi, two bytes of codes a row) and writes
+      // both columns' X rows, 8 consecutive r each
+      const int ch = threadIdx.x >> 5, j = wy & 3;
+      const int sw = ch ^ wx;
+      uint32_t h[8], l[8];
 #pragma unroll
-    for (int pass = 0; pass < PT / 32; ++pass) {
-      const int cl = wy + 32 * pass;
-      const int c = c0 + cl;
+      for (int k = 0; k < 8; ++k) {
+        h[k] = thi[(wx * 8 + k) * (PT / 2) + sw * 4 + j];
+        l[k] = *reinterpret_cast<const uint16_t*>(tlo + (wx * 8 + k) * PT + sw * 8 + j * 2);
+      }
       const int r = r0 + wx * 8;
-      if (c < e.cols) {
-        float u[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) u[k] = tile[wx * 8 + k][cl];
-        const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
-        if (r + 7 < e.rows) {
-          write_x8<kHiLo8>(p, xo, u);
-        } else {
-          for (int k = 0; k < 8 && r + k < e.rows; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
+      for (int half = 0; half < 2; ++half) {
+        const int c = c0 + ch * 8 + j * 2 + half;
+        if (c < e.cols) {
+          const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
+          const uint32_t hs = half ? 0x7632u : 0x5410u;   // the high or the low bf16 of each row's word
+          const uint32_t ls = half ? 0x7531u : 0x6420u;   // the odd or the even byte of each row's pair
+          const uint4 hv = make_uint4(__byte_perm(h[0], h[1], hs), __byte_perm(h[2], h[3], hs),
+                                      __byte_perm(h[4], h[5], hs), __byte_perm(h[6], h[7], hs));
+          const uint2 lv = make_uint2(__byte_perm(__byte_perm(l[0], l[1], 0x5410u), __byte_perm(l[2], l[3], 0x5410u), ls),
+                                      __byte_perm(__byte_perm(l[4], l[5], 0x5410u), __byte_perm(l[6], l[7], 0x5410u), ls));
+          if (r + 7 < e.rows) {
+            *reinterpret_cast<uint4*>(p.xb + xo) = hv;
+            *reinterpret_cast<uint2*>(p.xlo8 + xo) = lv;
+          } else {
+            const uint32_t hh[4] = {hv.x, hv.y, hv.z, hv.w}, ll[2] = {lv.x, lv.y};
+            for (int k = 0; k < 8 && r + k < e.rows; ++k) {
+              reinterpret_cast<uint16_t*>(p.xb)[xo + k] = static_cast<uint16_t>(hh[k >> 1] >> (16 * (k & 1)));
+              reinterpret_cast<uint8_t*>(p.xlo8)[xo + k] = static_cast<uint8_t>(ll[k >> 2] >> (8 * (k & 3)));
+            }
+          }
+        }
+      }
+    } else {
+      // X[c][r] = U[r][c]: thread (wx, wy) writes X rows c0+wy+32*pass, 8 consecutive r
+      // (16-byte hi stores; the column reads of the padded tile are free of bank conflicts)
+#pragma unroll
+      for (int pass = 0; pass < PT / 32; ++pass) {
+        const int cl = wy + 32 * pass;
+        const int c = c0 + cl;
+        const int r = r0 + wx * 8;
+        if (c < e.cols) {
+          const long long xo = xbase + static_cast<long long>(c) * p.ldx + r;
+          float u[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) u[k] = tile[wx * 8 + k][cl];
+          if (r + 7 < e.rows) {
+            write_x8<kHiLo8>(p, xo, u);
+          } else {
+            for (int k = 0; k < 8 && r + k < e.rows; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
+          }
         }
       }
     }
