@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
   // the row pass stores a chunk as one 16-byte (hi) and one 8-byte (codes)
   // store, and the column pass's lanes, which read rows of eight bands at
   // once, fall in distinct banks.
+  static_assert(PT == 64 && PREP_THREADS == 256, "eight 8-row bands, eight chunks, one warp per chunk");
   constexpr int TILE_BYTES = kHiLo8 ? PT * PT * 3 : PT * (PT + 1) * 4;
   __shared__ __align__(16) uint8_t tbuf[TILE_BYTES];
   float (*tile)[PT + 1] = reinterpret_cast<float (*)[PT + 1]>(tbuf);
