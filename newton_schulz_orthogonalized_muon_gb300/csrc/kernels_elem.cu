@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
           const float4 m1 = *reinterpret_cast<const float4*>(mst + rl * PT + tx * 8 + 4);
           const float mo[8] = {fmaf(mu, m0.x, g[0]), fmaf(mu, m0.y, g[1]), fmaf(mu, m0.z, g[2]), fmaf(mu, m0.w, g[3]),
                                fmaf(mu, m1.x, g[4]), fmaf(mu, m1.y, g[5]), fmaf(mu, m1.z, g[6]), fmaf(mu, m1.w, g[7])};
-          *reinterpret_cast<float4*>(e.mom + off) = make_float4(mo[0], mo[1], mo[2], mo[3]);
-          *reinterpret_cast<float4*>(e.mom + off + 4) = make_float4(mo[4], mo[5], mo[6], mo[7]);
+          // the new momentum goes back to the staged tile and leaves below
+          *reinterpret_cast<float4*>(mst + rl * PT + tx * 8) = make_float4(mo[0], mo[1], mo[2], mo[3]);
+          *reinterpret_cast<float4*>(mst + rl * PT + tx * 8 + 4) = make_float4(mo[4], mo[5], mo[6], mo[7]);
 #pragma unroll
           for (int k = 0; k < 8; ++k) u[k] = p.nesterov ? fmaf(mu, mo[k], g[k]) : mo[k];
         } else {
@@ -263,8 +264,20 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
     }
   }
 
+  if (mstage || e.transposed) __syncthreads();
+  if (mstage) {
+    // M tile out as the loads brought it in: lane-contiguous 16-byte
+    // chunks, every 32-byte sector written by one instruction (a thread's
+    // own two 16-byte stores 32 bytes apart wrote each sector in halves)
+    for (int q = threadIdx.x; q < PT * 16; q += PREP_THREADS) {
+      const int rl = q >> 4, c = c0 + (q & 15) * 4;
+      if (r0 + rl < e.rows && c < e.cols)
+        *reinterpret_cast<float4*>(e.mom + static_cast<long long>(r0 + rl) * e.ld + c) =
+            *reinterpret_cast<const float4*>(mst + rl * PT + (q & 15) * 4);
+    }
+  }
+
   if (e.transposed) {
-    __syncthreads();
     const int wx = threadIdx.x & 7, wy = threadIdx.x >> 3;
     if constexpr (kHiLo8) {
       // X[c][r] = U[r][c]: warp w takes the tile's chunk w (columns 8w ..
