@@ -103,6 +103,33 @@ __device__ __forceinline__ void write_x8(const PrepParams& p, long long xo, cons
     }
   }
 }
+// ... of 4 consecutive values (8-byte aligned at xo)
+template <bool kHiLo8>
+__device__ __forceinline__ void write_x4(const PrepParams& p, long long xo, const float* u) {
+  if constexpr (kHiLo8) {
+    uint32_t hw[2];
+    int q[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+      hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
+      q[2 * k] = lo8_code(__float_as_uint(u[2 * k]), hw[k] << 16);
+      q[2 * k + 1] = lo8_code(__float_as_uint(u[2 * k + 1]), hw[k] & 0xFFFF0000u);
+    }
+    *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint32_t*>(p.xlo8 + xo) = pack_lo8x4(q[0], q[1], q[2], q[3]);
+  } else {
+    if (p.xf != nullptr) *reinterpret_cast<float4*>(p.xf + xo) = make_float4(u[0], u[1], u[2], u[3]);
+    if (p.xb != nullptr) {
+      uint32_t hw[2], lw[2], l2w[2];
+      split_hi_lo(u, hw, lw, 2, l2w);
+      *reinterpret_cast<uint2*>(p.xb + xo) = make_uint2(hw[0], hw[1]);
+      if (p.xlo8 != nullptr) *reinterpret_cast<uint32_t*>(p.xlo8 + xo) = lo8_word(u);
+      if (p.xlo != nullptr) *reinterpret_cast<uint2*>(p.xlo + xo) = make_uint2(lw[0], lw[1]);
+      if (p.xlo2 != nullptr) *reinterpret_cast<uint2*>(p.xlo2 + xo) = make_uint2(l2w[0], l2w[1]);
+    }
+  }
+}
 template <bool kHiLo8>
 __device__ __forceinline__ void write_x1(const PrepParams& p, long long xo, float u) {
   if (!kHiLo8 && p.xf != nullptr) p.xf[xo] = u;
@@ -112,15 +139,23 @@ __device__ __forceinline__ void write_x1(const PrepParams& p, long long xo, floa
   if (kHiLo8 || p.xlo8 != nullptr) p.xlo8[xo] = static_cast<int8_t>(lo8_of(u));
 }
 
+// Shared-memory placements of the prepare kernel (tile row rl, 8-column
+// chunk ch, column lc): the staged G tile's 16-byte chunks swap halves on
+// odd rows; the bf16 path's transpose tile orders a row's chunks by XOR
+// with its 8-row band and with its parity (hi bits) or its second bit
+// (codes).  The row pass's 8-byte reads and its 8- and 4-byte tile stores,
+// and the column pass's reads of eight bands at once, then fall in
+// distinct banks.
+__device__ __forceinline__ int gst_col(int rl, int lc) { return (((lc >> 3) ^ ((rl & 1) << 2)) << 3) | (lc & 7); }
+__device__ __forceinline__ int hi_chunk(int rl, int ch) { return ch ^ (rl >> 3) ^ ((rl & 1) << 2); }
+__device__ __forceinline__ int lo_chunk(int rl, int ch) { return ch ^ (rl >> 3) ^ ((rl & 2) << 1); }
+
 template <bool kHiLo8>
 __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p) {
   // transpose tile: fp32 U (padded rows) for the generic instance; for the
   // bf16 path the encoded hi bits (64 x 64 bf16) and lo codes (64 x 64
-  // bytes), 12 KB, so six blocks fit on an SM.  Their rows are split into
-  // eight 8-column chunks whose order is XORed with the row's 8-row band:
-  // the row pass stores a chunk as one 16-byte (hi) and one 8-byte (codes)
-  // store, and the column pass's lanes, which read rows of eight bands at
-  // once, fall in distinct banks.
+  // bytes), 12 KB, so six blocks fit on an SM; their chunks placed by
+  // hi_chunk / lo_chunk.
   static_assert(PT == 64 && PREP_THREADS == 256, "eight 8-row bands, eight chunks, one warp per chunk");
   constexpr int TILE_BYTES = kHiLo8 ? PT * PT * 3 : PT * (PT + 1) * 4;
   __shared__ __align__(16) uint8_t tbuf[TILE_BYTES];
@@ -143,7 +178,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
   const int tiles_x = (e.cols + PT - 1) / PT;
   const int r0 = (blockIdx.x / tiles_x) * PT;
   const int c0 = (blockIdx.x % tiles_x) * PT;
-  const int tx = threadIdx.x & 7;   // 8-column group
+  const int tx = threadIdx.x & 7;   // column-group lane of a row
   const int ty = threadIdx.x >> 3;  // row within a 32-row pass
   const float mu = p.mu;
   const bool vec = ((e.cols & 7) == 0) && ((e.ld & 7) == 0) &&
@@ -160,7 +195,7 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
       for (int q = threadIdx.x; q < PT * 8; q += PREP_THREADS) {
         const int rl = q >> 3, c = c0 + (q & 7) * 8;
         if (r0 + rl < e.rows && c < e.cols)
-          cp_async16(gst + rl * PT + (q & 7) * 8,
+          cp_async16(gst + rl * PT + gst_col(rl, (q & 7) * 8),
                      reinterpret_cast<const __nv_bfloat16*>(e.g) + static_cast<long long>(r0 + rl) * e.ld + c);
       }
     }
@@ -175,108 +210,94 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
     __syncthreads();
   }
 
+  // Row pass: thread (tx, ty) takes tile rows ty and ty + 32 and, in each,
+  // the 4-column groups from 4tx and 32 + 4tx, so that the 8 lanes of a row
+  // store contiguous segments (M 128 bytes, X hi 64, X codes 32) and every
+  // 32-byte sector is written by one instruction.
 #pragma unroll
   for (int pass = 0; pass < PT / 32; ++pass) {
     const int rl = ty + 32 * pass;
     const int r = r0 + rl;
-    const int c = c0 + tx * 8;
-    float u[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) u[k] = 0.f;
-    if (r < e.rows) {
-      const long long off = static_cast<long long>(r) * e.ld + c;
-      if (vec && c + 7 < e.cols) {
-        float g[8];
-        if (e.gdtype == DT_BF16) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(gst + rl * PT + tx * 8);
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    for (int gi = 0; gi < 2; ++gi) {
+      const int lc = 32 * gi + 4 * tx;
+      const int c = c0 + lc;
+      float u[4] = {0.f, 0.f, 0.f, 0.f};
+      if (r < e.rows) {
+        const long long off = static_cast<long long>(r) * e.ld + c;
+        if (vec) {
+          if (c < e.cols) {   // cols % 8 == 0: a group that starts inside ends inside
+            float g[4];
+            if (e.gdtype == DT_BF16) {
+              const uint2 raw = *reinterpret_cast<const uint2*>(gst + rl * PT + gst_col(rl, lc));
+              const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+              const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+              g[0] = f0.x; g[1] = f0.y; g[2] = f1.x; g[3] = f1.y;
+            } else {
+              const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off);
+              g[0] = f.x; g[1] = f.y; g[2] = f.z; g[3] = f.w;
+            }
+            if (e.mom != nullptr) {
+              const float4 m = *reinterpret_cast<const float4*>(mst + rl * PT + lc);
+              const float mo[4] = {fmaf(mu, m.x, g[0]), fmaf(mu, m.y, g[1]), fmaf(mu, m.z, g[2]), fmaf(mu, m.w, g[3])};
+              *reinterpret_cast<float4*>(e.mom + off) = make_float4(mo[0], mo[1], mo[2], mo[3]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __bfloat1622float2(h[k]);
-            g[2 * k] = f.x;
-            g[2 * k + 1] = f.y;
+              for (int k = 0; k < 4; ++k) u[k] = p.nesterov ? fmaf(mu, mo[k], g[k]) : mo[k];
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) u[k] = g[k];
+            }
           }
         } else {
-          const float4 f0 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off);
-          const float4 f1 = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(e.g) + off + 4);
-          g[0] = f0.x; g[1] = f0.y; g[2] = f0.z; g[3] = f0.w; g[4] = f1.x; g[5] = f1.y; g[6] = f1.z; g[7] = f1.w;
-        }
-        if (e.mom != nullptr) {
-          const float4 m0 = *reinterpret_cast<const float4*>(mst + rl * PT + tx * 8);
-          const float4 m1 = *reinterpret_cast<const float4*>(mst + rl * PT + tx * 8 + 4);
-          const float mo[8] = {fmaf(mu, m0.x, g[0]), fmaf(mu, m0.y, g[1]), fmaf(mu, m0.z, g[2]), fmaf(mu, m0.w, g[3]),
-                               fmaf(mu, m1.x, g[4]), fmaf(mu, m1.y, g[5]), fmaf(mu, m1.z, g[6]), fmaf(mu, m1.w, g[7])};
-          // the new momentum goes back to the staged tile and leaves below
-          *reinterpret_cast<float4*>(mst + rl * PT + tx * 8) = make_float4(mo[0], mo[1], mo[2], mo[3]);
-          *reinterpret_cast<float4*>(mst + rl * PT + tx * 8 + 4) = make_float4(mo[4], mo[5], mo[6], mo[7]);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = p.nesterov ? fmaf(mu, mo[k], g[k]) : mo[k];
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = g[k];
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (c + k < e.cols) {
-            const float gv = load_as_f32(e.g, off + k, e.gdtype);
-            if (e.mom != nullptr) {
-              const float mv = fmaf(mu, e.mom[off + k], gv);
-              e.mom[off + k] = mv;
-              u[k] = p.nesterov ? fmaf(mu, mv, gv) : mv;
-            } else {
-              u[k] = gv;
+          for (int k = 0; k < 4; ++k) {
+            if (c + k < e.cols) {
+              const float gv = load_as_f32(e.g, off + k, e.gdtype);
+              if (e.mom != nullptr) {
+                const float mv = fmaf(mu, e.mom[off + k], gv);
+                e.mom[off + k] = mv;
+                u[k] = p.nesterov ? fmaf(mu, mv, gv) : mv;
+              } else {
+                u[k] = gv;
+              }
             }
           }
         }
       }
-    }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ss = fmaf(u[k], u[k], ss);
+      for (int k = 0; k < 4; ++k) ss = fmaf(u[k], u[k], ss);
 
-    if (!e.transposed) {
-      // NS orientation == parameter orientation: X[r][c]
-      if (r < e.rows) {
-        const long long xo = xbase + static_cast<long long>(r) * p.ldx + c;
-        if (c + 7 < e.cols) {
-          write_x8<kHiLo8>(p, xo, u);
-        } else {
-          for (int k = 0; k < 8 && c + k < e.cols; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
+      if (!e.transposed) {
+        // NS orientation == parameter orientation: X[r][c]
+        if (r < e.rows) {
+          const long long xo = xbase + static_cast<long long>(r) * p.ldx + c;
+          if (c + 3 < e.cols) {
+            write_x4<kHiLo8>(p, xo, u);
+          } else {
+            for (int k = 0; k < 4 && c + k < e.cols; ++k) write_x1<kHiLo8>(p, xo + k, u[k]);
+          }
         }
-      }
-    } else if constexpr (kHiLo8) {
-      uint32_t hw[4];
-      int q[8];
+      } else if constexpr (kHiLo8) {
+        uint32_t hw[2];
+        int q[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
-        hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
-        q[2 * k] = lo8_code(__float_as_uint(u[2 * k]), hw[k] << 16);
-        q[2 * k + 1] = lo8_code(__float_as_uint(u[2 * k + 1]), hw[k] & 0xFFFF0000u);
-      }
-      const int ch = tx ^ (rl >> 3);
-      *reinterpret_cast<uint4*>(thi + rl * (PT / 2) + ch * 4) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint2*>(tlo + rl * PT + ch * 8) =
-          make_uint2(pack_lo8x4(q[0], q[1], q[2], q[3]), pack_lo8x4(q[4], q[5], q[6], q[7]));
-    } else {
+        for (int k = 0; k < 2; ++k) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+          hw[k] = *reinterpret_cast<const uint32_t*>(&h2);
+          q[2 * k] = lo8_code(__float_as_uint(u[2 * k]), hw[k] << 16);
+          q[2 * k + 1] = lo8_code(__float_as_uint(u[2 * k + 1]), hw[k] & 0xFFFF0000u);
+        }
+        const int ch = lc >> 3, sub = tx & 1;     // the group is half `sub` of chunk ch
+        *reinterpret_cast<uint2*>(thi + rl * (PT / 2) + hi_chunk(rl, ch) * 4 + sub * 2) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint32_t*>(tlo + rl * PT + lo_chunk(rl, ch) * 8 + sub * 4) = pack_lo8x4(q[0], q[1], q[2], q[3]);
+      } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) tile[rl][tx * 8 + k] = u[k];
+        for (int k = 0; k < 4; ++k) tile[rl][lc + k] = u[k];
+      }
     }
   }
 
-  if (mstage || e.transposed) __syncthreads();
-  if (mstage) {
-    // M tile out as the loads brought it in: lane-contiguous 16-byte
-    // chunks, every 32-byte sector written by one instruction (a thread's
-    // own two 16-byte stores 32 bytes apart wrote each sector in halves)
-    for (int q = threadIdx.x; q < PT * 16; q += PREP_THREADS) {
-      const int rl = q >> 4, c = c0 + (q & 15) * 4;
-      if (r0 + rl < e.rows && c < e.cols)
-        *reinterpret_cast<float4*>(e.mom + static_cast<long long>(r0 + rl) * e.ld + c) =
-            *reinterpret_cast<const float4*>(mst + rl * PT + (q & 15) * 4);
-    }
-  }
-
+  if (e.transposed) __syncthreads();
   if (e.transposed) {
     const int wx = threadIdx.x & 7, wy = threadIdx.x >> 3;
     if constexpr (kHiLo8) {
@@ -285,12 +306,12 @@ __global__ void __launch_bounds__(PREP_THREADS) muon_prepare_kernel(PrepParams p
       // 8w+2j, 8w+2j+1 (one word of hi, two bytes of codes a row) and writes
       // both columns' X rows, 8 consecutive r each
       const int ch = threadIdx.x >> 5, j = wy & 3;
-      const int sw = ch ^ wx;
       uint32_t h[8], l[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        h[k] = thi[(wx * 8 + k) * (PT / 2) + sw * 4 + j];
-        l[k] = *reinterpret_cast<const uint16_t*>(tlo + (wx * 8 + k) * PT + sw * 8 + j * 2);
+        const int R = wx * 8 + k;
+        h[k] = thi[R * (PT / 2) + hi_chunk(R, ch) * 4 + j];
+        l[k] = *reinterpret_cast<const uint16_t*>(tlo + R * PT + lo_chunk(R, ch) * 8 + j * 2);
       }
       const int r = r0 + wx * 8;
 #pragma unroll
